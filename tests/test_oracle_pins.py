@@ -1,0 +1,407 @@
+"""Pins for the CPU oracle: each check ties the oracle to something other
+than itself — hand-derived fixtures under tests/golden/, closed forms,
+exhaustive tables, brute force over a whole 16-bit format, invariants of the
+quantiser, and library routines (numpy matmul, scipy expit, numpy float16).
+
+A plausible slip in the oracle (a dropped term, a wrong sign, a transposed
+operand, a wrong rounding tie, a swapped gate/up) fails at least one test.
+"""
+import bisect
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+from scipy.special import expit
+
+import oracle
+from bit_weight_only_mxfp4_gb300 import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    out = []
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                out.append(line.split())
+    return out
+
+
+# ---------------------------------------------------------------- E2M1/E8M0
+def test_e2m1_table_exhaustive():
+    for code, val in _rows("e2m1_values.txt"):
+        got = oracle.e2m1_value(int(code))
+        assert got == float(val)
+        assert math.copysign(1.0, got) == math.copysign(1.0, float(val))
+
+
+def test_e2m1_encode_roundtrip_all_codes():
+    for c in range(16):
+        assert oracle.e2m1_encode(oracle.e2m1_value(c)) == c
+
+
+def test_e2m1_rne_ties_and_saturation():
+    for t, code in _rows("e2m1_rne_ties.txt"):
+        assert oracle.e2m1_encode(float(t)) == int(code), t
+    # just off every midpoint the nearest value wins
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    lo_code = [0, 1, 2, 3, 4, 5, 6]
+    for mid, lo in zip(mids, lo_code):
+        assert oracle.e2m1_encode(np.nextafter(mid, 0.0)) == lo
+        assert oracle.e2m1_encode(np.nextafter(mid, 10.0)) == lo + 1
+    for t in [6.0, 6.5, 7.0, 7.999999, 8.0, 100.0, 1e300]:
+        assert oracle.e2m1_encode(t) == 7
+        assert oracle.e2m1_encode(-t) == 15
+
+
+def test_e8m0_closed_form():
+    assert oracle.e8m0_value(0) == 2.0 ** -127
+    assert oracle.e8m0_value(127) == 1.0
+    assert oracle.e8m0_value(254) == 2.0 ** 127
+    assert math.isnan(oracle.e8m0_value(255))
+    for b in range(255):
+        assert oracle.e8m0_value(b) == math.ldexp(1.0, b - 127)
+
+
+def test_floor_log2_at_powers_of_two_and_neighbours():
+    # exponent read off the bits, not a rounded log2
+    for e in range(-149, 128):
+        a = np.float32(2.0 ** e)
+        assert oracle.floor_log2(a) == e
+        up = np.nextafter(a, np.float32(np.inf))
+        if np.isfinite(up) and e > -149:  # 2^-149 + ulp is 2^-148
+            assert oracle.floor_log2(up) == e
+        if e > -149:
+            dn = np.nextafter(a, np.float32(0))
+            assert oracle.floor_log2(dn) == e - 1
+
+
+# ------------------------------------------------------ 16-bit float formats
+def _all_finite(fmt):
+    """Every finite value of a 16-bit format as (Fraction, bits)."""
+    bits = np.arange(65536, dtype=np.uint32)
+    if fmt == "bf16":
+        vals = (bits << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    else:
+        vals = bits.astype(np.uint16).view(np.float16).astype(np.float64)
+    pairs = [(Fraction(float(v)), int(b)) for v, b in zip(vals, bits)
+             if np.isfinite(v) and not (v == 0 and b & 0x8000)]
+    pairs.sort()
+    return pairs
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+def test_16bit_round_brute_force(fmt):
+    pairs = _all_finite(fmt)
+    keys = [p[0] for p in pairs]
+    top = pairs[-1][0]
+    nxt_pow = Fraction(2) ** (128 if fmt == "bf16" else 16)
+    overflow_at = (top + nxt_pow) / 2  # midpoint between max and 2^emax+1
+    g = np.random.default_rng(7)
+    probes = list(g.standard_normal(400) * 10.0 ** g.integers(-8, 8, 400))
+    # exact midpoints between neighbours, and their float neighbours
+    for i in g.integers(0, len(pairs) - 1, 300):
+        mid = (keys[i] + keys[i + 1]) / 2
+        m = float(mid)
+        probes += [m, np.nextafter(m, -np.inf), np.nextafter(m, np.inf)]
+    probes += [float(overflow_at), float(overflow_at) * (1 - 1e-12)]
+    rnd = oracle.bf16_round if fmt == "bf16" else oracle.f16_round
+    for v in probes:
+        fv = Fraction(float(v))
+        a = abs(fv)
+        if a >= overflow_at:
+            want = 0x7F80 if fmt == "bf16" else 0x7C00
+        else:
+            j = bisect.bisect_left(keys, a)
+            cands = [pairs[c] for c in (j - 1, j) if 0 <= c < len(pairs)]
+            cands.sort(key=lambda p: (abs(p[0] - a), p[1] & 1))
+            want = cands[0][1]
+        if v < 0 or (v == 0 and math.copysign(1, v) < 0):
+            want |= 0x8000
+        assert rnd(float(v)) == want, (fmt, v)
+
+
+def test_f16_value_all_patterns_vs_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_value(int(b)) for b in bits])
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.all(both_nan | (ref == got))
+    assert np.all(np.signbit(ref[~both_nan]) == np.signbit(got[~both_nan]))
+
+
+def test_f16_round_vs_numpy_library():
+    g = np.random.default_rng(3)
+    v = g.standard_normal(5000) * 10.0 ** g.integers(-9, 6, 5000)
+    want = v.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.f16_round(float(t)) for t in v], np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_bf16_value_closed_form():
+    for b in [0x0000, 0x3F80, 0xBF80, 0x4000, 0x0001, 0x7F7F, 0x3E80]:
+        want = np.array([b << 16], np.uint32).view(np.float32)[0]
+        assert oracle.bf16_value(b) == float(want)
+
+
+# -------------------------------------------------------------------- MXFP4
+def test_mxfp4_worked_block():
+    rows = _rows("mxfp4_worked_block.txt")
+    scale = int(rows[0][1])
+    vals = [r for r in rows[1:]]
+    assert len(vals) == 32
+    w = np.array([[float(r[0]) for r in vals]], np.float32)
+    # t column is 16 w by construction
+    for r in vals:
+        assert float(r[1]) == 16.0 * float(r[0])
+    codes, scales, st = oracle.mxfp4_quantize(w)
+    assert st == oracle.OK
+    assert scales[0, 0] == scale
+    got = [(codes[0, i // 2] >> (4 * (i % 2))) & 15 for i in range(32)]
+    assert got == [int(r[2]) for r in vals]
+
+
+def _rand_w(g, n, k, std=0.02):
+    return (g.standard_normal((n, k)) * std).astype(np.float32)
+
+
+def test_mxfp4_power_of_two_invariance():
+    g = np.random.default_rng(11)
+    w = _rand_w(g, 23, 96)
+    c0, s0, _ = oracle.mxfp4_quantize(w)
+    for j in [-20, -7, -1, 1, 3, 20]:
+        c1, s1, st = oracle.mxfp4_quantize((w * np.float32(2.0 ** j)).astype(np.float32))
+        assert st == oracle.OK
+        assert np.array_equal(c0, c1)
+        assert np.array_equal(s1.astype(int), s0.astype(int) + j)
+
+
+def test_mxfp4_quantize_is_idempotent_on_its_grid():
+    g = np.random.default_rng(12)
+    n, k = 17, 128
+    codes = synth.random_bytes(g, (n, k // 2))
+    # every block holds at least one code of magnitude >= 4, so its amax
+    # sits in the top binade and the scale is recovered exactly
+    for r in range(n):
+        for b in range(k // 32):
+            codes[r, b * 16] = (codes[r, b * 16] & 0xF0) | 0x06 | (g.integers(0, 2) << 3)
+    scales = g.integers(1, 250, size=(n, k // 32), dtype=np.uint8)
+    deq = oracle.mxfp4_dequantize(codes, scales).astype(np.float32)
+    c2, s2, st = oracle.mxfp4_quantize(deq)
+    assert st == oracle.OK
+    assert np.array_equal(s2, scales)
+    # -0 and +0 dequantise to signed zeros, which requantise to 8 and 0
+    assert np.array_equal(c2, codes)
+
+
+def test_mxfp4_error_bound():
+    g = np.random.default_rng(13)
+    w = _rand_w(g, 31, 160)
+    codes, scales, _ = oracle.mxfp4_quantize(w)
+    deq = oracle.mxfp4_dequantize(codes, scales)
+    X = np.repeat(scales.astype(np.int64) - 127, 32, axis=1)
+    t = np.abs(w.astype(np.float64)) / np.ldexp(1.0, X)
+    half_gap = np.where(t <= 2, 0.25, np.where(t <= 4, 0.5, np.where(t <= 6, 1.0, 2.0)))
+    assert np.all(np.abs(deq - w) <= half_gap * np.ldexp(1.0, X))
+    # the block maximum always lands in [4, 8) before rounding
+    amax = np.abs(w).reshape(31, 5, 32).max(axis=2)
+    ratio = amax / np.ldexp(1.0, scales.astype(np.int64) - 127)
+    assert np.all((ratio >= 4) & (ratio < 8))
+
+
+def test_mxfp4_zero_and_nonfinite_blocks():
+    w = np.zeros((2, 64), np.float32)
+    w[0, 1] = -0.0
+    w[1, 40] = np.nan
+    w[1, 5] = 0.5
+    codes, scales, st = oracle.mxfp4_quantize(w)
+    assert st == oracle.ERR_NONFINITE
+    assert scales[0, 0] == 0 and scales[0, 1] == 0
+    assert codes[0, 0] == 0x80  # +0 (even k), -0 (odd k)
+    assert scales[1, 1] == 0xFF and np.all(codes[1, 16:] == 0)
+    assert scales[1, 0] == 124  # amax 0.5 -> X = -3
+    assert (codes[1, 2] >> 4) == 6  # 0.5 / 2^-3 = 4 -> code 6
+
+
+def test_mxfp4_identity_matrix():
+    k = 64
+    w = np.eye(k, dtype=np.float32)
+    codes, scales, _ = oracle.mxfp4_quantize(w)
+    assert np.array_equal(oracle.mxfp4_dequantize(codes, scales), np.eye(k))
+    g = np.random.default_rng(5)
+    x = synth.normal_bf16(g, (2, k))
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    y = oracle.mxfp4_matvec(codes, scales, None, x)
+    assert np.array_equal(y, xf)
+    h = oracle.mxfp4_swiglu_matvec((codes, scales, None), (codes, scales, None), x)
+    np.testing.assert_allclose(h, xf * expit(xf) * xf, rtol=1e-14, atol=0)
+
+
+def test_mxfp4_matvec_equals_dense_dot_ragged():
+    g = np.random.default_rng(14)
+    n, k, m = 37, 96, 3
+    w = _rand_w(g, n, k)
+    codes, scales, _ = oracle.mxfp4_quantize(w)
+    ps = synth.uniform_f32(g, (n,), 0.9, 1.1)
+    x = synth.normal_bf16(g, (m, k))
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    deq = oracle.mxfp4_dequantize(codes, scales)
+    want = (xf @ deq.T) * ps.astype(np.float64)[None, :]
+    got = oracle.mxfp4_matvec(codes, scales, ps, x)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-15)
+    # one-hot rows pick x at the right column (catches a transposed operand)
+    oh = np.zeros((5, k), np.float32)
+    cols = [0, 31, 32, 63, 95]
+    for r, c in enumerate(cols):
+        oh[r, c] = 1.0
+    c1, s1, _ = oracle.mxfp4_quantize(oh)
+    y1 = oracle.mxfp4_matvec(c1, s1, None, x)
+    assert np.array_equal(y1, xf[:, cols])
+
+
+def test_swiglu_against_expit_and_gate_up_order():
+    g = np.random.default_rng(15)
+    a = g.standard_normal(1000) * 4
+    b = g.standard_normal(1000)
+    np.testing.assert_allclose(oracle.swiglu(a, b), a * expit(a) * b, rtol=1e-14)
+    # silu(g)*u is not symmetric in g and u
+    assert not np.allclose(oracle.swiglu(a, b), oracle.swiglu(b, a))
+    n, k = 19, 64
+    wg, wu = _rand_w(g, n, k), _rand_w(g, n, k)
+    cg, sg, _ = oracle.mxfp4_quantize(wg)
+    cu, su, _ = oracle.mxfp4_quantize(wu)
+    pg = synth.uniform_f32(g, (n,), 0.9, 1.1)
+    pu = synth.uniform_f32(g, (n,), 0.9, 1.1)
+    x = synth.normal_bf16(g, (1, k))
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)[0]
+    gv = oracle.mxfp4_dequantize(cg, sg) @ xf * pg
+    uv = oracle.mxfp4_dequantize(cu, su) @ xf * pu
+    h = oracle.mxfp4_swiglu_matvec((cg, sg, pg), (cu, su, pu), x)[0]
+    np.testing.assert_allclose(h, gv * expit(gv) * uv, rtol=1e-12, atol=1e-18)
+
+
+def test_bf16_swiglu_vs_numpy():
+    g = np.random.default_rng(16)
+    n, k = 13, 40
+    wg = synth.normal_bf16(g, (n, k), 0.02)
+    wu = synth.normal_bf16(g, (n, k), 0.02)
+    x = synth.normal_bf16(g, (2, k))
+    f = lambda a: synth.bf16_bits_to_f32(a).astype(np.float64)
+    gv = f(x) @ f(wg).T
+    uv = f(x) @ f(wu).T
+    np.testing.assert_allclose(oracle.bf16_matvec(wg, x), gv, rtol=1e-13, atol=1e-16)
+    np.testing.assert_allclose(oracle.bf16_swiglu_matvec(wg, wu, x),
+                               gv * expit(gv) * uv, rtol=1e-12, atol=1e-18)
+
+
+# ---------------------------------------------------------------------- MoE
+def test_topk_known_order_and_ties():
+    lg = np.array([0.1, 0.5, 0.5, -1.0, 0.3, 0.5, 0.3], np.float32)
+    assert list(oracle.topk(lg, 4)) == [1, 2, 5, 4]
+    assert list(oracle.topk(lg, 7)) == [1, 2, 5, 4, 6, 0, 3]
+    assert list(oracle.topk(np.zeros(8, np.float32), 3)) == [0, 1, 2]
+
+
+def test_softmax_selected_closed_forms():
+    lg = np.array([0.0, math.log(3.0), 7.0], np.float32)
+    p = oracle.softmax_selected(lg, np.array([0, 1], np.int32))
+    np.testing.assert_allclose(p, [1 / (1 + 3.0000001192), 3.0000001192 / (1 + 3.0000001192)], rtol=1e-7)
+    p4 = oracle.softmax_selected(np.full(6, 2.5, np.float32), np.array([5, 1, 2, 0], np.int32))
+    np.testing.assert_allclose(p4, [0.25] * 4, rtol=0, atol=1e-16)
+    g = np.random.default_rng(17)
+    lg = g.standard_normal(32).astype(np.float32)
+    idx = oracle.topk(lg, 4)
+    p = oracle.softmax_selected(lg, idx)
+    assert abs(p.sum() - 1.0) < 1e-15
+    assert np.all(np.diff(p) <= 0)
+
+
+def test_moe_composite_vs_numpy():
+    g = np.random.default_rng(18)
+    E, H, I, K = 6, 64, 96, 3
+    x = synth.normal_bf16(g, (H,))
+    wr = synth.normal_bf16(g, (E, H), 0.02)
+    gu = [_rand_w(g, 2 * I, H) for _ in range(E)]
+    dn = [_rand_w(g, H, I) for _ in range(E)]
+    q_gu = [oracle.mxfp4_quantize(a)[:2] for a in gu]
+    q_dn = [oracle.mxfp4_quantize(a)[:2] for a in dn]
+    gc = np.stack([q[0] for q in q_gu]); gs = np.stack([q[1] for q in q_gu])
+    dc = np.stack([q[0] for q in q_dn]); ds = np.stack([q[1] for q in q_dn])
+    out, idx, p, lg32, st = oracle.moe_mlp(x, wr, K, gc, gs, dc, ds)
+    assert st == oracle.OK
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    logits = synth.bf16_bits_to_f32(wr).astype(np.float64) @ xf
+    np.testing.assert_allclose(oracle.router_logits(x, wr), logits, rtol=1e-13)
+    assert np.array_equal(lg32, logits.astype(np.float32))
+    order = sorted(range(E), key=lambda e: (-float(lg32[e]), e))[:K]
+    assert list(idx) == order
+    sel = lg32[order].astype(np.float64)
+    pw = np.exp(sel - sel.max()); pw /= pw.sum()
+    np.testing.assert_allclose(p, pw, rtol=1e-14)
+    want = np.zeros(H)
+    for j, e in enumerate(order):
+        dgu = oracle.mxfp4_dequantize(gc[e], gs[e])
+        gv, uv = dgu[:I] @ xf, dgu[I:] @ xf
+        hv = gv * expit(gv) * uv
+        want += pw[j] * (oracle.mxfp4_dequantize(dc[e], ds[e]) @ hv)
+    np.testing.assert_allclose(out, want, rtol=1e-11, atol=1e-15)
+
+
+# --------------------------------------------------------------------- INT4
+def test_int4_worked_groups():
+    rows = _rows("int4_worked_groups.txt")
+    meta = [r for r in rows if r[0].startswith("group_")]
+    vals = [r for r in rows if not r[0].startswith("group_")]
+    w = np.array([[float(r[0]) for r in vals]], np.float32)
+    codes, scales, zp, st = oracle.int4_quantize(w, 8)
+    assert st == oracle.OK
+    for key, grp, val in meta:
+        if key == "group_scale_bits":
+            assert scales[0, int(grp)] == int(val)
+        else:
+            assert (zp[0, int(grp) // 2] >> (4 * (int(grp) % 2))) & 15 == int(val)
+    q = [(codes[0, i // 2] >> (4 * (i % 2))) & 15 for i in range(12)]
+    assert q == [int(r[1]) for r in vals]
+    assert oracle.f16_value(10854) == 1.599609375 * 2.0 ** -5
+
+
+def test_int4_error_bound_and_partial_group_stats():
+    g = np.random.default_rng(19)
+    n, k, G = 9, 2880, 128
+    w = _rand_w(g, n, k)
+    w[3, 2816:] *= 25.0  # the 64-wide last group has its own range
+    codes, scales, zp, st = oracle.int4_quantize(w, G)
+    assert st == oracle.OK and scales.shape == (n, 23) and zp.shape == (n, 12)
+    assert np.all(zp[:, 11] >> 4 == 0)  # the unused high nibble stays 0
+    deq = oracle.int4_dequantize(codes, scales, zp, G)
+    s = np.repeat(np.array([[oracle.f16_value(int(b)) for b in row] for row in scales]), G, axis=1)[:, :k]
+    assert np.all(np.abs(deq - w) <= s / 2 * (1 + 1e-12))
+    last = w[3, 2816:]
+    assert oracle.f16_value(int(scales[3, 22])) == pytest.approx((last.max() - last.min()) / 15, rel=1e-3)
+    assert oracle.f16_value(int(scales[3, 21])) < oracle.f16_value(int(scales[3, 22])) / 5
+
+
+def test_int4_degenerate_and_nonfinite_groups():
+    w = np.zeros((1, 256), np.float32)
+    w[0, :128] = 0.75          # constant group: s = 0, q = zp = 0
+    w[0, 200] = np.inf
+    codes, scales, zp, st = oracle.int4_quantize(w, 128)
+    assert st == oracle.ERR_NONFINITE
+    assert scales[0, 0] == 0 and (zp[0, 0] & 15) == 0 and np.all(codes[0, :64] == 0)
+    assert scales[0, 1] == 0x7E00 and np.all(codes[0, 64:] == 0)
+
+
+def test_int4_matvec_equals_dense_dot():
+    g = np.random.default_rng(20)
+    n, k, G = 21, 320, 128  # last group 64
+    w = _rand_w(g, n, k)
+    codes, scales, zp, _ = oracle.int4_quantize(w, G)
+    x = synth.normal_bf16(g, (2, k))
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    want = xf @ oracle.int4_dequantize(codes, scales, zp, G).T
+    np.testing.assert_allclose(oracle.int4_matvec(codes, scales, zp, G, x), want,
+                               rtol=1e-12, atol=1e-15)
