@@ -1,0 +1,472 @@
+"""Benchmark of the weight-only MXFP4 decode matvec path on one GB300.
+
+One step = one pass of the SmolLM3-3B-shaped gate/up stack at batch 1:
+24 MXFP4 gate/up SwiGLU layers (K=2048, N=11008, fp32 row postscale) and
+12 bf16 gate/up SwiGLU layers, each layer with its own weights and its own
+bf16 activation vector.  The stack's weights (1.66 GB) exceed L2 many times,
+so every step streams from HBM.
+
+Prints one JSON line.  `value` is the stack's algorithmic weight traffic per
+second (GB/s); per-layer microseconds, the roofline fraction of the dominant
+kernel, the other workloads (single layer, batch sweep, ...) and the CPU
+oracle baseline ride along in the same line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl thinmx|reference]
+
+Under torchrun (N > 1) each rank runs an independent replica (the path has no
+exchange step); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------------------
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            hbm = d.get("hbm_gbs") or d.get("hbm_GBs")
+            if hbm:
+                return float(hbm), "measured", d
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback", {}
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def build_stack(torch, synth, loader, cfg, device):
+    """Device-resident weights of the 36-layer stack (seeded synthetic draws)."""
+    layers = []
+    for l in range(cfg.layers):
+        x = synth.torch_normal((1, cfg.k), 1.0, cfg.wid, l, 2, device).to(torch.bfloat16)
+        h = torch.empty((1, cfg.n), dtype=torch.bfloat16, device=device)
+        if l < cfg.mxfp4_layers:
+            wg = synth.torch_normal((cfg.n, cfg.k), synth.WEIGHT_STD, cfg.wid, l, 0, device)
+            wu = synth.torch_normal((cfg.n, cfg.k), synth.WEIGHT_STD, cfg.wid, l, 1, device)
+            pg = synth.torch_uniform((cfg.n,), 0.9, 1.1, cfg.wid, l, 3, device)
+            pu = synth.torch_uniform((cfg.n,), 0.9, 1.1, cfg.wid, l, 4, device)
+            packed = loader.mxfp4_gate_up_from_f32(wg, wu, pg, pu)
+            del wg, wu
+            layers.append(("mxfp4", packed, x, h))
+        else:
+            wg = synth.torch_normal((cfg.n, cfg.k), synth.WEIGHT_STD, cfg.wid, l, 0,
+                                    device).to(torch.bfloat16)
+            wu = synth.torch_normal((cfg.n, cfg.k), synth.WEIGHT_STD, cfg.wid, l, 1,
+                                    device).to(torch.bfloat16)
+            layers.append(("bf16", (wg, wu), x, h))
+    torch.cuda.synchronize()
+    return layers
+
+
+def run_layer(thinmx, cfg, layer, x=None, h=None):
+    kind, w, x0, h0 = layer
+    x = x0 if x is None else x
+    h = h0 if h is None else h
+    if kind == "mxfp4":
+        thinmx.tt_mxfp4_swiglu_matvec(w, cfg.n, cfg.k, x, 1, h)
+    else:
+        thinmx.tt_bf16_swiglu_matvec(w[0], w[1], cfg.n, cfg.k, x, 1, h)
+
+
+def capture(torch, fn):
+    fn()  # eager warm-up (sets kernel attributes outside capture)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(torch, g, reps, warm=3):
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps  # ms per replay
+
+
+def stack_bytes(cfg):
+    mx = 2 * (cfg.n * cfg.k // 2 + cfg.n * cfg.k // 32 + 4 * cfg.n) + 2 * cfg.k + 2 * cfg.n
+    bf = 2 * (cfg.n * cfg.k * 2) + 2 * cfg.k + 2 * cfg.n
+    return mx, bf
+
+
+def gate_up_bytes(n, k, m, postscale=True):
+    return 2 * (n * k // 2 + n * k // 32 + (4 * n if postscale else 0)) + 2 * m * k + 2 * m * n
+
+
+# ---------------------------------------------------------------------------
+def cpu_baseline(target_s: float = 10.0, rows=None):
+    """The fp64 CPU oracle, as it stands, on a bounded sample of the stack:
+    one MXFP4 layer and one bf16 layer (rows of each), run alternately until
+    about target_s seconds of oracle time have been spent."""
+    import oracle
+    from bit_weight_only_mxfp4_gb300 import synth
+    cfg = synth.STACK
+    rows = rows or cfg.n
+    d = synth.gate_up_inputs(cfg.wid, 0, rows, cfg.k)
+    gc, gs, _ = oracle.mxfp4_quantize(d["wg"])
+    uc, us, _ = oracle.mxfp4_quantize(d["wu"])
+    db = synth.bf16_gate_up_inputs(cfg.wid, cfg.mxfp4_layers, rows, cfg.k)
+    mx_bytes = gate_up_bytes(rows, cfg.k, 1)
+    bf_bytes = 2 * rows * cfg.k * 2 + 2 * cfg.k + 2 * rows
+    t_total, bytes_total, calls = 0.0, 0, 0
+    while t_total < target_s or calls < 2:
+        t0 = time.perf_counter()
+        oracle.mxfp4_swiglu_matvec((gc, gs, d["pg"]), (uc, us, d["pu"]), d["x"])
+        oracle.bf16_swiglu_matvec(db["wg"], db["wu"], db["x"])
+        t_total += time.perf_counter() - t0
+        bytes_total += mx_bytes + bf_bytes
+        calls += 2
+    return {"value": bytes_total / t_total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"MXFP4 gate/up layer 0 and bf16 layer 24 of the stack ({rows} of {cfg.n} "
+                      f"rows each), {calls} calls, {t_total:.1f} s, fp64 single thread",
+            "seconds": round(t_total, 2)}
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="thinmx", choices=["thinmx", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="skip the secondary workloads")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+    from bit_weight_only_mxfp4_gb300 import build as tt_build
+    from bit_weight_only_mxfp4_gb300 import loader, synth, thinmx
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        pg = dist
+    if rank == 0:
+        tt_build.build()
+    if pg:
+        pg.barrier()
+    thinmx.load()
+
+    cfg = synth.STACK
+    layers = build_stack(torch, synth, loader, cfg, device)
+    mx_b, bf_b = stack_bytes(cfg)
+    step_bytes = cfg.mxfp4_layers * mx_b + (cfg.layers - cfg.mxfp4_layers) * bf_b
+
+    g_step = capture(torch, lambda: [run_layer(thinmx, cfg, L) for L in layers])
+    mx_layers = [L for L in layers if L[0] == "mxfp4"]
+    bf_layers = [L for L in layers if L[0] == "bf16"]
+    g_mx = capture(torch, lambda: [run_layer(thinmx, cfg, L) for L in mx_layers])
+    g_bf = capture(torch, lambda: [run_layer(thinmx, cfg, L) for L in bf_layers])
+
+    # ---- timed region: K steps of the stack -------------------------------
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            g_step.replay()
+        e1.record()
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if pg:
+        t = torch.tensor([ms], device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # per-kernel average launch duration (same stream, CUDA events)
+    reps = max(10, args.steps)
+    ms_mx = time_graph(torch, g_mx, reps) / len(mx_layers)
+    ms_bf = time_graph(torch, g_bf, reps) / len(bf_layers)
+
+    # ---- end to end through the public API with host buffers --------------
+    L = len(layers)
+    x_host = torch.empty((L, cfg.k), dtype=torch.bfloat16).pin_memory()
+    h_host = torch.empty((L, cfg.n), dtype=torch.bfloat16).pin_memory()
+    for i, lay in enumerate(layers):
+        x_host[i].copy_(lay[2][0].cpu())
+    x_dev = torch.empty((L, cfg.k), dtype=torch.bfloat16, device=device)
+    h_dev = torch.empty((L, cfg.n), dtype=torch.bfloat16, device=device)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        for i, lay in enumerate(layers):
+            run_layer(thinmx, cfg, lay, x_dev[i:i + 1], h_dev[i:i + 1])
+        h_host.copy_(h_dev, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+
+    # ---- secondary workloads (rank 0 only) -----------------------------------
+    others = {}
+    hbm, peak_kind, _ = peaks()
+    if rank == 0 and not args.quick:
+        others = secondary(torch, synth, loader, thinmx, device, hbm, peak_kind)
+
+    # ---- cpu baseline ---------------------------------------------------------
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+
+    err = thinmx.tt_device_error_read()
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+
+    gbs = step_bytes * world / (ms * 1e-3) / 1e9
+    mx_ach = mx_b / (ms_mx * 1e-3) / 1e9
+    bf_ach = bf_b / (ms_bf * 1e-3) / 1e9
+    t_mx_total = ms_mx * len(mx_layers)
+    t_bf_total = ms_bf * len(bf_layers)
+    kernels = [
+        {"kernel": "swiglu_mxfp4_m1_kernel", "bound": "hbm", "achieved": round(mx_ach, 1),
+         "peak": hbm, "unit": "GB/s", "frac": round(mx_ach / hbm, 4),
+         "bytes_per_launch": mx_b, "us_per_launch": round(ms_mx * 1e3, 3),
+         "time_share": round(t_mx_total / (t_mx_total + t_bf_total), 3)},
+        {"kernel": "swiglu_bf16_kernel", "bound": "hbm", "achieved": round(bf_ach, 1),
+         "peak": hbm, "unit": "GB/s", "frac": round(bf_ach / hbm, 4),
+         "bytes_per_launch": bf_b, "us_per_launch": round(ms_bf * 1e3, 3),
+         "time_share": round(t_bf_total / (t_mx_total + t_bf_total), 3)},
+    ]
+    dominant = max(kernels, key=lambda d: d["time_share"])
+    roofline = {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac")}
+    roofline["traffic"] = None
+    roofline["kernel"] = dominant["kernel"]
+    roofline["peak_source"] = f"{peak_kind} HBM copy bandwidth"
+    line = {
+        "metric": "batch-1 MXFP4 SwiGLU matvec µs/layer, weight GB/s and % of GB300 HBM roofline",
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp4(e2m1+e8m0) x bf16 -> fp32 acc -> bf16",
+        "data": "synthetic: W ~ N(0,0.02^2) quantised to MXFP4 on the GPU, x ~ N(0,1) bf16, "
+                "postscale ~ U[0.9,1.1]; seeded",
+        "config": {"workload": cfg.name, "layers": cfg.layers, "mxfp4_layers": "0:24",
+                   "k": cfg.k, "n": cfg.n, "m": 1, "bytes_per_step": step_bytes,
+                   "l2_policy": "inputs larger than L2 (1.66 GB of weights per step)",
+                   "timing": "CUDA graph of the 36 calls, CUDA events on the replay stream"},
+        "us_per_layer": {"mxfp4": round(ms_mx * 1e3, 3), "bf16": round(ms_bf * 1e3, 3),
+                         "stack_total": round(ms * 1e3, 2)},
+        "roofline": roofline,
+        "roofline_by_kernel": kernels,
+        "e2e": {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": L * cfg.k * 2, "d2h_bytes_per_step": L * cfg.n * 2,
+                "path": "pinned host x -> device, 36 C-ABI calls (no graph), h -> pinned host"},
+        "gpu_launches": len(layers) * args.steps,
+        "clocks": clk.summary(),
+        "others": others,
+        "cpu_baseline": cpu,
+        "device_error": err,
+    }
+    print(json.dumps(line))
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
+    """Single gate/up layer (rotating copies > 2x L2) and the Phi-4 batch sweep."""
+    out = {}
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    # single SmolLM3 gate/up layer, M=1
+    c = synth.GATE_UP
+    per = gate_up_bytes(c.n, c.k, 1)
+    copies = max(4, int(2 * l2 // per) + 2)
+    bufs = []
+    for i in range(copies):
+        wg = synth.torch_normal((c.n, c.k), synth.WEIGHT_STD, c.wid, i, 0, device)
+        wu = synth.torch_normal((c.n, c.k), synth.WEIGHT_STD, c.wid, i, 1, device)
+        pgv = synth.torch_uniform((c.n,), 0.9, 1.1, c.wid, i, 3, device)
+        puv = synth.torch_uniform((c.n,), 0.9, 1.1, c.wid, i, 4, device)
+        packed = loader.mxfp4_gate_up_from_f32(wg, wu, pgv, puv)
+        del wg, wu
+        x = synth.torch_normal((1, c.k), 1.0, c.wid, i, 2, device).to(torch.bfloat16)
+        h = torch.empty((1, c.n), dtype=torch.bfloat16, device=device)
+        bufs.append((packed, x, h))
+    g = capture(torch, lambda: [thinmx.tt_mxfp4_swiglu_matvec(p, c.n, c.k, x, 1, h)
+                                for p, x, h in bufs])
+    ms = time_graph(torch, g, 50) / copies
+    out[c.name] = {"us": round(ms * 1e3, 3), "GBps": round(per / (ms * 1e-3) / 1e9, 1),
+                   "frac": round(per / (ms * 1e-3) / 1e9 / hbm, 4), "bytes": per,
+                   "rotating_copies": copies}
+    del bufs, g
+    torch.cuda.empty_cache()
+
+    # Phi-4 gate/up batch sweep
+    s = synth.SWEEP
+    wg = synth.torch_normal((s.n, s.k), synth.WEIGHT_STD, s.wid, 0, 0, device)
+    wu = synth.torch_normal((s.n, s.k), synth.WEIGHT_STD, s.wid, 0, 1, device)
+    pgv = synth.torch_uniform((s.n,), 0.9, 1.1, s.wid, 0, 3, device)
+    puv = synth.torch_uniform((s.n,), 0.9, 1.1, s.wid, 0, 4, device)
+    base = loader.mxfp4_gate_up_from_f32(wg, wu, pgv, puv)
+    del wg, wu
+    per_w = base.numel()
+    copies = max(3, int(2 * l2 // per_w) + 1)
+    packs = [base] + [base.clone() for _ in range(copies - 1)]
+    sweep = {}
+    for m in s.ms:
+        if m > 8:
+            sweep[str(m)] = {"status": "tensor-core path not built yet"}
+            continue
+        xs = [synth.torch_normal((m, s.k), 1.0, s.wid, 0, 2, device).to(torch.bfloat16)
+              for _ in range(copies)]
+        hs = [torch.empty((m, s.n), dtype=torch.bfloat16, device=device) for _ in range(copies)]
+        g = capture(torch, lambda: [thinmx.tt_mxfp4_swiglu_matvec(p, s.n, s.k, x, m, h)
+                                    for p, x, h in zip(packs, xs, hs)])
+        ms = time_graph(torch, g, 20) / copies
+        b = gate_up_bytes(s.n, s.k, m)
+        sweep[str(m)] = {"us": round(ms * 1e3, 3), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
+                         "frac": round(b / (ms * 1e-3) / 1e9 / hbm, 4),
+                         "TFLOPs": round(4 * m * s.n * s.k / (ms * 1e-3) / 1e12, 2)}
+        del g
+    out[s.name] = sweep
+    out["peak"] = {"hbm_gbs": hbm, "source": peak_kind}
+    del packs, base
+    torch.cuda.empty_cache()
+    return out
+
+
+def reference_arm(args, world, rank):
+    """The CPU oracle timed as the reference arm (the pages ship no runnable
+    implementation): each step is a bounded sample of the stack."""
+    if rank != 0:
+        return 0
+    from bit_weight_only_mxfp4_gb300 import synth
+    cfg = synth.STACK
+    rows = 512
+    for _ in range(args.warmup):
+        cpu_baseline(0.0, rows)
+    t0 = time.perf_counter()
+    vals = [cpu_baseline(0.0, rows) for _ in range(args.steps)]
+    dt = time.perf_counter() - t0
+    v = statistics.median(x["value"] for x in vals)
+    line = {
+        "impl": "reference",
+        "metric": "batch-1 MXFP4 SwiGLU matvec µs/layer, weight GB/s and % of GB300 HBM roofline",
+        "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic, seeded (same draws as the GPU arm)",
+        "config": {"workload": cfg.name, "sample_rows": rows},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,168 @@
+// The C ABI (include/thinmx.h): host-side validation, then one launch on
+// the caller's stream.  Nothing here allocates device memory or
+// synchronises, except the diagnostic tt_device_error_read.
+#include <mutex>
+
+#include "../../include/thinmx.h"
+#include "common.cuh"
+#include "launch.h"
+#include "layout.cuh"
+
+namespace tt {
+
+// The library's device error word (first asynchronous error wins).
+static __device__ int32_t g_device_error = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_ok[kMaxDevices];
+std::mutex g_info_mu;
+}  // namespace
+
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_info_mu);
+  if (!g_info_ok[dev]) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return nullptr;
+    if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+      return nullptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    d.error_word = static_cast<int32_t*>(p);
+    g_info[dev] = d;
+    g_info_ok[dev] = true;
+  }
+  return &g_info[dev];
+}
+
+}  // namespace tt
+
+namespace {
+
+inline bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+inline tt_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return TT_OK;
+  (void)cudaGetLastError();  // clear a sticky launch error so later calls see their own
+  return TT_ERR_CUDA;
+}
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
+constexpr int64_t kMaxK = 16384;
+
+// Programmatic dependent launch on the hot-path kernels.
+constexpr bool kPdl = true;
+
+}  // namespace
+
+extern "C" {
+
+const char* tt_status_str(int status) {
+  switch (status) {
+    case TT_OK: return "TT_OK";
+    case TT_ERR_NULL: return "TT_ERR_NULL";
+    case TT_ERR_SHAPE: return "TT_ERR_SHAPE";
+    case TT_ERR_ALIGN: return "TT_ERR_ALIGN";
+    case TT_ERR_NONFINITE: return "TT_ERR_NONFINITE";
+    case TT_ERR_UNSUPPORTED: return "TT_ERR_UNSUPPORTED";
+    case TT_ERR_CUDA: return "TT_ERR_CUDA";
+    case TT_ERR_TIMEOUT: return "TT_ERR_TIMEOUT";
+    case TT_ERR_SIZE: return "TT_ERR_SIZE";
+    default: return "TT_ERR_UNKNOWN";
+  }
+}
+
+int tt_version(void) { return 10000; }
+
+tt_status tt_device_error_read(int32_t* out) {
+  if (!out) return TT_ERR_NULL;
+  const tt::DeviceInfo* di = tt::device_info();
+  if (!di) return TT_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return from_cuda(cudaErrorUnknown);
+  int32_t v = 0;
+  if (cudaMemcpy(&v, di->error_word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return from_cuda(cudaErrorUnknown);
+  const int32_t zero = 0;
+  if (cudaMemcpy(di->error_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return from_cuda(cudaErrorUnknown);
+  *out = v;
+  return TT_OK;
+}
+
+tt_status tt_quantize_mxfp4(const float* w, int64_t n, int64_t k, uint8_t* codes,
+                            uint8_t* scales, int32_t* status_dev, void* stream) {
+  if (n < 0 || k < 0 || k % 32 != 0 || n > kMaxRows) return TT_ERR_SHAPE;
+  if (n == 0 || k == 0) return TT_OK;
+  if (!w || !codes || !scales) return TT_ERR_NULL;
+  if (!aligned(w, 16) || !aligned(codes, 16) || (status_dev && !aligned(status_dev, 4)))
+    return TT_ERR_ALIGN;
+  return from_cuda(tt::launch_quantize_mxfp4(w, n, k, codes, scales, status_dev,
+                                             as_stream(stream)));
+}
+
+tt_status tt_mxfp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k,
+                              float* out, void* stream) {
+  if (n < 0 || k < 0 || k % 32 != 0 || n > kMaxRows) return TT_ERR_SHAPE;
+  if (n == 0 || k == 0) return TT_OK;
+  if (!codes || !scales || !out) return TT_ERR_NULL;
+  if (!aligned(out, 8)) return TT_ERR_ALIGN;
+  return from_cuda(tt::launch_dequantize_mxfp4(codes, scales, n, k, out, as_stream(stream)));
+}
+
+size_t tt_mxfp4_swiglu_packed_bytes(int64_t n, int64_t k) {
+  if (n < 1 || k < 32 || k % 32 != 0 || k > kMaxK || n > kMaxRows) return 0;
+  return size_t(n) * size_t(tt::SwigluRecord(int(k)).bytes);
+}
+
+tt_status tt_mxfp4_pack_swiglu(const uint8_t* gate_codes, const uint8_t* gate_scales,
+                               const float* gate_postscale, const uint8_t* up_codes,
+                               const uint8_t* up_scales, const float* up_postscale, int64_t n,
+                               int64_t k, void* packed, size_t packed_bytes, void* stream) {
+  if (n < 1 || k < 32 || k % 32 != 0 || k > kMaxK || n > kMaxRows) return TT_ERR_SHAPE;
+  if (!gate_codes || !gate_scales || !up_codes || !up_scales || !packed) return TT_ERR_NULL;
+  if (packed_bytes < tt_mxfp4_swiglu_packed_bytes(n, k)) return TT_ERR_SIZE;
+  if (!aligned(packed, 16) || (gate_postscale && !aligned(gate_postscale, 4)) ||
+      (up_postscale && !aligned(up_postscale, 4)))
+    return TT_ERR_ALIGN;
+  return from_cuda(tt::launch_pack_swiglu(gate_codes, gate_scales, gate_postscale, up_codes,
+                                          up_scales, up_postscale, n, k,
+                                          static_cast<uint8_t*>(packed), as_stream(stream)));
+}
+
+tt_status tt_mxfp4_swiglu_matvec(const void* packed, int64_t n, int64_t k,
+                                 const uint16_t* x_bf16, int64_t m, uint16_t* h_bf16,
+                                 void* stream) {
+  if (n < 1 || k < 32 || k % 32 != 0 || k > kMaxK || n > kMaxRows) return TT_ERR_SHAPE;
+  if (m < 1 || m > 64) return TT_ERR_SHAPE;
+  if (!packed || !x_bf16 || !h_bf16) return TT_ERR_NULL;
+  if (!aligned(packed, 16) || !aligned(x_bf16, 16) || !aligned(h_bf16, 2)) return TT_ERR_ALIGN;
+  if (m > 8) return TT_ERR_UNSUPPORTED;
+  const cudaError_t e =
+      tt::launch_swiglu_mxfp4_cc(static_cast<const uint8_t*>(packed), int(n), int(k), x_bf16,
+                                 int(m), h_bf16, as_stream(stream), kPdl);
+  if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+tt_status tt_bf16_swiglu_matvec(const uint16_t* wg, const uint16_t* wu, int64_t n, int64_t k,
+                                const uint16_t* x_bf16, int64_t m, uint16_t* h_bf16,
+                                void* stream) {
+  if (n < 1 || k < 8 || k % 8 != 0 || k > (int64_t(1) << 30) || n > kMaxRows) return TT_ERR_SHAPE;
+  if (m < 1 || m > 8) return TT_ERR_SHAPE;
+  if (!wg || !wu || !x_bf16 || !h_bf16) return TT_ERR_NULL;
+  if (!aligned(wg, 16) || !aligned(wu, 16) || !aligned(x_bf16, 16) || !aligned(h_bf16, 2))
+    return TT_ERR_ALIGN;
+  return from_cuda(tt::launch_swiglu_bf16(wg, wu, int(n), int(k), x_bf16, int(m), h_bf16,
+                                          as_stream(stream), kPdl));
+}
+
+}  // extern "C"

@@ -1,0 +1,440 @@
+// CUDA-core MXFP4 gate/up SwiGLU matvec for small batches (m = 1..8).
+//
+// Method: ThinTensor devlog (kerbin.cskartikey.dev/@satvikhardat), Dev Log #4
+// "Where Blackwell helps": read the MXFP4 bytes, use the block scales,
+// multiply against bf16 activations, accumulate safely, then apply the row
+// postscale; the gate/up pair feeds the gated activation of Dev Log #2.
+// Decode is a weight-read problem (Dev Log #4, "Why gate/up was the right
+// target"), so the kernel is built to stream the packed codes once at HBM
+// speed:
+//
+//  * persistent grid, one CTA per SM, each CTA owning a contiguous range of
+//    row records of the packed layout (layout.cuh);
+//  * every warp runs its own ring of `slots` shared-memory slots, refilled
+//    by one-instruction bulk copies (TMA, non-tensor) signalled on an
+//    mbarrier; the first copies are issued before the programmatic-
+//    dependent-launch wait, so weight streaming overlaps the previous
+//    kernel's tail;
+//  * lane l owns the 32-weight blocks l, l+32, l+64, ... of every row, so
+//    its slice of x is converted once (to f16 after an exact power-of-two
+//    prescale) and reused for every row;
+//  * E2M1 pairs are widened with cvt.rn.f16x2.e2m1x2 and multiplied into
+//    fp32 with fma.rn.f32.f16 (the e2m1 x f16 products are exact), the
+//    block's E8M0 scale is applied once per 32 products, and the split-K
+//    partial sums meet in a warp-shuffle reduction;
+//  * K is always looped in bounded 1024-wide chunks (the project page's
+//    wide-matvec devlog: never pad K into one oversized tile).
+#include "common.cuh"
+#include "launch.h"
+#include "layout.cuh"
+
+namespace tt {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+
+// 32 E2M1 codes (one 16-byte chunk) dotted with 32 f16 values (16 f16x2),
+// fp32 accumulation in four chains.
+__device__ __forceinline__ float dot32(const uint4& c, const uint32_t* xv) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  uint32_t h[16];
+  e2m1x8_to_f16x2(c.x, h[0], h[1], h[2], h[3]);
+  e2m1x8_to_f16x2(c.y, h[4], h[5], h[6], h[7]);
+  e2m1x8_to_f16x2(c.z, h[8], h[9], h[10], h[11]);
+  e2m1x8_to_f16x2(c.w, h[12], h[13], h[14], h[15]);
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    fma_f16x2_f32(a0, a1, h[i], xv[i]);
+    fma_f16x2_f32(a2, a3, h[i + 1], xv[i + 1]);
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
+__device__ __forceinline__ void decode32(const uint4& c, uint32_t* h) {
+  e2m1x8_to_f16x2(c.x, h[0], h[1], h[2], h[3]);
+  e2m1x8_to_f16x2(c.y, h[4], h[5], h[6], h[7]);
+  e2m1x8_to_f16x2(c.z, h[8], h[9], h[10], h[11]);
+  e2m1x8_to_f16x2(c.w, h[12], h[13], h[14], h[15]);
+}
+
+__device__ __forceinline__ float dot32_decoded(const uint32_t* h, const uint32_t* xv) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    fma_f16x2_f32(a0, a1, h[i], xv[i]);
+    fma_f16x2_f32(a2, a3, h[i + 1], xv[i + 1]);
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// Per-warp ring of bulk-copy slots over the warp's records r0 + warp + j*kWarps.
+struct WarpRing {
+  uint8_t* base;
+  uint64_t* bars;
+  int slots;
+  int bytes;
+  const uint8_t* src;  // first record of the CTA + warp offset
+  int64_t stride;      // bytes between consecutive records of this warp
+  uint64_t policy;
+
+  __device__ void init(int lane) {
+    if (lane == 0) {
+      for (int s = 0; s < slots; ++s) mbar_init(smem_u32(&bars[s]), 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+  }
+  __device__ void issue(int j) {  // lane 0 only
+    const int s = j % slots;
+    const uint32_t bar = smem_u32(&bars[s]);
+    mbar_arrive_expect_tx(bar, uint32_t(bytes));
+    bulk_g2s(smem_u32(base + (size_t)s * bytes), src + (int64_t)j * stride, uint32_t(bytes), bar,
+             policy);
+  }
+  // Returns the slot of record j once its copy has landed, nullptr after a
+  // timeout (warp-uniform).
+  __device__ const uint8_t* wait(int j) {
+    const int s = j % slots;
+    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), uint32_t((j / slots) & 1));
+    if (!__all_sync(0xffffffffu, ok)) return nullptr;
+    return base + (size_t)s * bytes;
+  }
+  // After a timeout at record j: give the copies already issued a bounded
+  // chance to land before the CTA may exit.
+  __device__ void drain(int j, int nrec) {
+    const int issued = min(nrec, j + slots);
+    for (int t = j + 1; t < issued; ++t)
+      (void)mbar_wait_bounded(smem_u32(&bars[t % slots]), uint32_t((t / slots) & 1));
+  }
+};
+
+// ---------------------------------------------------------------------------
+// m = 1, x held in registers.  NB = number of 1024-wide K chunks (k <= 1024*NB).
+// ---------------------------------------------------------------------------
+template <int NB>
+__global__ void __launch_bounds__(kThreads, (NB <= 3 ? 2 : 1))
+    swiglu_mxfp4_m1_kernel(const uint8_t* __restrict__ packed, int n, int k,
+                           const uint16_t* __restrict__ x, uint16_t* __restrict__ h, int slots,
+                           int32_t* err) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const SwigluRecord L(k);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r0 = int((int64_t)n * blockIdx.x / gridDim.x);
+  const int r1 = int((int64_t)n * (blockIdx.x + 1) / gridDim.x);
+  const int cnt = r1 - r0;
+  const int nrec = cnt > warp ? (cnt - warp + kWarps - 1) / kWarps : 0;
+
+  WarpRing ring;
+  ring.slots = slots;
+  ring.bytes = L.bytes;
+  ring.base = smem + (size_t)warp * slots * L.bytes;
+  ring.bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * slots * L.bytes) + warp * slots;
+  ring.src = packed + (int64_t)(r0 + warp) * L.bytes;
+  ring.stride = (int64_t)kWarps * L.bytes;
+  ring.policy = l2_evict_first_policy();
+  ring.init(lane);
+
+  pdl_allow_next_grid();
+  // Weights do not depend on the previous kernel: start streaming them now.
+  if (lane == 0)
+    for (int j = 0; j < min(slots, nrec); ++j) ring.issue(j);
+  pdl_wait_prior_grid();
+
+  // x slice of this lane -> f16x2 registers, prescaled by 2^sx (exact).
+  uint32_t xr[NB][16];
+  float xmax = 0.f;
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    const int b = 32 * i + lane;
+    uint4 q[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                  make_uint4(0, 0, 0, 0)};
+    if (b < L.nblk) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)b * 32);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) q[t] = src[t];
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      xr[i][4 * t + 0] = q[t].x;
+      xr[i][4 * t + 1] = q[t].y;
+      xr[i][4 * t + 2] = q[t].z;
+      xr[i][4 * t + 3] = q[t].w;
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      xmax = fmaxf(xmax, fabsf(bf16_bits_to_f32(xr[i][t] & 0xFFFFu)));
+      xmax = fmaxf(xmax, fabsf(bf16_bits_to_f32(xr[i][t] >> 16)));
+    }
+  }
+  xmax = warp_max(xmax);
+  const int sx = min(f16_prescale_exponent(xmax), 127);
+  const float two_s = scalbnf(1.0f, sx);
+#pragma unroll
+  for (int i = 0; i < NB; ++i)
+#pragma unroll
+    for (int t = 0; t < 16; ++t)
+      xr[i][t] = pack_f16x2_scaled(bf16_bits_to_f32(xr[i][t] & 0xFFFFu),
+                                   bf16_bits_to_f32(xr[i][t] >> 16), two_s);
+
+  for (int j = 0; j < nrec; ++j) {
+    const uint8_t* rec = ring.wait(j);
+    if (rec == nullptr) {
+      if (lane == 0) flag_error(err, kErrTimeout);
+      ring.drain(j, nrec);
+      return;
+    }
+    float ag = 0.f, au = 0.f;
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+      const int b = 32 * i + lane;
+      if (b < L.nblk) {
+        const uint4 cg = *reinterpret_cast<const uint4*>(rec + L.gate_codes() + b * 16);
+        const uint4 cu = *reinterpret_cast<const uint4*>(rec + L.up_codes() + b * 16);
+        const float sg = e8m0_to_f32(rec[L.gate_scales() + b]);
+        const float su = e8m0_to_f32(rec[L.up_scales() + b]);
+        ag = fmaf(dot32(cg, xr[i]), sg, ag);
+        au = fmaf(dot32(cu, xr[i]), su, au);
+      }
+    }
+    const float pg = *reinterpret_cast<const float*>(rec + L.post);
+    const float pu = *reinterpret_cast<const float*>(rec + L.post + 4);
+    __syncwarp();
+    if (lane == 0 && j + slots < nrec) ring.issue(j + slots);
+    const float v = warp_sum2(ag, au, lane);
+    const float vu = __shfl_sync(0xffffffffu, v, 16);
+    if (lane == 0) {
+      const float g = scalbnf(v, -sx) * pg;
+      const float u = scalbnf(vu, -sx) * pu;
+      h[r0 + warp + j * kWarps] = f32_to_bf16_rne(silu_mul(g, u));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// m = 1..8 (MT = 1, 2, 4 or 8 rows of x), x staged in shared memory as f16.
+// x layout in shared memory: 16-byte chunk q (0..3) of block b of row i at
+// ((i*4 + q) * nblk + b) * 16, so lanes reading consecutive blocks hit
+// consecutive 16-byte words (no bank conflicts).
+// ---------------------------------------------------------------------------
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 1)
+    swiglu_mxfp4_mt_kernel(const uint8_t* __restrict__ packed, int n, int k, int m,
+                           const uint16_t* __restrict__ x, uint16_t* __restrict__ h, int slots,
+                           int32_t* err) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const SwigluRecord L(k);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r0 = int((int64_t)n * blockIdx.x / gridDim.x);
+  const int r1 = int((int64_t)n * (blockIdx.x + 1) / gridDim.x);
+  const int cnt = r1 - r0;
+  const int nrec = cnt > warp ? (cnt - warp + kWarps - 1) / kWarps : 0;
+  const size_t ring_bytes = (size_t)kWarps * slots * L.bytes;
+  uint4* xs = reinterpret_cast<uint4*>(smem + ring_bytes);            // MT * 4 * nblk chunks
+  int* sxs = reinterpret_cast<int*>(smem + ring_bytes + (size_t)MT * 2 * k);  // MT exponents
+  float* red = reinterpret_cast<float*>(sxs + MT);                      // MT * kWarps maxima
+  uint64_t* bars_all = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(red + MT * kWarps) + 7) & ~uintptr_t(7));
+
+  WarpRing ring;
+  ring.slots = slots;
+  ring.bytes = L.bytes;
+  ring.base = smem + (size_t)warp * slots * L.bytes;
+  ring.bars = bars_all + warp * slots;
+  ring.src = packed + (int64_t)(r0 + warp) * L.bytes;
+  ring.stride = (int64_t)kWarps * L.bytes;
+  ring.policy = l2_evict_first_policy();
+  ring.init(lane);
+
+  pdl_allow_next_grid();
+  if (lane == 0)
+    for (int j = 0; j < min(slots, nrec); ++j) ring.issue(j);
+  pdl_wait_prior_grid();
+
+  // Per-row max |x| -> prescale exponent; then convert x into shared memory.
+  for (int i = 0; i < MT; ++i) {
+    float mx = 0.f;
+    if (i < m)
+      for (int t = threadIdx.x; t < k; t += kThreads)
+        mx = fmaxf(mx, fabsf(bf16_bits_to_f32(x[(size_t)i * k + t])));
+    mx = warp_max(mx);
+    if (lane == 0) red[i * kWarps + warp] = mx;
+  }
+  __syncthreads();
+  if (threadIdx.x < MT) {
+    float mx = 0.f;
+    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red[threadIdx.x * kWarps + w]);
+    sxs[threadIdx.x] = min(f16_prescale_exponent(mx), 127);
+  }
+  __syncthreads();
+  const int nblk = L.nblk;
+  for (int c = threadIdx.x; c < MT * 4 * nblk; c += kThreads) {
+    const int i = c / (4 * nblk);
+    const int rem = c - i * 4 * nblk;
+    const int q = rem / nblk, b = rem - q * nblk;
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (i < m) {
+      const float two_s = scalbnf(1.0f, sxs[i]);
+      const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)i * k + b * 32 + q * 8);
+      o.x = pack_f16x2_scaled(bf16_bits_to_f32(v.x & 0xFFFFu), bf16_bits_to_f32(v.x >> 16), two_s);
+      o.y = pack_f16x2_scaled(bf16_bits_to_f32(v.y & 0xFFFFu), bf16_bits_to_f32(v.y >> 16), two_s);
+      o.z = pack_f16x2_scaled(bf16_bits_to_f32(v.z & 0xFFFFu), bf16_bits_to_f32(v.z >> 16), two_s);
+      o.w = pack_f16x2_scaled(bf16_bits_to_f32(v.w & 0xFFFFu), bf16_bits_to_f32(v.w >> 16), two_s);
+    }
+    xs[c] = o;
+  }
+  __syncthreads();
+
+  const int nchunk = (nblk + 31) / 32;
+  for (int j = 0; j < nrec; ++j) {
+    const uint8_t* rec = ring.wait(j);
+    if (rec == nullptr) {
+      if (lane == 0) flag_error(err, kErrTimeout);
+      ring.drain(j, nrec);
+      return;
+    }
+    float ag[MT], au[MT];
+#pragma unroll
+    for (int i = 0; i < MT; ++i) ag[i] = au[i] = 0.f;
+    for (int c = 0; c < nchunk; ++c) {
+      const int b = 32 * c + lane;
+      if (b < nblk) {
+        uint32_t hg[16], hu[16];
+        decode32(*reinterpret_cast<const uint4*>(rec + L.gate_codes() + b * 16), hg);
+        decode32(*reinterpret_cast<const uint4*>(rec + L.up_codes() + b * 16), hu);
+        const float sg = e8m0_to_f32(rec[L.gate_scales() + b]);
+        const float su = e8m0_to_f32(rec[L.up_scales() + b]);
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+          uint32_t xv[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 t = xs[(i * 4 + q) * nblk + b];
+            xv[4 * q + 0] = t.x;
+            xv[4 * q + 1] = t.y;
+            xv[4 * q + 2] = t.z;
+            xv[4 * q + 3] = t.w;
+          }
+          ag[i] = fmaf(dot32_decoded(hg, xv), sg, ag[i]);
+          au[i] = fmaf(dot32_decoded(hu, xv), su, au[i]);
+        }
+      }
+    }
+    const float pg = *reinterpret_cast<const float*>(rec + L.post);
+    const float pu = *reinterpret_cast<const float*>(rec + L.post + 4);
+    __syncwarp();
+    if (lane == 0 && j + slots < nrec) ring.issue(j + slots);
+    const int r = r0 + warp + j * kWarps;
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+      const float v = warp_sum2(ag[i], au[i], lane);
+      const float vu = __shfl_sync(0xffffffffu, v, 16);
+      if (lane == 0 && i < m) {
+        const float g = scalbnf(v, -sxs[i]) * pg;
+        const float u = scalbnf(vu, -sxs[i]) * pu;
+        h[(size_t)i * n + r] = f32_to_bf16_rne(silu_mul(g, u));
+      }
+    }
+  }
+}
+
+template <typename Kern>
+cudaError_t launch_pdl(Kern kern, int grid, int smem, cudaStream_t s, bool pdl,
+                       const uint8_t* packed, int n, int k, const uint16_t* x, uint16_t* h,
+                       int slots, int32_t* err) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, packed, n, k, x, h, slots, err);
+}
+
+template <typename Kern>
+cudaError_t launch_pdl_m(Kern kern, int grid, int smem, cudaStream_t s, bool pdl,
+                         const uint8_t* packed, int n, int k, int m, const uint16_t* x,
+                         uint16_t* h, int slots, int32_t* err) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, packed, n, k, m, x, h, slots, err);
+}
+
+// Shared memory given to one CTA's ring: small enough that two CTAs fit on
+// an SM, so the next kernel's CTA can start streaming while this one ends.
+constexpr int kRingBudget = 100 * 1024;
+
+template <int NB>
+cudaError_t run_m1(const DeviceInfo& di, const uint8_t* packed, int n, int k, const uint16_t* x,
+                   uint16_t* h, cudaStream_t s, bool pdl) {
+  const SwigluRecord L(k);
+  int slots = kRingBudget / (kWarps * L.bytes);
+  slots = slots < 2 ? 2 : (slots > 6 ? 6 : slots);
+  const int smem = kWarps * slots * (L.bytes + 8);
+  if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
+  auto kern = swiglu_mxfp4_m1_kernel<NB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int grid = n < di.sms ? n : di.sms;
+  return launch_pdl(kern, grid, smem, s, pdl, packed, n, k, x, h, slots, di.error_word);
+}
+
+template <int MT>
+cudaError_t run_mt(const DeviceInfo& di, const uint8_t* packed, int n, int k, int m,
+                   const uint16_t* x, uint16_t* h, cudaStream_t s, bool pdl) {
+  const SwigluRecord L(k);
+  const int xs_bytes = MT * 2 * k + MT * 4 + MT * kWarps * 4 + 16;
+  const int avail = di.smem_optin - xs_bytes;
+  int slots = (avail < kRingBudget ? avail : kRingBudget) / (kWarps * (L.bytes + 8));
+  if (slots < 1) return cudaErrorInvalidConfiguration;
+  if (slots > 6) slots = 6;
+  const int smem = kWarps * slots * (L.bytes + 8) + xs_bytes;
+  auto kern = swiglu_mxfp4_mt_kernel<MT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int grid = n < di.sms ? n : di.sms;
+  return launch_pdl_m(kern, grid, smem, s, pdl, packed, n, k, m, x, h, slots, di.error_word);
+}
+
+}  // namespace
+
+cudaError_t launch_swiglu_mxfp4_cc(const uint8_t* packed, int n, int k, const uint16_t* x, int m,
+                                   uint16_t* h, cudaStream_t s, bool pdl) {
+  const DeviceInfo* di = device_info();
+  if (!di) return cudaErrorNoDevice;
+  if (m == 1) {
+    const int nb = (k / 32 + 31) / 32;
+    switch (nb) {
+      case 1: return run_m1<1>(*di, packed, n, k, x, h, s, pdl);
+      case 2: return run_m1<2>(*di, packed, n, k, x, h, s, pdl);
+      case 3: return run_m1<3>(*di, packed, n, k, x, h, s, pdl);
+      case 4: return run_m1<4>(*di, packed, n, k, x, h, s, pdl);
+      case 5: return run_m1<5>(*di, packed, n, k, x, h, s, pdl);
+      case 6: return run_m1<6>(*di, packed, n, k, x, h, s, pdl);
+      default: return run_mt<1>(*di, packed, n, k, 1, x, h, s, pdl);
+    }
+  }
+  if (m == 2) return run_mt<2>(*di, packed, n, k, m, x, h, s, pdl);
+  if (m <= 4) return run_mt<4>(*di, packed, n, k, m, x, h, s, pdl);
+  if (m <= 8) return run_mt<8>(*di, packed, n, k, m, x, h, s, pdl);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tt

@@ -171,3 +171,26 @@ def int4_inputs(wid: int, layer: int, n: int, k: int, m: int = 1):
     x = normal_bf16(rng(wid, layer, 1), (m, k), 1.0)
     return dict(w=w, x=x)
 
+
+
+# --------------------------------------------------------------------------
+# Bulk device-side draws for the benchmark (full-size stacks would take
+# minutes in numpy).  torch's CUDA Philox generator, seeded per
+# (workload, layer, part); same distributions as above.
+# --------------------------------------------------------------------------
+def torch_seed(workload: int, layer: int = 0, part: int = 0) -> int:
+    return ((workload * 1000003 + layer) * 1009 + part) & 0x7FFFFFFF
+
+
+def torch_normal(shape, std, workload, layer=0, part=0, device="cuda"):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(torch_seed(workload, layer, part))
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std
+
+
+def torch_uniform(shape, lo, hi, workload, layer=0, part=0, device="cuda"):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(torch_seed(workload, layer, part))
+    return torch.rand(shape, generator=g, device=device, dtype=torch.float32) * (hi - lo) + lo

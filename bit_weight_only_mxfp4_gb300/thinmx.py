@@ -1,0 +1,136 @@
+"""Thin Python binding over libthinmx.so (include/thinmx.h).
+
+Each ``tt_*`` function here has the same name and argument order as the C
+entry point; it only marshals torch tensors into device pointers and the
+current CUDA stream, calls the library, and raises ``ThinmxError`` on a
+non-OK status.  All arithmetic runs in the library's CUDA kernels; there is
+no CPU or PyTorch fallback — if the library is missing the call fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libthinmx.so")
+
+STATUS = {
+    0: "TT_OK", 1: "TT_ERR_NULL", 2: "TT_ERR_SHAPE", 3: "TT_ERR_ALIGN",
+    4: "TT_ERR_NONFINITE", 5: "TT_ERR_UNSUPPORTED", 6: "TT_ERR_CUDA",
+    7: "TT_ERR_TIMEOUT", 8: "TT_ERR_SIZE",
+}
+TT_OK = 0
+
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_SZ = ctypes.c_size_t
+
+# name -> (restype, argtypes); mirrors include/thinmx.h
+SIGNATURES = {
+    "tt_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+    "tt_version": (ctypes.c_int, []),
+    "tt_device_error_read": (ctypes.c_int, [_P]),
+    "tt_quantize_mxfp4": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P]),
+    "tt_mxfp4_dequantize": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _P]),
+    "tt_mxfp4_swiglu_packed_bytes": (_SZ, [_I64, _I64]),
+    "tt_mxfp4_pack_swiglu": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P]),
+    "tt_mxfp4_swiglu_matvec": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _P, _P]),
+    "tt_bf16_swiglu_matvec": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _I64, _P, _P]),
+}
+
+
+class ThinmxError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with bit_weight_only_mxfp4_gb300.build.build()")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, st: int):
+    if st != TT_OK:
+        raise ThinmxError(fn, st)
+
+
+# ---------------------------------------------------------------- entry points
+def tt_status_str(status: int) -> str:
+    return load().tt_status_str(status).decode()
+
+
+def tt_version() -> int:
+    return load().tt_version()
+
+
+def tt_device_error_read() -> int:
+    out = ctypes.c_int32(0)
+    _check("tt_device_error_read", load().tt_device_error_read(ctypes.addressof(out)))
+    return out.value
+
+
+def tt_quantize_mxfp4(w, n, k, codes, scales, status_dev=None, stream=None):
+    _check("tt_quantize_mxfp4", load().tt_quantize_mxfp4(
+        _ptr(w), n, k, _ptr(codes), _ptr(scales), _ptr(status_dev), _stream(stream)))
+
+
+def tt_mxfp4_dequantize(codes, scales, n, k, out, stream=None):
+    _check("tt_mxfp4_dequantize", load().tt_mxfp4_dequantize(
+        _ptr(codes), _ptr(scales), n, k, _ptr(out), _stream(stream)))
+
+
+def tt_mxfp4_swiglu_packed_bytes(n, k) -> int:
+    return int(load().tt_mxfp4_swiglu_packed_bytes(n, k))
+
+
+def tt_mxfp4_pack_swiglu(gate_codes, gate_scales, gate_postscale, up_codes, up_scales,
+                         up_postscale, n, k, packed, packed_bytes, stream=None):
+    _check("tt_mxfp4_pack_swiglu", load().tt_mxfp4_pack_swiglu(
+        _ptr(gate_codes), _ptr(gate_scales), _ptr(gate_postscale), _ptr(up_codes),
+        _ptr(up_scales), _ptr(up_postscale), n, k, _ptr(packed), packed_bytes,
+        _stream(stream)))
+
+
+def tt_mxfp4_swiglu_matvec(packed, n, k, x_bf16, m, h_bf16, stream=None):
+    _check("tt_mxfp4_swiglu_matvec", load().tt_mxfp4_swiglu_matvec(
+        _ptr(packed), n, k, _ptr(x_bf16), m, _ptr(h_bf16), _stream(stream)))
+
+
+def tt_bf16_swiglu_matvec(wg, wu, n, k, x_bf16, m, h_bf16, stream=None):
+    _check("tt_bf16_swiglu_matvec", load().tt_bf16_swiglu_matvec(
+        _ptr(wg), _ptr(wu), n, k, _ptr(x_bf16), m, _ptr(h_bf16), _stream(stream)))

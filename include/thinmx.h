@@ -1,0 +1,167 @@
+/*
+ * thinmx — weight-only low-bit decode matvecs for GB300 (sm_103a).
+ *
+ * A C ABI over hand-written CUDA kernels for the batch-1 (small-M) matvecs
+ * of a weight-only quantised decoder:
+ *   - MXFP4 gate/up matvec fused into SwiGLU (h = silu(g) * u);
+ *   - the MoE variant: router, top-k, softmax and only the selected
+ *     experts' gate/up/down;
+ *   - grouped affine INT4 matvec for the dense Q/K/V/O projections;
+ *   - bf16 gate/up SwiGLU matvec for the layers kept in bf16.
+ *
+ * Sources.  The method is the ThinTensor decode runtime's:
+ *   [DL4]  kerbin.cskartikey.dev/@satvikhardat, "Dev Log #4 — 91–96 tok/s
+ *          with Selective MXFP4": MXFP4 on gate/up of layers 0:24 with an
+ *          fp32 row postscale, the rest bf16 ("Why this was not just normal
+ *          quantization"); MXFP4 as an execution format — read fewer bytes,
+ *          block scales, bf16 activations, safe accumulation, then the row
+ *          postscale ("Where Blackwell helps"); decode is a weight-read
+ *          problem ("Why gate/up was the right target").
+ *   [DL2]  same feed, "Dev Log #2": the gated_activation, router and expert
+ *          operators of the execution tape.
+ *   [SHIP] stardance.hackclub.com/projects/29750, "Hitting 100hrs and final
+ *          ship" (production MXFP4/INT4 quantizers, exact routing, expert
+ *          routing on the decode hot path), the MoE drift devlog (block-
+ *          scaled matvec over the selected experts; fast_math lost accuracy),
+ *          the 97.87 tok/s notes (dense_int4_layers for Q/K/V/O), the fixes
+ *          list (affine INT4 with a partial last group; no allocations on
+ *          the hot path; device given by the caller) and the wide-matvec
+ *          devlog (always loop over K with a bounded tile).
+ *
+ * Formats (canonical layouts; the parity surface):
+ *   E2M1 code: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa:
+ *     +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}.  E8M0 scale byte b: 2^(b-127), 255=NaN.
+ *   MXFP4 matrix W [n][k] (row n = output, k = reduction), k % 32 == 0:
+ *     codes  uint8 [n][k/2]  — byte j holds k=2j (low nibble), 2j+1 (high);
+ *     scales uint8 [n][k/32] — one E8M0 byte per 32 consecutive k;
+ *     postscale fp32 [n] (optional; absent = 1), applied after the sum.
+ *   INT4 matrix [n][k], group G along k (last group may be partial):
+ *     codes uint8 [n][k/2] (low nibble = even k), scales fp16 [n][ceil(k/G)],
+ *     zero points uint8 [n][ceil(ceil(k/G)/2)] (low nibble = even group);
+ *     w = (q - zp) * s.
+ *   Activations x: bf16 [m][k] row-major; outputs bf16 [m][n] row-major.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers owned by the caller, on the current
+ *     device; the library never allocates, frees or synchronises
+ *     (tt_device_error_read is the one synchronising diagnostic).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *   - Arguments are validated on the host before any launch; a non-OK
+ *     status means nothing was launched.  TT_ERR_CUDA reports a launch
+ *     error (cudaGetLastError) after the launch.
+ *   - Asynchronous faults inside a kernel (a bounded wait that gave up)
+ *     are recorded in a library-wide device error word, read and cleared by
+ *     tt_device_error_read.
+ *   - Alignment: every device pointer 16 bytes, except the per-row vectors
+ *     (postscales, scales_f16, zero points, status words) which need their
+ *     natural alignment.
+ */
+#ifndef THINMX_H
+#define THINMX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TT_OK = 0,
+    TT_ERR_NULL = 1,        /* a required pointer is NULL                     */
+    TT_ERR_SHAPE = 2,       /* a size is negative, zero where not allowed,
+                               or breaks a divisibility rule                  */
+    TT_ERR_ALIGN = 3,       /* a pointer is not aligned as documented         */
+    TT_ERR_NONFINITE = 4,   /* NaN/Inf met by a quantiser (reported through
+                               its device status word)                        */
+    TT_ERR_UNSUPPORTED = 5, /* valid request outside what is implemented      */
+    TT_ERR_CUDA = 6,        /* the CUDA runtime reported an error             */
+    TT_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up             */
+    TT_ERR_SIZE = 8         /* a caller buffer is smaller than required       */
+} tt_status;
+
+/* Human-readable name of a status.  Never NULL. */
+const char* tt_status_str(int status);
+
+/* ABI version: major*10000 + minor*100 + patch. */
+int tt_version(void);
+
+/* Reads the library's device error word (TT_OK, TT_ERR_TIMEOUT, ...) into
+   *out and clears it.  Synchronises the device.  A diagnostic, not for the
+   hot path. */
+tt_status tt_device_error_read(int32_t* out);
+
+/* ------------------------------------------------------------------------
+ * MXFP4 quantiser  [SHIP "final ship": production MXFP4 quantizers]
+ *
+ * Per row and per block of 32 consecutive k:
+ *   amax = max|w|; X = floor(log2 amax) - 2, read from the fp32 exponent
+ *   field, clamped to [-127, 127] (X = -127 when amax = 0); scale byte
+ *   X + 127; code = E2M1 round-to-nearest-even of w / 2^X, saturating at
+ *   +-6, the sign bit kept on zero (a negative value that rounds to 0 gives
+ *   code 0x8).  A block holding NaN/Inf gets scale 0xFF and zero codes, and
+ *   TT_ERR_NONFINITE is OR-ed into *status_dev.
+ * w: fp32 [n][k] device; codes [n][k/2]; scales [n][k/32];
+ * status_dev: device int32 (may be NULL); the caller zeroes it beforehand.
+ * Requires n >= 0, k >= 0, k % 32 == 0.  Setup step, not on the hot path.
+ * --------------------------------------------------------------------- */
+tt_status tt_quantize_mxfp4(const float* w, int64_t n, int64_t k,
+                            uint8_t* codes, uint8_t* scales,
+                            int32_t* status_dev, void* stream);
+
+/* Test aid: out[n][k] fp32 = E2M1(code) * 2^(scale-127), exact (scale 0xFF
+   gives NaN).  Canonical inputs. */
+tt_status tt_mxfp4_dequantize(const uint8_t* codes, const uint8_t* scales,
+                              int64_t n, int64_t k, float* out, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Packed gate/up layout and loader  [DL4 "Where Blackwell helps": read
+ * fewer bytes; the packed layout keeps the source encoding bit-exact]
+ *
+ * The packed buffer holds, for each output row r, one record with gate row
+ * r's codes, up row r's codes and both rows' scales, contiguous and padded
+ * to 16 bytes, followed by the two fp32 postscale vectors.  The exact
+ * record layout is private; only its size is part of the ABI.  Packing is
+ * a byte-for-byte rearrangement (no rounding).
+ * --------------------------------------------------------------------- */
+size_t tt_mxfp4_swiglu_packed_bytes(int64_t n, int64_t k);
+
+/* gate_*, up_*: canonical MXFP4 [n][k]; postscales may be NULL (= 1).
+   packed: device buffer of at least tt_mxfp4_swiglu_packed_bytes(n, k)
+   bytes, 16-byte aligned.  Requires n >= 1, k >= 32, k % 32 == 0. */
+tt_status tt_mxfp4_pack_swiglu(const uint8_t* gate_codes,
+                               const uint8_t* gate_scales,
+                               const float* gate_postscale,
+                               const uint8_t* up_codes,
+                               const uint8_t* up_scales,
+                               const float* up_postscale, int64_t n,
+                               int64_t k, void* packed, size_t packed_bytes,
+                               void* stream);
+
+/* ------------------------------------------------------------------------
+ * MXFP4 gate/up SwiGLU matvec  [DL4 "Where Blackwell helps"; DL2
+ * gated_activation]
+ *
+ *   g[i][r] = post_g[r] * sum_k Wg[r][k] * x[i][k]
+ *   u[i][r] = post_u[r] * sum_k Wu[r][k] * x[i][k]
+ *   h[i][r] = bf16_rne( silu(g) * u ),  silu(g) = g / (1 + exp(-g))
+ * with fp32 accumulation.  packed: from tt_mxfp4_pack_swiglu(n, k).
+ * x_bf16 [m][k], h_bf16 [m][n]; 1 <= m <= 64.  m < 16 runs the CUDA-core
+ * streaming kernel; m >= 16 the tcgen05 tensor-core kernel.
+ * Requires n >= 1, 32 <= k <= 16384, k % 32 == 0.
+ * --------------------------------------------------------------------- */
+tt_status tt_mxfp4_swiglu_matvec(const void* packed, int64_t n, int64_t k,
+                                 const uint16_t* x_bf16, int64_t m,
+                                 uint16_t* h_bf16, void* stream);
+
+/* bf16 gate/up SwiGLU matvec (the layers a selective profile keeps in
+   bf16) [DL4 "Why this was not just normal quantization"].
+   wg, wu: bf16 [n][k]; x [m][k]; h [m][n]; 1 <= m <= 8; k % 8 == 0. */
+tt_status tt_bf16_swiglu_matvec(const uint16_t* wg, const uint16_t* wu,
+                                int64_t n, int64_t k, const uint16_t* x_bf16,
+                                int64_t m, uint16_t* h_bf16, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* THINMX_H */

@@ -1,0 +1,81 @@
+"""Host-side checks of the C ABI: the library builds for sm_103a, loads
+without a GPU, exports every entry point declared in include/thinmx.h, and
+rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bit_weight_only_mxfp4_gb300 import build as tt_build
+from bit_weight_only_mxfp4_gb300 import thinmx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tt_build.build()
+    return thinmx.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "thinmx.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tt_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared_symbols()
+    for required in ["tt_quantize_mxfp4", "tt_mxfp4_swiglu_matvec"]:
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in thinmx.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    assert thinmx.tt_status_str(0) == "TT_OK"
+    assert thinmx.tt_status_str(7) == "TT_ERR_TIMEOUT"
+    assert thinmx.tt_status_str(99) == "TT_ERR_UNKNOWN"
+    assert thinmx.tt_version() >= 10000
+
+
+def test_packed_bytes_host_arithmetic(lib):
+    # record = gate codes + up codes + both scale rows + 8 B of postscales, 16-B padded
+    assert thinmx.tt_mxfp4_swiglu_packed_bytes(11008, 2048) == 11008 * 2192
+    assert thinmx.tt_mxfp4_swiglu_packed_bytes(2880, 2880) == 2880 * 3072
+    assert thinmx.tt_mxfp4_swiglu_packed_bytes(17920, 5120) == 17920 * 5456
+    assert thinmx.tt_mxfp4_swiglu_packed_bytes(1, 32) == 48
+    assert thinmx.tt_mxfp4_swiglu_packed_bytes(1, 48) == 0      # k % 32 != 0
+    assert thinmx.tt_mxfp4_swiglu_packed_bytes(0, 64) == 0
+
+
+def _st(fn, *args):
+    return getattr(thinmx.load(), fn)(*args)
+
+
+def test_validation_before_launch(lib):
+    A = 1 << 20  # a fake, 16-byte aligned "device" address; never dereferenced
+    s = None
+    # shapes
+    assert _st("tt_mxfp4_swiglu_matvec", A, 128, 48, A, 1, A, s) == 2
+    assert _st("tt_mxfp4_swiglu_matvec", A, 0, 64, A, 1, A, s) == 2
+    assert _st("tt_mxfp4_swiglu_matvec", A, 128, 64, A, 0, A, s) == 2
+    assert _st("tt_mxfp4_swiglu_matvec", A, 128, 64, A, 65, A, s) == 2
+    assert _st("tt_mxfp4_swiglu_matvec", A, 128, 32768, A, 1, A, s) == 2
+    assert _st("tt_quantize_mxfp4", A, 4, 40, A, A, None, s) == 2
+    # null pointers
+    assert _st("tt_mxfp4_swiglu_matvec", None, 128, 64, A, 1, A, s) == 1
+    assert _st("tt_quantize_mxfp4", None, 4, 64, A, A, None, s) == 1
+    # alignment
+    assert _st("tt_mxfp4_swiglu_matvec", A + 8, 128, 64, A, 1, A, s) == 3
+    assert _st("tt_mxfp4_swiglu_matvec", A, 128, 64, A + 2, 1, A, s) == 3
+    assert _st("tt_bf16_swiglu_matvec", A, A + 4, 16, 64, A, 1, A, s) == 3
+    # caller buffer too small for the packed layout
+    assert _st("tt_mxfp4_pack_swiglu", A, A, None, A, A, None, 16, 64, A, 100, s) == 8
+    # empty quantise is a no-op
+    assert _st("tt_quantize_mxfp4", None, 0, 64, None, None, None, s) == 0

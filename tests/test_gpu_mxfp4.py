@@ -1,0 +1,194 @@
+"""GPU parity of the MXFP4 quantiser, dequantiser, loader and gate/up SwiGLU
+matvec against the CPU oracle (bit-exact for codes/scales/dequantised
+weights; the float tolerance of tests/parity.py for h)."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from bit_weight_only_mxfp4_gb300 import synth
+
+from . import gpu_util as gu
+from .parity import assert_float_parity, bf16_to_f64
+
+pytestmark = pytest.mark.gpu
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available()
+    gu.ensure_lib()
+    assert gu.device_error() == 0
+
+
+def _special_rows(k=128):
+    g = np.random.default_rng(99)
+    rows = [
+        np.zeros(k),
+        -np.zeros(k),
+        g.standard_normal(k) * 1e-40,                       # subnormal fp32
+        g.standard_normal(k) * 1e30,
+        np.ldexp(1.0, g.integers(-130, 120, k)) * g.choice([-1, 1], k),
+        np.nextafter(np.ldexp(1.0, g.integers(-20, 20, k)), 0) * g.choice([-1, 1], k),
+        np.full(k, 3.4e38),
+        g.standard_normal(k) * 0.02,
+    ]
+    return np.array(rows, dtype=np.float32)
+
+
+def _check_quantize(w):
+    codes, scales, status = gu.quantize(w)
+    rc, rs, rst = oracle.mxfp4_quantize(w)
+    assert np.array_equal(gu.host(scales), rs)
+    assert np.array_equal(gu.host(codes), rc)
+    assert int(gu.host(status)[0]) == rst
+    return codes, scales
+
+
+def test_quantize_worked_block_matches_hand_values():
+    rows = []
+    for line in open(os.path.join(GOLD, "mxfp4_worked_block.txt")):
+        line = line.split("#", 1)[0].split()
+        if line:
+            rows.append(line)
+    w = np.array([[float(r[0]) for r in rows[1:]]], np.float32)
+    codes, scales, status = gu.quantize(w)
+    c = gu.host(codes)[0]
+    got = [(c[i // 2] >> (4 * (i % 2))) & 15 for i in range(32)]
+    assert int(gu.host(scales)[0, 0]) == int(rows[0][1])
+    assert got == [int(r[2]) for r in rows[1:]]
+
+
+def test_quantize_random_ragged():
+    g = synth.rng(90)
+    _check_quantize(synth.normal_f32(g, (37, 96), 0.02))
+
+
+def test_quantize_special_values():
+    _check_quantize(_special_rows())
+
+
+def test_quantize_nonfinite_blocks_flag_status():
+    w = _special_rows(64)
+    w[1, 3] = np.nan
+    w[5, 40] = np.inf
+    w[6, 63] = -np.inf
+    codes, scales = _check_quantize(w)
+    s = gu.host(scales)
+    assert s[1, 0] == 255 and s[5, 1] == 255 and s[6, 1] == 255
+
+
+def test_quantize_full_gate_up_layer():
+    d = synth.gate_up_inputs(synth.GATE_UP.wid, 0, synth.GATE_UP.n, synth.GATE_UP.k)
+    _check_quantize(d["wg"])
+    _check_quantize(d["wu"])
+
+
+def test_dequantize_bit_exact_all_codes_and_scales():
+    g = synth.rng(91)
+    n, k = 256, 64
+    codes = synth.random_bytes(g, (n, k // 2))
+    scales = g.integers(0, 256, size=(n, k // 32), dtype=np.uint8)
+    scales[:, 0] = np.arange(n) % 256  # every scale byte, including 0 and 255
+    out = gu.dev(np.zeros((n, k), np.float32))
+    from bit_weight_only_mxfp4_gb300 import thinmx
+    thinmx.tt_mxfp4_dequantize(gu.dev(codes), gu.dev(scales), n, k, out)
+    got = gu.host(out)
+    ref = oracle.mxfp4_dequantize(codes, scales)
+    with np.errstate(over="ignore", invalid="ignore"):
+        ref32 = ref.astype(np.float32)
+    nan = np.isnan(ref32)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref32[~nan].view(np.uint32))
+
+
+def _swiglu_case(n, k, m, postscale=True, wid=92, layer=0):
+    d = synth.gate_up_inputs(wid, layer, n, k, m=m, postscale=postscale)
+    gc, gs, st1 = gu.quantize(d["wg"])
+    uc, us, st2 = gu.quantize(d["wu"])
+    gp = None if d["pg"] is None else gu.dev(d["pg"])
+    up = None if d["pu"] is None else gu.dev(d["pu"])
+    packed = gu.pack_swiglu(gc, gs, gp, uc, us, up, n, k)
+    h = gu.swiglu(packed, n, k, d["x"])
+    ref = oracle.mxfp4_swiglu_matvec((gu.host(gc), gu.host(gs), d["pg"]),
+                                     (gu.host(uc), gu.host(us), d["pu"]), d["x"])
+    return h, ref, packed, d
+
+
+@pytest.mark.parametrize("n,k,m,post", [
+    (37, 96, 1, True), (64, 32, 1, False), (129, 1024, 1, True), (300, 2880, 1, True),
+    (50, 5120, 1, False), (33, 8192, 1, True), (21, 16384, 1, True),
+    (77, 2048, 2, True), (77, 2048, 3, False), (45, 5120, 4, True), (40, 2880, 8, True),
+    (31, 1056, 5, True), (19, 6144, 6, False),
+])
+def test_swiglu_matvec_shapes(n, k, m, post):
+    h, ref, _, _ = _swiglu_case(n, k, m, post)
+    assert h.shape == (m, n)
+    assert_float_parity(h, ref, f"n={n} k={k} m={m}")
+    assert gu.device_error() == 0
+
+
+def test_swiglu_matvec_full_gate_up_layer_is_deterministic():
+    c = synth.GATE_UP
+    h, ref, packed, d = _swiglu_case(c.n, c.k, 1, True, wid=c.wid)
+    rel, cos = assert_float_parity(h, ref, "gate/up 11008x2048")
+    h2 = gu.swiglu(packed, c.n, c.k, d["x"])
+    assert np.array_equal(h, h2)
+    # most outputs equal the oracle's own bf16 rounding
+    match = np.mean(h.ravel() == oracle.bf16_round_array(ref.ravel()))
+    assert match > 0.99, match
+
+
+def test_swiglu_identity_weights_give_silu_x_times_x():
+    k = 64
+    eye = np.eye(k, dtype=np.float32)
+    gc, gs, _ = gu.quantize(eye)
+    x = synth.normal_bf16(synth.rng(93), (2, k))
+    packed = gu.pack_swiglu(gc, gs, None, gc, gs, None, k, k)
+    h = gu.swiglu(packed, k, k, x)
+    xf = bf16_to_f64(x)
+    from scipy.special import expit
+    assert_float_parity(h, xf * expit(xf) * xf, "identity")
+
+
+def test_swiglu_large_activations_use_exact_prescale():
+    # activations far outside the f16 range still give exact products
+    n, k = 64, 256
+    d = synth.gate_up_inputs(94, 0, n, k, m=1)
+    x = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(d["x"]) * np.float32(2.0 ** 40))
+    gc, gs, _ = gu.quantize(d["wg"])
+    uc, us, _ = gu.quantize(d["wu"])
+    packed = gu.pack_swiglu(gc, gs, gu.dev(d["pg"]), uc, us, gu.dev(d["pu"]), n, k)
+    h = gu.swiglu(packed, n, k, x)
+    ref = oracle.mxfp4_swiglu_matvec((gu.host(gc), gu.host(gs), d["pg"]),
+                                     (gu.host(uc), gu.host(us), d["pu"]), x)
+    assert_float_parity(h, ref, "x * 2^40")
+
+
+def test_swiglu_full_batch_sweep_sampled_rows():
+    """Phi-4-sized gate/up (k=5120, n=17920) at m = 1..8 in the launch
+    configuration the benchmark times, checked on sampled rows."""
+    import torch
+    c = synth.SWEEP
+    g = synth.rng(c.wid, 0, 50)
+    wg = synth.normal_f32(synth.rng(c.wid, 0, 0), (c.n, c.k), synth.WEIGHT_STD)
+    wu = synth.normal_f32(synth.rng(c.wid, 0, 1), (c.n, c.k), synth.WEIGHT_STD)
+    pg = synth.uniform_f32(synth.rng(c.wid, 0, 3), (c.n,), 0.9, 1.1)
+    pu = synth.uniform_f32(synth.rng(c.wid, 0, 4), (c.n,), 0.9, 1.1)
+    gc, gs, _ = gu.quantize(wg)
+    uc, us, _ = gu.quantize(wu)
+    del wg, wu
+    packed = gu.pack_swiglu(gc, gs, gu.dev(pg), uc, us, gu.dev(pu), c.n, c.k)
+    rows = np.sort(g.choice(c.n, 192, replace=False))
+    rows = np.unique(np.concatenate([rows, [0, c.n - 1]]))
+    hgc, hgs, huc, hus = gu.host(gc), gu.host(gs), gu.host(uc), gu.host(us)
+    for m in [1, 2, 4, 8]:
+        x = synth.normal_bf16(synth.rng(c.wid, 0, 2), (m, c.k))
+        h = gu.swiglu(packed, c.n, c.k, x)
+        ref = oracle.mxfp4_swiglu_matvec((hgc[rows], hgs[rows], pg[rows]),
+                                         (huc[rows], hus[rows], pu[rows]), x)
+        assert_float_parity(h[:, rows], ref, f"sweep m={m}")
+    torch.cuda.empty_cache()
