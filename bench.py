@@ -208,6 +208,8 @@ def main():
     ap.add_argument("--impl", default="thinmx", choices=["thinmx", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--only", default=None, choices=["gate_up"],
+                    help="run one small workload only (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -235,6 +237,13 @@ def main():
     if pg:
         pg.barrier()
     thinmx.load()
+
+    if args.only == "gate_up":
+        hbm, peak_kind, _ = peaks()
+        r = single_gate_up(torch, synth, loader, thinmx, device, hbm, copies=4,
+                           reps=args.steps)
+        print(json.dumps({"only": "gate_up", **r}))
+        return 0
 
     cfg = synth.STACK
     layers = build_stack(torch, synth, loader, cfg, device)
@@ -375,14 +384,14 @@ def main():
     return 0
 
 
-def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
-    """Single gate/up layer (rotating copies > 2x L2) and the Phi-4 batch sweep."""
-    out = {}
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    # single SmolLM3 gate/up layer, M=1
+def single_gate_up(torch, synth, loader, thinmx, device, hbm, copies=None, reps=50):
+    """One SmolLM3 gate/up layer at M=1, cycling through enough weight copies
+    that their total exceeds twice the L2 size."""
     c = synth.GATE_UP
     per = gate_up_bytes(c.n, c.k, 1)
-    copies = max(4, int(2 * l2 // per) + 2)
+    if copies is None:
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        copies = max(4, int(2 * l2 // per) + 2)
     bufs = []
     for i in range(copies):
         wg = synth.torch_normal((c.n, c.k), synth.WEIGHT_STD, c.wid, i, 0, device)
@@ -396,12 +405,18 @@ def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
         bufs.append((packed, x, h))
     g = capture(torch, lambda: [thinmx.tt_mxfp4_swiglu_matvec(p, c.n, c.k, x, 1, h)
                                 for p, x, h in bufs])
-    ms = time_graph(torch, g, 50) / copies
-    out[c.name] = {"us": round(ms * 1e3, 3), "GBps": round(per / (ms * 1e-3) / 1e9, 1),
-                   "frac": round(per / (ms * 1e-3) / 1e9 / hbm, 4), "bytes": per,
-                   "rotating_copies": copies}
+    ms = time_graph(torch, g, reps) / copies
     del bufs, g
     torch.cuda.empty_cache()
+    return {c.name: {"us": round(ms * 1e3, 3), "GBps": round(per / (ms * 1e-3) / 1e9, 1),
+                     "frac": round(per / (ms * 1e-3) / 1e9 / hbm, 4), "bytes": per,
+                     "rotating_copies": copies}}
+
+
+def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
+    """Single gate/up layer (rotating copies > 2x L2) and the Phi-4 batch sweep."""
+    out = dict(single_gate_up(torch, synth, loader, thinmx, device, hbm))
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
 
     # Phi-4 gate/up batch sweep
     s = synth.SWEEP

@@ -3,7 +3,7 @@
 // synchronises, except the diagnostic tt_device_error_read.
 #include <mutex>
 
-#include "../../include/thinmx.h"
+#include "thinmx.h"
 #include "common.cuh"
 #include "launch.h"
 #include "layout.cuh"

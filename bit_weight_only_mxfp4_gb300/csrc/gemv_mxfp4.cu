@@ -34,6 +34,31 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 
+// Launch shape of the m = 1 kernel for k <= 3072 (x fits in 128 registers):
+// CTAs per SM, ring slots per warp and records per bulk copy.
+#ifndef TT_M1_CTAS_PER_SM
+#define TT_M1_CTAS_PER_SM 2
+#endif
+#ifndef TT_M1_SLOTS
+#define TT_M1_SLOTS 2
+#endif
+#ifndef TT_M1_RPC
+#define TT_M1_RPC 1
+#endif
+// Allow the next kernel to launch only once x has been read: its weight
+// prefetch would otherwise queue ahead of this kernel's x loads.
+#ifndef TT_M1_LATE_TRIGGER
+#define TT_M1_LATE_TRIGGER 0
+#endif
+// m = 1 with x staged in shared memory (1) or held in registers (0), and the
+// warps per CTA of the shared-memory variant.
+#ifndef TT_M1_XSMEM
+#define TT_M1_XSMEM 1
+#endif
+#ifndef TT_M1_WARPS
+#define TT_M1_WARPS 16
+#endif
+
 // 32 E2M1 codes (one 16-byte chunk) dotted with 32 f16 values (16 f16x2),
 // fp32 accumulation in four chains.
 __device__ __forceinline__ float dot32(const uint4& c, const uint32_t* xv) {
@@ -73,14 +98,16 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float v) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 
-// Per-warp ring of bulk-copy slots over the warp's records r0 + warp + j*kWarps.
+// Per-warp ring of bulk-copy slots.  Item j of the warp is a "unit" of up to
+// `rpc` consecutive records starting at record first(j); one bulk copy
+// brings the whole unit into slot j % slots.
 struct WarpRing {
   uint8_t* base;
   uint64_t* bars;
   int slots;
-  int bytes;
-  const uint8_t* src;  // first record of the CTA + warp offset
-  int64_t stride;      // bytes between consecutive records of this warp
+  int slot_bytes;     // rpc * record bytes
+  int rec_bytes;
+  const uint8_t* packed;
   uint64_t policy;
 
   __device__ void init(int lane) {
@@ -90,34 +117,85 @@ struct WarpRing {
     }
     __syncwarp();
   }
-  __device__ void issue(int j) {  // lane 0 only
+  // lane 0 only: copy `count` records starting at record `first` into the
+  // slot of item j.
+  __device__ void issue(int j, int first, int count) {
     const int s = j % slots;
     const uint32_t bar = smem_u32(&bars[s]);
-    mbar_arrive_expect_tx(bar, uint32_t(bytes));
-    bulk_g2s(smem_u32(base + (size_t)s * bytes), src + (int64_t)j * stride, uint32_t(bytes), bar,
-             policy);
+    const uint32_t bytes = uint32_t(count * rec_bytes);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(smem_u32(base + (size_t)s * slot_bytes), packed + (int64_t)first * rec_bytes, bytes,
+             bar, policy);
   }
-  // Returns the slot of record j once its copy has landed, nullptr after a
+  // Returns the slot of item j once its copy has landed, nullptr after a
   // timeout (warp-uniform).
   __device__ const uint8_t* wait(int j) {
     const int s = j % slots;
     const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), uint32_t((j / slots) & 1));
     if (!__all_sync(0xffffffffu, ok)) return nullptr;
-    return base + (size_t)s * bytes;
+    return base + (size_t)s * slot_bytes;
   }
-  // After a timeout at record j: give the copies already issued a bounded
+  // After a timeout at item j: give the copies already issued a bounded
   // chance to land before the CTA may exit.
-  __device__ void drain(int j, int nrec) {
-    const int issued = min(nrec, j + slots);
+  __device__ void drain(int j, int nitems) {
+    const int issued = min(nitems, j + slots);
     for (int t = j + 1; t < issued; ++t)
       (void)mbar_wait_bounded(smem_u32(&bars[t % slots]), uint32_t((t / slots) & 1));
   }
 };
 
+// Sums four values over the warp in six shuffles.  Lanes 0-7 get the total
+// of a, 8-15 of b, 16-23 of c, 24-31 of d.
+__device__ __forceinline__ float warp_sum4(float a, float b, float c, float d, int lane) {
+  const bool hi16 = (lane & 16) != 0;
+  float k0 = hi16 ? c : a, k1 = hi16 ? d : b;
+  const float s0 = hi16 ? a : c, s1 = hi16 ? b : d;
+  k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+  k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+  const bool hi8 = (lane & 8) != 0;
+  float k = hi8 ? k1 : k0;
+  const float s = hi8 ? k0 : k1;
+  k += __shfl_xor_sync(0xffffffffu, s, 8);
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  return k;
+}
+
+// The SwiGLU epilogue of a warp's records, batched: lane (t % 32) keeps the
+// postscaled g and u of the warp's t-th record, and every 32 records (or at
+// the end) all lanes apply silu(g)*u and store bf16 together, instead of one
+// lane per record.
+struct EpilogueBatch {
+  float g = 0.f, u = 0.f;
+  int row = -1;
+  int fill = 0;
+
+  // v holds a reduced value on every lane; gsrc/usrc are lanes holding this
+  // record's g and u sums.
+  __device__ void put(float v, int gsrc, int usrc, float pg, float pu, float inv, int r,
+                      int lane) {
+    const float gg = __shfl_sync(0xffffffffu, v, gsrc);
+    const float uu = __shfl_sync(0xffffffffu, v, usrc);
+    if (lane == fill) {
+      g = gg * inv * pg;
+      u = uu * inv * pu;
+      row = r;
+    }
+    ++fill;
+  }
+  __device__ void flush(uint16_t* __restrict__ h) {
+    if (row >= 0) h[row] = f32_to_bf16_rne(silu_mul(g, u));
+    row = -1;
+    fill = 0;
+  }
+};
+
 // ---------------------------------------------------------------------------
-// m = 1, x held in registers.  NB = number of 1024-wide K chunks (k <= 1024*NB).
+// m = 1, x held in registers.  NB = number of 1024-wide K chunks
+// (k <= 1024*NB); RPC = records per bulk copy (1 or 2).
 // ---------------------------------------------------------------------------
-template <int NB>
+template <int NB, int RPC>
 __global__ void __launch_bounds__(kThreads, (NB <= 3 ? 2 : 1))
     swiglu_mxfp4_m1_kernel(const uint8_t* __restrict__ packed, int n, int k,
                            const uint16_t* __restrict__ x, uint16_t* __restrict__ h, int slots,
@@ -127,24 +205,36 @@ __global__ void __launch_bounds__(kThreads, (NB <= 3 ? 2 : 1))
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r0 = int((int64_t)n * blockIdx.x / gridDim.x);
   const int r1 = int((int64_t)n * (blockIdx.x + 1) / gridDim.x);
-  const int cnt = r1 - r0;
-  const int nrec = cnt > warp ? (cnt - warp + kWarps - 1) / kWarps : 0;
+  const int units = (r1 - r0 + RPC - 1) / RPC;
+  const int nitems = units > warp ? (units - warp + kWarps - 1) / kWarps : 0;
 
   WarpRing ring;
   ring.slots = slots;
-  ring.bytes = L.bytes;
-  ring.base = smem + (size_t)warp * slots * L.bytes;
-  ring.bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * slots * L.bytes) + warp * slots;
-  ring.src = packed + (int64_t)(r0 + warp) * L.bytes;
-  ring.stride = (int64_t)kWarps * L.bytes;
+  ring.rec_bytes = L.bytes;
+  ring.slot_bytes = RPC * L.bytes;
+  ring.base = smem + (size_t)warp * slots * ring.slot_bytes;
+  ring.bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * slots * ring.slot_bytes) +
+              warp * slots;
+  ring.packed = packed;
   ring.policy = l2_evict_first_policy();
   ring.init(lane);
 
-  pdl_allow_next_grid();
+  auto first_of = [&](int j) { return r0 + (warp + j * kWarps) * RPC; };
+  auto count_of = [&](int first) { return min(RPC, r1 - first); };
+
+  if (!TT_M1_LATE_TRIGGER) pdl_allow_next_grid();
   // Weights do not depend on the previous kernel: start streaming them now.
   if (lane == 0)
-    for (int j = 0; j < min(slots, nrec); ++j) ring.issue(j);
+    for (int j = 0; j < min(slots, nitems); ++j) ring.issue(j, first_of(j), count_of(first_of(j)));
   pdl_wait_prior_grid();
+
+  // x is read from global memory once per CTA (not once per warp: thousands
+  // of warps fetching the same few lines would queue on a few L2 slices).
+  uint4* xs = reinterpret_cast<uint4*>(
+      smem + (size_t)kWarps * slots * ring.slot_bytes + (size_t)kWarps * slots * 8);
+  for (int c = threadIdx.x; c < (k >> 3); c += kThreads)
+    xs[c] = reinterpret_cast<const uint4*>(x)[c];
+  __syncthreads();
 
   // x slice of this lane -> f16x2 registers, prescaled by 2^sx (exact).
   uint32_t xr[NB][16];
@@ -155,9 +245,8 @@ __global__ void __launch_bounds__(kThreads, (NB <= 3 ? 2 : 1))
     uint4 q[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
                   make_uint4(0, 0, 0, 0)};
     if (b < L.nblk) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)b * 32);
 #pragma unroll
-      for (int t = 0; t < 4; ++t) q[t] = src[t];
+      for (int t = 0; t < 4; ++t) q[t] = xs[b * 4 + t];
     }
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -181,39 +270,205 @@ __global__ void __launch_bounds__(kThreads, (NB <= 3 ? 2 : 1))
     for (int t = 0; t < 16; ++t)
       xr[i][t] = pack_f16x2_scaled(bf16_bits_to_f32(xr[i][t] & 0xFFFFu),
                                    bf16_bits_to_f32(xr[i][t] >> 16), two_s);
+  if (TT_M1_LATE_TRIGGER) pdl_allow_next_grid();
+  const float inv = scalbnf(1.0f, -sx);  // exact power of two
+  EpilogueBatch ep;
 
-  for (int j = 0; j < nrec; ++j) {
-    const uint8_t* rec = ring.wait(j);
-    if (rec == nullptr) {
+  for (int j = 0; j < nitems; ++j) {
+    const uint8_t* slot = ring.wait(j);
+    if (slot == nullptr) {
       if (lane == 0) flag_error(err, kErrTimeout);
-      ring.drain(j, nrec);
+      ring.drain(j, nitems);
       return;
     }
-    float ag = 0.f, au = 0.f;
+    const int first = first_of(j);
+    const int count = count_of(first);
+    float ag[RPC], au[RPC], pg[RPC], pu[RPC];
+#pragma unroll
+    for (int rr = 0; rr < RPC; ++rr) {
+      ag[rr] = au[rr] = 0.f;
+      pg[rr] = pu[rr] = 1.f;
+      if (rr < count) {
+        const uint8_t* rec = slot + rr * L.bytes;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const int b = 32 * i + lane;
+          if (b < L.nblk) {
+            const uint4 cg = *reinterpret_cast<const uint4*>(rec + L.gate_codes() + b * 16);
+            const uint4 cu = *reinterpret_cast<const uint4*>(rec + L.up_codes() + b * 16);
+            const float sg = e8m0_to_f32(rec[L.gate_scales() + b]);
+            const float su = e8m0_to_f32(rec[L.up_scales() + b]);
+            ag[rr] = fmaf(dot32(cg, xr[i]), sg, ag[rr]);
+            au[rr] = fmaf(dot32(cu, xr[i]), su, au[rr]);
+          }
+        }
+        pg[rr] = *reinterpret_cast<const float*>(rec + L.post);
+        pu[rr] = *reinterpret_cast<const float*>(rec + L.post + 4);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && j + slots < nitems) {
+      const int f = first_of(j + slots);
+      ring.issue(j + slots, f, count_of(f));
+    }
+    if constexpr (RPC == 2) {
+      // lanes 0-7: g0, 8-15: u0, 16-23: g1, 24-31: u1
+      const float v = warp_sum4(ag[0], au[0], ag[1], au[1], lane);
+      if (ep.fill > 30) ep.flush(h);
+      ep.put(v, 0, 8, pg[0], pu[0], inv, first, lane);
+      if (count > 1) ep.put(v, 16, 24, pg[1], pu[1], inv, first + 1, lane);
+    } else {
+      const float v = warp_sum2(ag[0], au[0], lane);  // lanes 0-15: g, 16-31: u
+      if (ep.fill > 31) ep.flush(h);
+      ep.put(v, 0, 16, pg[0], pu[0], inv, first, lane);
+    }
+  }
+  ep.flush(h);
+}
+
+// ---------------------------------------------------------------------------
+// m = 1, x staged once per CTA in shared memory as f16 (prescaled by 2^sx),
+// laid out chunk-major: 16-byte chunk q (0..3) of block b at xs[q*nblk + b],
+// so a warp reading blocks b..b+31 touches 32 consecutive 16-byte words.
+// Keeping x out of registers lets WARPS warps per CTA stay resident while
+// the next kernel's CTA (programmatic dependent launch) shares the SM.
+// NB = number of 1024-wide K chunks; RPC = records per bulk copy.
+// ---------------------------------------------------------------------------
+template <int NB, int RPC, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 2)
+    swiglu_mxfp4_m1x_kernel(const uint8_t* __restrict__ packed, int n, int k,
+                            const uint16_t* __restrict__ x, uint16_t* __restrict__ h, int slots,
+                            int32_t* err) {
+  constexpr int THREADS = WARPS * 32;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const SwigluRecord L(k);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r0 = int((int64_t)n * blockIdx.x / gridDim.x);
+  const int r1 = int((int64_t)n * (blockIdx.x + 1) / gridDim.x);
+  const int units = (r1 - r0 + RPC - 1) / RPC;
+  const int nitems = units > warp ? (units - warp + WARPS - 1) / WARPS : 0;
+
+  const size_t ring_bytes = (size_t)WARPS * slots * RPC * L.bytes;
+  WarpRing ring;
+  ring.slots = slots;
+  ring.rec_bytes = L.bytes;
+  ring.slot_bytes = RPC * L.bytes;
+  ring.base = smem + (size_t)warp * slots * ring.slot_bytes;
+  ring.bars = reinterpret_cast<uint64_t*>(smem + ring_bytes) + warp * slots;
+  ring.packed = packed;
+  ring.policy = l2_evict_first_policy();
+  uint4* xraw = reinterpret_cast<uint4*>(smem + ring_bytes + (size_t)WARPS * slots * 8);
+  uint4* xs = xraw + (k >> 3);
+  float* red = reinterpret_cast<float*>(xs + (k >> 3));
+  ring.init(lane);
+
+  auto first_of = [&](int j) { return r0 + (warp + j * WARPS) * RPC; };
+  auto count_of = [&](int first) { return min(RPC, r1 - first); };
+
+  if (!TT_M1_LATE_TRIGGER) pdl_allow_next_grid();
+  // Weights do not depend on the previous kernel: start streaming them now.
+  if (lane == 0)
+    for (int j = 0; j < min(slots, nitems); ++j) ring.issue(j, first_of(j), count_of(first_of(j)));
+  pdl_wait_prior_grid();
+
+  // x: one global read per CTA, CTA-wide max |x| -> exact power-of-two
+  // prescale, then f16 in the chunk-major layout.
+  const int nchunk16 = k >> 3;
+  float mx = 0.f;
+  for (int c = threadIdx.x; c < nchunk16; c += THREADS) {
+    const uint4 v = reinterpret_cast<const uint4*>(x)[c];
+    xraw[c] = v;
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_bits_to_f32(v.x & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.x >> 16))),
+                         fmaxf(fabsf(bf16_bits_to_f32(v.y & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.y >> 16)))));
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_bits_to_f32(v.z & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.z >> 16))),
+                         fmaxf(fabsf(bf16_bits_to_f32(v.w & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.w >> 16)))));
+  }
+  mx = warp_max(mx);
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  float gmax = red[0];
+#pragma unroll
+  for (int w = 1; w < WARPS; ++w) gmax = fmaxf(gmax, red[w]);
+  const int sx = min(f16_prescale_exponent(gmax), 127);
+  const float two_s = scalbnf(1.0f, sx);
+  for (int c = threadIdx.x; c < nchunk16; c += THREADS) {
+    const uint4 v = xraw[c];
+    uint4 o;
+    o.x = pack_f16x2_scaled(bf16_bits_to_f32(v.x & 0xFFFFu), bf16_bits_to_f32(v.x >> 16), two_s);
+    o.y = pack_f16x2_scaled(bf16_bits_to_f32(v.y & 0xFFFFu), bf16_bits_to_f32(v.y >> 16), two_s);
+    o.z = pack_f16x2_scaled(bf16_bits_to_f32(v.z & 0xFFFFu), bf16_bits_to_f32(v.z >> 16), two_s);
+    o.w = pack_f16x2_scaled(bf16_bits_to_f32(v.w & 0xFFFFu), bf16_bits_to_f32(v.w >> 16), two_s);
+    xs[(c & 3) * L.nblk + (c >> 2)] = o;  // chunk q = c % 4 of block b = c / 4
+  }
+  __syncthreads();
+  if (TT_M1_LATE_TRIGGER) pdl_allow_next_grid();
+  const float inv = scalbnf(1.0f, -sx);  // exact power of two
+  EpilogueBatch ep;
+
+  for (int j = 0; j < nitems; ++j) {
+    const uint8_t* slot = ring.wait(j);
+    if (slot == nullptr) {
+      if (lane == 0) flag_error(err, kErrTimeout);
+      ring.drain(j, nitems);
+      return;
+    }
+    const int first = first_of(j);
+    const int count = count_of(first);
+    float ag[RPC], au[RPC];
+#pragma unroll
+    for (int rr = 0; rr < RPC; ++rr) ag[rr] = au[rr] = 0.f;
 #pragma unroll
     for (int i = 0; i < NB; ++i) {
       const int b = 32 * i + lane;
       if (b < L.nblk) {
-        const uint4 cg = *reinterpret_cast<const uint4*>(rec + L.gate_codes() + b * 16);
-        const uint4 cu = *reinterpret_cast<const uint4*>(rec + L.up_codes() + b * 16);
-        const float sg = e8m0_to_f32(rec[L.gate_scales() + b]);
-        const float su = e8m0_to_f32(rec[L.up_scales() + b]);
-        ag = fmaf(dot32(cg, xr[i]), sg, ag);
-        au = fmaf(dot32(cu, xr[i]), su, au);
+        uint32_t xv[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 t = xs[q * L.nblk + b];
+          xv[4 * q + 0] = t.x;
+          xv[4 * q + 1] = t.y;
+          xv[4 * q + 2] = t.z;
+          xv[4 * q + 3] = t.w;
+        }
+#pragma unroll
+        for (int rr = 0; rr < RPC; ++rr) {
+          if (rr < count) {
+            const uint8_t* rec = slot + rr * L.bytes;
+            const uint4 cg = *reinterpret_cast<const uint4*>(rec + L.gate_codes() + b * 16);
+            const uint4 cu = *reinterpret_cast<const uint4*>(rec + L.up_codes() + b * 16);
+            const float sg = e8m0_to_f32(rec[L.gate_scales() + b]);
+            const float su = e8m0_to_f32(rec[L.up_scales() + b]);
+            ag[rr] = fmaf(dot32(cg, xv), sg, ag[rr]);
+            au[rr] = fmaf(dot32(cu, xv), su, au[rr]);
+          }
+        }
       }
     }
-    const float pg = *reinterpret_cast<const float*>(rec + L.post);
-    const float pu = *reinterpret_cast<const float*>(rec + L.post + 4);
+    float pg[RPC], pu[RPC];
+#pragma unroll
+    for (int rr = 0; rr < RPC; ++rr) {
+      const uint8_t* rec = slot + rr * L.bytes;
+      pg[rr] = rr < count ? *reinterpret_cast<const float*>(rec + L.post) : 1.f;
+      pu[rr] = rr < count ? *reinterpret_cast<const float*>(rec + L.post + 4) : 1.f;
+    }
     __syncwarp();
-    if (lane == 0 && j + slots < nrec) ring.issue(j + slots);
-    const float v = warp_sum2(ag, au, lane);
-    const float vu = __shfl_sync(0xffffffffu, v, 16);
-    if (lane == 0) {
-      const float g = scalbnf(v, -sx) * pg;
-      const float u = scalbnf(vu, -sx) * pu;
-      h[r0 + warp + j * kWarps] = f32_to_bf16_rne(silu_mul(g, u));
+    if (lane == 0 && j + slots < nitems) {
+      const int f = first_of(j + slots);
+      ring.issue(j + slots, f, count_of(f));
+    }
+    if constexpr (RPC == 2) {
+      // lanes 0-7: g0, 8-15: u0, 16-23: g1, 24-31: u1
+      const float v = warp_sum4(ag[0], au[0], ag[1], au[1], lane);
+      if (ep.fill > 30) ep.flush(h);
+      ep.put(v, 0, 8, pg[0], pu[0], inv, first, lane);
+      if (count > 1) ep.put(v, 16, 24, pg[1], pu[1], inv, first + 1, lane);
+    } else {
+      const float v = warp_sum2(ag[0], au[0], lane);  // lanes 0-15: g, 16-31: u
+      if (ep.fill > 31) ep.flush(h);
+      ep.put(v, 0, 16, pg[0], pu[0], inv, first, lane);
     }
   }
+  ep.flush(h);
 }
 
 // ---------------------------------------------------------------------------
@@ -243,17 +498,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   WarpRing ring;
   ring.slots = slots;
-  ring.bytes = L.bytes;
+  ring.rec_bytes = L.bytes;
+  ring.slot_bytes = L.bytes;
   ring.base = smem + (size_t)warp * slots * L.bytes;
   ring.bars = bars_all + warp * slots;
-  ring.src = packed + (int64_t)(r0 + warp) * L.bytes;
-  ring.stride = (int64_t)kWarps * L.bytes;
+  ring.packed = packed;
   ring.policy = l2_evict_first_policy();
   ring.init(lane);
 
   pdl_allow_next_grid();
   if (lane == 0)
-    for (int j = 0; j < min(slots, nrec); ++j) ring.issue(j);
+    for (int j = 0; j < min(slots, nrec); ++j) ring.issue(j, r0 + warp + j * kWarps, 1);
   pdl_wait_prior_grid();
 
   // Per-row max |x| -> prescale exponent; then convert x into shared memory.
@@ -328,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float pg = *reinterpret_cast<const float*>(rec + L.post);
     const float pu = *reinterpret_cast<const float*>(rec + L.post + 4);
     __syncwarp();
-    if (lane == 0 && j + slots < nrec) ring.issue(j + slots);
+    if (lane == 0 && j + slots < nrec) ring.issue(j + slots, r0 + warp + (j + slots) * kWarps, 1);
     const int r = r0 + warp + j * kWarps;
 #pragma unroll
     for (int i = 0; i < MT; ++i) {
@@ -381,19 +636,68 @@ cudaError_t launch_pdl_m(Kern kern, int grid, int smem, cudaStream_t s, bool pdl
 // an SM, so the next kernel's CTA can start streaming while this one ends.
 constexpr int kRingBudget = 100 * 1024;
 
-template <int NB>
+template <int NB, int RPC>
 cudaError_t run_m1(const DeviceInfo& di, const uint8_t* packed, int n, int k, const uint16_t* x,
                    uint16_t* h, cudaStream_t s, bool pdl) {
+  // Two CTAs per SM (16 resident warps) with two slots per warp while x fits
+  // in 128 registers; one CTA per SM with deeper rings for wider K.
   const SwigluRecord L(k);
-  int slots = kRingBudget / (kWarps * L.bytes);
-  slots = slots < 2 ? 2 : (slots > 6 ? 6 : slots);
-  const int smem = kWarps * slots * (L.bytes + 8);
+  const int ctas_per_sm = NB <= 3 ? TT_M1_CTAS_PER_SM : 1;
+  const int slot_bytes = RPC * L.bytes;
+  int slots = kRingBudget / (kWarps * (slot_bytes + 8));
+  slots = slots < 2 ? 2 : (slots > 4 ? 4 : slots);
+  if (NB <= 3) slots = TT_M1_SLOTS;
+  const int smem = kWarps * slots * (slot_bytes + 8) + 2 * k;  // ring, barriers, x
   if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
-  auto kern = swiglu_mxfp4_m1_kernel<NB>;
+  auto kern = swiglu_mxfp4_m1_kernel<NB, RPC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int grid = n < di.sms ? n : di.sms;
+  int grid = ctas_per_sm * di.sms;
+  const int units = (n + RPC - 1) / RPC;
+  if (grid > units) grid = units;
   return launch_pdl(kern, grid, smem, s, pdl, packed, n, k, x, h, slots, di.error_word);
+}
+
+template <typename Kern>
+cudaError_t launch_threads(Kern kern, int grid, int threads, int smem, cudaStream_t s, bool pdl,
+                           const uint8_t* packed, int n, int k, const uint16_t* x, uint16_t* h,
+                           int slots, int32_t* err) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, packed, n, k, x, h, slots, err);
+}
+
+// Shared memory of one CTA of the x-in-shared-memory kernel: at most half an
+// SM, so that the next kernel's CTA fits beside it.
+constexpr int kHalfSmBudget = 110 * 1024;
+
+template <int NB, int RPC, int WARPS>
+cudaError_t run_m1x(const DeviceInfo& di, const uint8_t* packed, int n, int k, const uint16_t* x,
+                    uint16_t* h, cudaStream_t s, bool pdl) {
+  const SwigluRecord L(k);
+  const int slot_bytes = RPC * L.bytes;
+  const int fixed = 4 * k + WARPS * 4 + 16;  // raw + f16 x, per-warp maxima
+  int slots = (kHalfSmBudget - fixed) / (WARPS * (slot_bytes + 8));
+  if (slots > TT_M1_SLOTS) slots = TT_M1_SLOTS;
+  if (slots < 1) slots = 1;
+  const int smem = WARPS * slots * (slot_bytes + 8) + fixed;
+  if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
+  auto kern = swiglu_mxfp4_m1x_kernel<NB, RPC, WARPS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int grid = di.sms;
+  const int units = (n + RPC - 1) / RPC;
+  if (grid > units) grid = units;
+  return launch_threads(kern, grid, WARPS * 32, smem, s, pdl, packed, n, k, x, h, slots,
+                        di.error_word);
 }
 
 template <int MT>
@@ -402,7 +706,9 @@ cudaError_t run_mt(const DeviceInfo& di, const uint8_t* packed, int n, int k, in
   const SwigluRecord L(k);
   const int xs_bytes = MT * 2 * k + MT * 4 + MT * kWarps * 4 + 16;
   const int avail = di.smem_optin - xs_bytes;
-  int slots = (avail < kRingBudget ? avail : kRingBudget) / (kWarps * (L.bytes + 8));
+  const int per_slot = kWarps * (L.bytes + 8);
+  int slots = (avail < kRingBudget ? avail : kRingBudget) / per_slot;
+  if (slots < 2) slots = avail / per_slot < 2 ? avail / per_slot : 2;  // wide K: use more smem
   if (slots < 1) return cudaErrorInvalidConfiguration;
   if (slots > 6) slots = 6;
   const int smem = kWarps * slots * (L.bytes + 8) + xs_bytes;
@@ -419,15 +725,29 @@ cudaError_t launch_swiglu_mxfp4_cc(const uint8_t* packed, int n, int k, const ui
                                    uint16_t* h, cudaStream_t s, bool pdl) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorNoDevice;
+  if (m == 1 && TT_M1_XSMEM) {
+    const int nb = (k / 32 + 31) / 32;
+    switch (nb) {
+      case 1: return run_m1x<1, TT_M1_RPC, TT_M1_WARPS>(*di, packed, n, k, x, h, s, pdl);
+      case 2: return run_m1x<2, TT_M1_RPC, TT_M1_WARPS>(*di, packed, n, k, x, h, s, pdl);
+      case 3: return run_m1x<3, TT_M1_RPC, TT_M1_WARPS>(*di, packed, n, k, x, h, s, pdl);
+      case 4: return run_m1x<4, 1, TT_M1_WARPS>(*di, packed, n, k, x, h, s, pdl);
+      case 5: return run_m1x<5, 1, TT_M1_WARPS>(*di, packed, n, k, x, h, s, pdl);
+      case 6: return run_m1x<6, 1, TT_M1_WARPS>(*di, packed, n, k, x, h, s, pdl);
+      case 7: return run_m1x<7, 1, TT_M1_WARPS>(*di, packed, n, k, x, h, s, pdl);
+      case 8: return run_m1x<8, 1, TT_M1_WARPS>(*di, packed, n, k, x, h, s, pdl);
+      default: break;
+    }
+  }
   if (m == 1) {
     const int nb = (k / 32 + 31) / 32;
     switch (nb) {
-      case 1: return run_m1<1>(*di, packed, n, k, x, h, s, pdl);
-      case 2: return run_m1<2>(*di, packed, n, k, x, h, s, pdl);
-      case 3: return run_m1<3>(*di, packed, n, k, x, h, s, pdl);
-      case 4: return run_m1<4>(*di, packed, n, k, x, h, s, pdl);
-      case 5: return run_m1<5>(*di, packed, n, k, x, h, s, pdl);
-      case 6: return run_m1<6>(*di, packed, n, k, x, h, s, pdl);
+      case 1: return run_m1<1, TT_M1_RPC>(*di, packed, n, k, x, h, s, pdl);
+      case 2: return run_m1<2, TT_M1_RPC>(*di, packed, n, k, x, h, s, pdl);
+      case 3: return run_m1<3, TT_M1_RPC>(*di, packed, n, k, x, h, s, pdl);
+      case 4: return run_m1<4, 1>(*di, packed, n, k, x, h, s, pdl);
+      case 5: return run_m1<5, 1>(*di, packed, n, k, x, h, s, pdl);
+      case 6: return run_m1<6, 1>(*di, packed, n, k, x, h, s, pdl);
       default: return run_mt<1>(*di, packed, n, k, 1, x, h, s, pdl);
     }
   }
