@@ -45,15 +45,43 @@ constexpr int kThreads = kWarps * 32;
 #ifndef TT_M1_RPC
 #define TT_M1_RPC 1
 #endif
-// Allow the next kernel to launch only once x has been read: its weight
-// prefetch would otherwise queue ahead of this kernel's x loads.
+// When the register-x and shared-x kernels allow the dependent launch:
+// 0 = at entry (measured best), 1 = once x has been read.
 #ifndef TT_M1_LATE_TRIGGER
 #define TT_M1_LATE_TRIGGER 0
+#endif
+// Each CTA prefetches its whole weight range into L2 at launch, so that the
+// number of bytes in flight is not limited by the shared-memory ring.
+#ifndef TT_M1_L2PF
+#define TT_M1_L2PF 0
 #endif
 // m = 1 with x staged in shared memory (1) or held in registers (0), and the
 // warps per CTA of the shared-memory variant.
 #ifndef TT_M1_XSMEM
 #define TT_M1_XSMEM 1
+#endif
+// m = 1 through the stage-pipelined, warp-specialised kernel (and its ring
+// depth cap).
+#ifndef TT_M1_STAGED
+#define TT_M1_STAGED 0
+#endif
+#ifndef TT_M1X_CTAS_PER_SM
+#define TT_M1X_CTAS_PER_SM 1
+#endif
+#ifndef TT_M1S_SLOTS
+#define TT_M1S_SLOTS 8
+#endif
+#ifndef TT_M1S_INTERLEAVE
+#define TT_M1S_INTERLEAVE 0
+#endif
+// When the dependent launch is allowed: 0 = at entry, 1 = once the producer
+// has issued the last copy of this kernel.
+#ifndef TT_M1S_TRIGGER
+#define TT_M1S_TRIGGER 1
+#endif
+// Queue the stages beyond the ring into L2 at entry.
+#ifndef TT_M1S_L2PF
+#define TT_M1S_L2PF 1
 #endif
 #ifndef TT_M1_WARPS
 #define TT_M1_WARPS 16
@@ -366,6 +394,15 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   auto count_of = [&](int first) { return min(RPC, r1 - first); };
 
   if (!TT_M1_LATE_TRIGGER) pdl_allow_next_grid();
+  if (TT_M1_L2PF) {
+    // The CTA's records are contiguous: ask L2 for all of them now, in
+    // 16 KB pieces spread over the CTA's threads.
+    const char* base = reinterpret_cast<const char*>(packed) + (int64_t)r0 * L.bytes;
+    const int64_t total = (int64_t)(r1 - r0) * L.bytes;
+    constexpr int64_t kPiece = 16384;
+    for (int64_t off = (int64_t)threadIdx.x * kPiece; off < total; off += (int64_t)THREADS * kPiece)
+      bulk_prefetch_l2(base + off, uint32_t(min(kPiece, total - off)));
+  }
   // Weights do not depend on the previous kernel: start streaming them now.
   if (lane == 0)
     for (int j = 0; j < min(slots, nitems); ++j) ring.issue(j, first_of(j), count_of(first_of(j)));
@@ -375,8 +412,9 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   // prescale, then f16 in the chunk-major layout.
   const int nchunk16 = k >> 3;
   float mx = 0.f;
+  const uint64_t x_policy = l2_evict_last_policy();
   for (int c = threadIdx.x; c < nchunk16; c += THREADS) {
-    const uint4 v = reinterpret_cast<const uint4*>(x)[c];
+    const uint4 v = ld_global_v4_hint(reinterpret_cast<const uint4*>(x) + c, x_policy);
     xraw[c] = v;
     mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_bits_to_f32(v.x & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.x >> 16))),
                          fmaxf(fabsf(bf16_bits_to_f32(v.y & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.y >> 16)))));
@@ -469,6 +507,184 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     }
   }
   ep.flush(h);
+}
+
+// ---------------------------------------------------------------------------
+// m = 1, stage-pipelined and warp-specialised.
+//
+// The CTA's records are consumed in stages of R consecutive records, each
+// brought in by ONE bulk copy into a ring of `slots` shared-memory stages.
+// Warp NB*R (the producer) issues the copies and, once every consumer warp
+// has released a stage, runs the SwiGLU epilogue of its records and refills
+// the slot.  Consumer warp w owns K chunk c = w % NB (lane l owns block
+// 32c + l) of the stage's record w / NB, so it keeps only that 1024-wide
+// slice of x (16 registers) and per stage does two 32-weight dot products,
+// one warp reduction and one arrive: no per-record control flow.
+// ---------------------------------------------------------------------------
+template <int NB, int R>
+__global__ void __launch_bounds__((NB * R + 1) * 32, 1)
+    swiglu_mxfp4_m1s_kernel(const uint8_t* __restrict__ packed, int n, int k,
+                            const uint16_t* __restrict__ x, uint16_t* __restrict__ h, int slots,
+                            int32_t* err) {
+  constexpr int W = NB * R;  // consumer warps
+  extern __shared__ __align__(128) uint8_t smem[];
+  const SwigluRecord L(k);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // Stage t of this CTA covers records [first(t), first(t) + cnt(t)).  With
+  // TT_M1S_INTERLEAVE the CTAs take global stages round-robin, so the whole
+  // grid sweeps the matrix front to back; otherwise each CTA owns a
+  // contiguous range.
+#if TT_M1S_INTERLEAVE
+  const int nstage_all = (n + R - 1) / R;
+  const int stages = nstage_all > (int)blockIdx.x
+                         ? (nstage_all - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+                         : 0;
+  auto first = [&](int t) { return ((int)blockIdx.x + t * (int)gridDim.x) * R; };
+  auto cnt = [&](int t) { return min(R, n - first(t)); };
+#else
+  const int r0 = int((int64_t)n * blockIdx.x / gridDim.x);
+  const int r1 = int((int64_t)n * (blockIdx.x + 1) / gridDim.x);
+  const int stages = (r1 - r0 + R - 1) / R;
+  auto first = [&](int t) { return r0 + t * R; };
+  auto cnt = [&](int t) { return min(R, r1 - (r0 + t * R)); };
+#endif
+  const int stage_bytes = R * L.bytes;
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)slots * stage_bytes);
+  uint64_t* empty = full + slots;
+  float* part = reinterpret_cast<float*>(empty + slots);  // [slots][R][NB][2]
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < slots; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), W * 32);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (TT_M1S_TRIGGER == 0) pdl_allow_next_grid();
+
+  if (warp == W) {
+    // ---------------- producer and epilogue warp ----------------
+    const uint64_t policy = l2_evict_first_policy();
+    int issued = 0;
+    auto issue = [&](int t) {  // lane 0 only
+      const int s = t % slots;
+      const uint32_t bytes = uint32_t(cnt(t) * L.bytes);
+      mbar_arrive_expect_tx(smem_u32(&full[s]), bytes);
+      bulk_g2s(smem_u32(ring + (size_t)s * stage_bytes), packed + (int64_t)first(t) * L.bytes,
+               bytes, smem_u32(&full[s]), policy);
+    };
+    // Weights do not depend on the previous kernel: start streaming them now.
+    if (lane == 0) {
+      for (int t = 0; t < min(slots, stages); ++t) issue(t);
+      // The stages that do not fit the ring yet: queue them into L2 now, so
+      // their HBM reads happen while the ring drains.
+      if (TT_M1S_L2PF)
+        for (int t = slots; t < stages; ++t)
+          bulk_prefetch_l2(packed + (int64_t)first(t) * L.bytes, uint32_t(cnt(t) * L.bytes));
+    }
+    issued = min(slots, stages);
+    // Let the next kernel launch once every weight byte of this one has been
+    // requested, so its prefetch queues behind this kernel's reads.
+    if (TT_M1S_TRIGGER == 1 && stages <= slots) pdl_allow_next_grid();
+    pdl_wait_prior_grid();  // h may still be read by the previous kernel
+    for (int t = 0; t < stages; ++t) {
+      const int s = t % slots;
+      const bool ok = mbar_wait_bounded(smem_u32(&empty[s]), uint32_t((t / slots) & 1));
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) flag_error(err, kErrTimeout);
+        // let the copies already issued land before the CTA may exit
+        for (int u = t; u < issued; ++u)
+          (void)mbar_wait_bounded(smem_u32(&full[u % slots]), uint32_t((u / slots) & 1));
+        return;
+      }
+      if (lane < cnt(t)) {
+        const float* p = part + ((size_t)s * R + lane) * NB * 2;
+        float g = 0.f, u = 0.f;
+#pragma unroll
+        for (int c = 0; c < NB; ++c) {
+          g += p[2 * c];
+          u += p[2 * c + 1];
+        }
+        const uint8_t* rec = ring + (size_t)s * stage_bytes + (size_t)lane * L.bytes;
+        g *= *reinterpret_cast<const float*>(rec + L.post);
+        u *= *reinterpret_cast<const float*>(rec + L.post + 4);
+        h[first(t) + lane] = f32_to_bf16_rne(silu_mul(g, u));
+      }
+      __syncwarp();
+      if (t + slots < stages) {
+        if (lane == 0) issue(t + slots);
+        ++issued;
+        if (TT_M1S_TRIGGER == 1 && t + slots == stages - 1) pdl_allow_next_grid();
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumer warps ----------------
+  const int chunk = warp % NB, rslot = warp / NB;
+  const int b = 32 * chunk + lane;
+  const bool active = b < L.nblk;
+  pdl_wait_prior_grid();
+  // This warp's slice of x -> f16x2, prescaled by a power of two chosen from
+  // the slice's own max |x| (exact); partial sums are unscaled before they
+  // meet the other chunks'.
+  uint32_t xv[16];
+  float xmax = 0.f;
+  {
+    const uint64_t xpol = l2_evict_last_policy();
+    uint4 q[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                  make_uint4(0, 0, 0, 0)};
+    if (active) {
+      const uint4* src = reinterpret_cast<const uint4*>(x) + (size_t)b * 4;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) q[t] = ld_global_v4_hint(src + t, xpol);
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      xv[4 * t + 0] = q[t].x;
+      xv[4 * t + 1] = q[t].y;
+      xv[4 * t + 2] = q[t].z;
+      xv[4 * t + 3] = q[t].w;
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      xmax = fmaxf(xmax, fabsf(bf16_bits_to_f32(xv[t] & 0xFFFFu)));
+      xmax = fmaxf(xmax, fabsf(bf16_bits_to_f32(xv[t] >> 16)));
+    }
+  }
+  xmax = warp_max(xmax);
+  const int sx = min(f16_prescale_exponent(xmax), 127);
+  const float two_s = scalbnf(1.0f, sx);
+  const float inv = scalbnf(1.0f, -sx);
+#pragma unroll
+  for (int t = 0; t < 16; ++t)
+    xv[t] = pack_f16x2_scaled(bf16_bits_to_f32(xv[t] & 0xFFFFu), bf16_bits_to_f32(xv[t] >> 16),
+                              two_s);
+
+  for (int t = 0; t < stages; ++t) {
+    const int s = t % slots;
+    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), uint32_t((t / slots) & 1));
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) flag_error(err, kErrTimeout);
+      return;
+    }
+    if (rslot < cnt(t)) {
+      float ag = 0.f, au = 0.f;
+      if (active) {
+        const uint8_t* rec = ring + (size_t)s * stage_bytes + (size_t)rslot * L.bytes;
+        const uint4 cg = *reinterpret_cast<const uint4*>(rec + L.gate_codes() + b * 16);
+        const uint4 cu = *reinterpret_cast<const uint4*>(rec + L.up_codes() + b * 16);
+        ag = dot32(cg, xv) * e8m0_to_f32(rec[L.gate_scales() + b]);
+        au = dot32(cu, xv) * e8m0_to_f32(rec[L.up_scales() + b]);
+      }
+      const float v = warp_sum2(ag, au, lane);  // lanes 0-15: g, 16-31: u
+      if ((lane & 15) == 0)
+        part[((size_t)s * R + rslot) * NB * 2 + chunk * 2 + (lane >> 4)] = v * inv;
+    }
+    mbar_arrive(smem_u32(&empty[s]));
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -693,10 +909,37 @@ cudaError_t run_m1x(const DeviceInfo& di, const uint8_t* packed, int n, int k, c
   auto kern = swiglu_mxfp4_m1x_kernel<NB, RPC, WARPS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  int grid = di.sms;
+  int grid = TT_M1X_CTAS_PER_SM * di.sms;
   const int units = (n + RPC - 1) / RPC;
   if (grid > units) grid = units;
   return launch_threads(kern, grid, WARPS * 32, smem, s, pdl, packed, n, k, x, h, slots,
+                        di.error_word);
+}
+
+// Stage budget of the warp-specialised kernel: under half an SM, so that
+// the next kernel's CTA fits beside it.
+constexpr int kStageBudget = 100 * 1024;
+
+template <int NB>
+cudaError_t run_m1s(const DeviceInfo& di, const uint8_t* packed, int n, int k, const uint16_t* x,
+                    uint16_t* h, cudaStream_t s, bool pdl) {
+  constexpr int R = NB >= 16 ? 1 : 16 / NB;
+  constexpr int W = NB * R;
+  const SwigluRecord L(k);
+  const int stage_bytes = R * L.bytes;
+  const int per_slot = stage_bytes + 16 + R * NB * 8;
+  int slots = kStageBudget / per_slot;
+  if (slots > TT_M1S_SLOTS) slots = TT_M1S_SLOTS;
+  if (slots < 2) slots = 2;
+  const int smem = slots * per_slot;
+  if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
+  auto kern = swiglu_mxfp4_m1s_kernel<NB, R>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int grid = di.sms;
+  const int units = (n + R - 1) / R;
+  if (grid > units) grid = units;
+  return launch_threads(kern, grid, (W + 1) * 32, smem, s, pdl, packed, n, k, x, h, slots,
                         di.error_word);
 }
 
@@ -725,6 +968,27 @@ cudaError_t launch_swiglu_mxfp4_cc(const uint8_t* packed, int n, int k, const ui
                                    uint16_t* h, cudaStream_t s, bool pdl) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorNoDevice;
+  if (m == 1 && TT_M1_STAGED) {
+    switch ((k / 32 + 31) / 32) {
+      case 1: return run_m1s<1>(*di, packed, n, k, x, h, s, pdl);
+      case 2: return run_m1s<2>(*di, packed, n, k, x, h, s, pdl);
+      case 3: return run_m1s<3>(*di, packed, n, k, x, h, s, pdl);
+      case 4: return run_m1s<4>(*di, packed, n, k, x, h, s, pdl);
+      case 5: return run_m1s<5>(*di, packed, n, k, x, h, s, pdl);
+      case 6: return run_m1s<6>(*di, packed, n, k, x, h, s, pdl);
+      case 7: return run_m1s<7>(*di, packed, n, k, x, h, s, pdl);
+      case 8: return run_m1s<8>(*di, packed, n, k, x, h, s, pdl);
+      case 9: return run_m1s<9>(*di, packed, n, k, x, h, s, pdl);
+      case 10: return run_m1s<10>(*di, packed, n, k, x, h, s, pdl);
+      case 11: return run_m1s<11>(*di, packed, n, k, x, h, s, pdl);
+      case 12: return run_m1s<12>(*di, packed, n, k, x, h, s, pdl);
+      case 13: return run_m1s<13>(*di, packed, n, k, x, h, s, pdl);
+      case 14: return run_m1s<14>(*di, packed, n, k, x, h, s, pdl);
+      case 15: return run_m1s<15>(*di, packed, n, k, x, h, s, pdl);
+      case 16: return run_m1s<16>(*di, packed, n, k, x, h, s, pdl);
+      default: break;
+    }
+  }
   if (m == 1 && TT_M1_XSMEM) {
     const int nb = (k / 32 + 31) / 32;
     switch (nb) {
