@@ -165,4 +165,83 @@ tt_status tt_bf16_swiglu_matvec(const uint16_t* wg, const uint16_t* wu, int64_t 
                                           as_stream(stream), kPdl));
 }
 
+size_t tt_mxfp4_rows_packed_bytes(int64_t n, int64_t k) {
+  if (n < 1 || k < 32 || k % 32 != 0 || k > kMaxK || n > kMaxRows) return 0;
+  return size_t(n) * size_t(tt::RowRecord(int(k)).bytes);
+}
+
+tt_status tt_mxfp4_pack_rows(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k,
+                             void* packed, size_t packed_bytes, void* stream) {
+  if (n < 1 || k < 32 || k % 32 != 0 || k > kMaxK || n > kMaxRows) return TT_ERR_SHAPE;
+  if (!codes || !scales || !packed) return TT_ERR_NULL;
+  if (packed_bytes < tt_mxfp4_rows_packed_bytes(n, k)) return TT_ERR_SIZE;
+  if (!aligned(packed, 16)) return TT_ERR_ALIGN;
+  return from_cuda(tt::launch_pack_rows(codes, scales, n, k, static_cast<uint8_t*>(packed),
+                                        as_stream(stream)));
+}
+
+size_t tt_moe_workspace_bytes(int64_t hidden, int64_t inter, int32_t n_experts, int32_t top_k) {
+  if (hidden < 32 || inter < 32 || n_experts < 1 || n_experts > 256 || top_k < 1 || top_k > 8 ||
+      top_k > n_experts)
+    return 0;
+  return tt::moe_workspace_bytes(hidden, inter, n_experts, top_k);
+}
+
+tt_status tt_moe_mxfp4_topk_mlp(const uint16_t* x_bf16, int64_t hidden, int64_t inter,
+                                const uint16_t* router_w_bf16, int32_t n_experts, int32_t top_k,
+                                const void* gate_up_packed, const void* down_packed,
+                                uint16_t* out_bf16, int32_t* out_idx, float* out_prob,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (hidden < 32 || hidden % 32 != 0 || hidden > kMaxK) return TT_ERR_SHAPE;
+  if (inter < 32 || inter % 32 != 0 || inter > 8192) return TT_ERR_SHAPE;
+  if (n_experts < 1 || n_experts > 256 || top_k < 1 || top_k > 8 || top_k > n_experts)
+    return TT_ERR_SHAPE;
+  if (!x_bf16 || !router_w_bf16 || !gate_up_packed || !down_packed || !out_bf16 || !out_idx ||
+      !out_prob || !workspace)
+    return TT_ERR_NULL;
+  if (workspace_bytes < tt_moe_workspace_bytes(hidden, inter, n_experts, top_k))
+    return TT_ERR_SIZE;
+  if (!aligned(x_bf16, 16) || !aligned(router_w_bf16, 16) || !aligned(gate_up_packed, 16) ||
+      !aligned(down_packed, 16) || !aligned(out_bf16, 2) || !aligned(out_idx, 4) ||
+      !aligned(out_prob, 4) || !aligned(workspace, 16))
+    return TT_ERR_ALIGN;
+  const cudaError_t e = tt::launch_moe(
+      x_bf16, int(hidden), int(inter), router_w_bf16, int(n_experts), int(top_k),
+      static_cast<const uint8_t*>(gate_up_packed), static_cast<const uint8_t*>(down_packed),
+      out_bf16, out_idx, out_prob, workspace, as_stream(stream), kPdl);
+  if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+tt_status tt_quantize_int4_grouped(const float* w, int64_t n, int64_t k, int32_t group,
+                                   uint8_t* codes, uint16_t* scales_f16, uint8_t* zp_u4,
+                                   int32_t* status_dev, void* stream) {
+  if (n < 0 || k < 0 || k % 2 != 0 || group < 2 || group % 2 != 0 || n > kMaxRows)
+    return TT_ERR_SHAPE;
+  if (n == 0 || k == 0) return TT_OK;
+  if (!w || !codes || !scales_f16 || !zp_u4) return TT_ERR_NULL;
+  if (!aligned(w, 4) || !aligned(scales_f16, 2) || (status_dev && !aligned(status_dev, 4)))
+    return TT_ERR_ALIGN;
+  return from_cuda(tt::launch_quantize_int4(w, n, k, group, codes, scales_f16, zp_u4, status_dev,
+                                            as_stream(stream)));
+}
+
+tt_status tt_int4_grouped_matvec(const uint8_t* codes, const uint16_t* scales_f16,
+                                 const uint8_t* zp_u4, int64_t n, int64_t k, int32_t group,
+                                 const uint16_t* x_bf16, int64_t m, uint16_t* y_bf16,
+                                 void* stream) {
+  if (n < 1 || k < 32 || k % 32 != 0 || k > 8192 || n > kMaxRows) return TT_ERR_SHAPE;
+  if (group < 32 || group % 32 != 0) return TT_ERR_SHAPE;
+  if (m < 1 || m > 8) return TT_ERR_SHAPE;
+  if (!codes || !scales_f16 || !zp_u4 || !x_bf16 || !y_bf16) return TT_ERR_NULL;
+  if (!aligned(codes, 16) || !aligned(scales_f16, 2) || !aligned(x_bf16, 16) ||
+      !aligned(y_bf16, 2))
+    return TT_ERR_ALIGN;
+  const cudaError_t e = tt::launch_int4_matvec(codes, scales_f16, zp_u4, int(n), int(k),
+                                               int(group), x_bf16, int(m), y_bf16,
+                                               as_stream(stream), kPdl);
+  if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
 }  // extern "C"

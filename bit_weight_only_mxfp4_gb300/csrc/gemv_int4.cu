@@ -1,0 +1,247 @@
+// Grouped affine INT4 matvec for the dense Q/K/V/O projections, m = 1..8.
+//
+// Method: the ThinTensor project page (stardance.hackclub.com/projects/29750)
+// runs Q/K/V/O as INT4 under dense_int4_layers="all" (97.87 tok/s notes), with
+// affine groups whose last group may be partial (fixes list).  Per row and
+// group g: w = (q - zp_g) * s_g, so
+//     y = sum_g s_g * sum_{k in g} (q_k - zp_g) * x_k.
+//
+// Kernel: one warp per output row; lane l owns the 32-weight chunks l, l+32,
+// ... of the row (group % 32 == 0, so a chunk never straddles two groups).
+// A chunk's 16 code bytes arrive with one 128-bit load.  Nibble pairs
+// (q_i, q_{i+4}) of each 32-bit word become f16x2 (1024 + q) with one LOP3
+// against the exponent pattern 0x6400, and one HSUB2 of (1024 + zp) turns
+// them into the exact small integers q - zp; the products with x (f16 after
+// an exact power-of-two prescale, stored in shared memory in the same pair
+// order) accumulate in fp32 with fma.rn.f32.f16, and each chunk's sum is
+// scaled by its group's fp16 scale.
+#include "common.cuh"
+#include "launch.h"
+
+namespace tt {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRowsPerIter = 2;
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t bits) {
+  uint32_t d;
+  // d = (a & mask) | bits
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Sum over one 32-weight chunk of (q - zp) * x, x given as 16 f16x2 values
+// in the pair order (x[8t+i], x[8t+i+4]) for word t, pair i.
+__device__ __forceinline__ float chunk_dot(const uint4& c, uint32_t zz, const uint32_t* xv) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t p0 = hsub2(lop3_and_or(w[t], 0x000F000Fu, 0x64006400u), zz);
+    const uint32_t p1 = hsub2(lop3_and_or(w[t] >> 4, 0x000F000Fu, 0x64006400u), zz);
+    const uint32_t p2 = hsub2(lop3_and_or(w[t] >> 8, 0x000F000Fu, 0x64006400u), zz);
+    const uint32_t p3 = hsub2(lop3_and_or(w[t] >> 12, 0x000F000Fu, 0x64006400u), zz);
+    fma_f16x2_f32(a0, a1, p0, xv[4 * t + 0]);
+    fma_f16x2_f32(a2, a3, p1, xv[4 * t + 1]);
+    fma_f16x2_f32(a0, a1, p2, xv[4 * t + 2]);
+    fma_f16x2_f32(a2, a3, p3, xv[4 * t + 3]);
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
+template <int CPL, int MT>
+__global__ void __launch_bounds__(kThreads, 2)
+    int4_matvec_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                       const uint8_t* __restrict__ zp, int n, int k, int group,
+                       const uint16_t* __restrict__ x, int m, uint16_t* __restrict__ y) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nch = k >> 5;                     // 32-weight chunks per row
+  const int ng = (k + group - 1) / group;     // groups per row
+  const int zb = (ng + 1) >> 1;               // zero-point bytes per row
+  const int gw = blockIdx.x * kWarps + warp;
+  const int nw = gridDim.x * kWarps;
+  uint4* xs = reinterpret_cast<uint4*>(smem);  // [MT][4][nch]
+  float* red = reinterpret_cast<float*>(xs + (size_t)MT * 4 * nch);  // [MT][kWarps]
+  int* sxs = reinterpret_cast<int*>(red + MT * kWarps);              // [MT]
+
+  pdl_allow_next_grid();
+
+  // Codes of this warp's first rows do not depend on the previous kernel.
+  uint4 cw[kRowsPerIter][CPL];
+  auto load_rows = [&](int r) {
+#pragma unroll
+    for (int u = 0; u < kRowsPerIter; ++u) {
+      const int row = r + u * nw;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const int j = c * 32 + lane;
+        cw[u][c] = (row < n && j < nch)
+                       ? __ldcs(reinterpret_cast<const uint4*>(codes + (size_t)row * (k >> 1)) + j)
+                       : make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  load_rows(gw);
+  pdl_wait_prior_grid();
+
+  // x -> f16 (prescaled per row of x by a power of two) in pair order.
+  for (int i = 0; i < MT; ++i) {
+    float mx = 0.f;
+    if (i < m)
+      for (int t = threadIdx.x; t < (k >> 3); t += kThreads) {
+        const uint4 v = reinterpret_cast<const uint4*>(x + (size_t)i * k)[t];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(wv[e] & 0xFFFFu)),
+                               fabsf(bf16_bits_to_f32(wv[e] >> 16))));
+      }
+    mx = warp_max(mx);
+    if (lane == 0) red[i * kWarps + warp] = mx;
+  }
+  __syncthreads();
+  if (threadIdx.x < MT) {
+    float mx = 0.f;
+    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red[threadIdx.x * kWarps + w]);
+    sxs[threadIdx.x] = min(f16_prescale_exponent(mx), 127);
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < MT * (k >> 3); c += kThreads) {
+    const int i = c / (k >> 3), t8 = c - i * (k >> 3);  // x[8*t8 .. 8*t8+7] of row i
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (i < m) {
+      const float two_s = scalbnf(1.0f, sxs[i]);
+      const uint4 v = reinterpret_cast<const uint4*>(x + (size_t)i * k)[t8];
+      const float e0 = bf16_bits_to_f32(v.x & 0xFFFFu), e1 = bf16_bits_to_f32(v.x >> 16);
+      const float e2 = bf16_bits_to_f32(v.y & 0xFFFFu), e3 = bf16_bits_to_f32(v.y >> 16);
+      const float e4 = bf16_bits_to_f32(v.z & 0xFFFFu), e5 = bf16_bits_to_f32(v.z >> 16);
+      const float e6 = bf16_bits_to_f32(v.w & 0xFFFFu), e7 = bf16_bits_to_f32(v.w >> 16);
+      o.x = pack_f16x2_scaled(e0, e4, two_s);
+      o.y = pack_f16x2_scaled(e1, e5, two_s);
+      o.z = pack_f16x2_scaled(e2, e6, two_s);
+      o.w = pack_f16x2_scaled(e3, e7, two_s);
+    }
+    // word t = t8 % 4 of chunk j = t8 / 4
+    xs[((size_t)i * 4 + (t8 & 3)) * nch + (t8 >> 2)] = o;
+  }
+  __syncthreads();
+
+  for (int r = gw; r < n; r += kRowsPerIter * nw) {
+    float acc[kRowsPerIter][MT];
+#pragma unroll
+    for (int u = 0; u < kRowsPerIter; ++u)
+#pragma unroll
+      for (int i = 0; i < MT; ++i) acc[u][i] = 0.f;
+#pragma unroll
+    for (int u = 0; u < kRowsPerIter; ++u) {
+      const int row = r + u * nw;
+      if (row >= n) break;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const int j = c * 32 + lane;
+        if (j < nch) {
+          const int g = (j * 32) / group;
+          const float sc = __half2float(__ushort_as_half(__ldg(scales + (size_t)row * ng + g)));
+          const uint32_t z = (__ldg(zp + (size_t)row * zb + (g >> 1)) >> (4 * (g & 1))) & 15u;
+          const uint32_t zz = 0x64006400u + z * 0x00010001u;  // f16x2 (1024 + z)
+#pragma unroll
+          for (int i = 0; i < MT; ++i) {
+            if (i < m) {
+              uint32_t xv[16];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const uint4 q = xs[((size_t)i * 4 + t) * nch + j];
+                xv[4 * t + 0] = q.x;
+                xv[4 * t + 1] = q.y;
+                xv[4 * t + 2] = q.z;
+                xv[4 * t + 3] = q.w;
+              }
+              acc[u][i] = fmaf(chunk_dot(cw[u][c], zz, xv), sc, acc[u][i]);
+            }
+          }
+        }
+      }
+    }
+    // prefetch the next rows' codes before reducing these
+    const int rn = r + kRowsPerIter * nw;
+    load_rows(rn);
+#pragma unroll
+    for (int u = 0; u < kRowsPerIter; ++u) {
+      const int row = r + u * nw;
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        const float v = warp_sum(acc[u][i]);
+        if (lane == 0 && row < n && i < m) {
+          __nv_bfloat16 b = __float2bfloat16_rn(scalbnf(v, -sxs[i]));
+          y[(size_t)i * n + row] = *reinterpret_cast<uint16_t*>(&b);
+        }
+      }
+    }
+  }
+}
+
+template <int CPL, int MT>
+cudaError_t run(const DeviceInfo& di, const uint8_t* codes, const uint16_t* scales,
+                const uint8_t* zp, int n, int k, int group, const uint16_t* x, int m,
+                uint16_t* y, cudaStream_t s, bool pdl) {
+  const int smem = MT * 4 * (k >> 5) * 16 + MT * kWarps * 4 + MT * 4;
+  if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
+  auto kern = int4_matvec_kernel<CPL, MT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int grid = 2 * di.sms;
+  const int need = (n + kWarps * kRowsPerIter - 1) / (kWarps * kRowsPerIter);
+  if (grid > need) grid = need;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, codes, scales, zp, n, k, group, x, m, y);
+}
+
+template <int CPL>
+cudaError_t run_m(const DeviceInfo& di, const uint8_t* codes, const uint16_t* scales,
+                  const uint8_t* zp, int n, int k, int group, const uint16_t* x, int m,
+                  uint16_t* y, cudaStream_t s, bool pdl) {
+  if (m == 1) return run<CPL, 1>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+  if (m == 2) return run<CPL, 2>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+  if (m <= 4) return run<CPL, 4>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+  return run<CPL, 8>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+}
+
+}  // namespace
+
+cudaError_t launch_int4_matvec(const uint8_t* codes, const uint16_t* scales, const uint8_t* zp,
+                               int n, int k, int group, const uint16_t* x, int m, uint16_t* y,
+                               cudaStream_t s, bool pdl) {
+  const DeviceInfo* di = device_info();
+  if (!di) return cudaErrorNoDevice;
+  switch ((k / 32 + 31) / 32) {
+    case 1: return run_m<1>(*di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+    case 2: return run_m<2>(*di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+    case 3: return run_m<3>(*di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+    case 4: return run_m<4>(*di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+    case 5: return run_m<5>(*di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+    case 6: return run_m<6>(*di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+    case 7: return run_m<7>(*di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+    case 8: return run_m<8>(*di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace tt

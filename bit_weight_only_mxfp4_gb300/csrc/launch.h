@@ -34,6 +34,17 @@ cudaError_t launch_quantize_int4(const float* w, int64_t n, int64_t k, int group
 cudaError_t launch_swiglu_mxfp4_cc(const uint8_t* packed, int n, int k, const uint16_t* x,
                                    int m, uint16_t* h, cudaStream_t s, bool pdl);
 
+// gemv_int4.cu — grouped affine INT4 matvec, m in [1, 8]
+cudaError_t launch_int4_matvec(const uint8_t* codes, const uint16_t* scales, const uint8_t* zp,
+                               int n, int k, int group, const uint16_t* x, int m, uint16_t* y,
+                               cudaStream_t s, bool pdl);
+
+// moe.cu — router, top-k, gathered gate/up and down of the selected experts
+size_t moe_workspace_bytes(int64_t hidden, int64_t inter, int n_experts, int top_k);
+cudaError_t launch_moe(const uint16_t* x, int hidden, int inter, const uint16_t* wr, int E,
+                       int top_k, const uint8_t* gu, const uint8_t* dn, uint16_t* out,
+                       int32_t* out_idx, float* out_prob, void* ws, cudaStream_t s, bool pdl);
+
 // gemv_bf16.cu
 cudaError_t launch_swiglu_bf16(const uint16_t* wg, const uint16_t* wu, int n, int k,
                                const uint16_t* x, int m, uint16_t* h, cudaStream_t s, bool pdl);

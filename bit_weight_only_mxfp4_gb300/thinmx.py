@@ -41,6 +41,13 @@ SIGNATURES = {
     "tt_mxfp4_pack_swiglu": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P]),
     "tt_mxfp4_swiglu_matvec": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _P, _P]),
     "tt_bf16_swiglu_matvec": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _I64, _P, _P]),
+    "tt_mxfp4_rows_packed_bytes": (_SZ, [_I64, _I64]),
+    "tt_mxfp4_pack_rows": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _SZ, _P]),
+    "tt_moe_workspace_bytes": (_SZ, [_I64, _I64, _I32, _I32]),
+    "tt_moe_mxfp4_topk_mlp": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P,
+                                              _P, _SZ, _P]),
+    "tt_quantize_int4_grouped": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
+    "tt_int4_grouped_matvec": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _P]),
 }
 
 
@@ -134,3 +141,39 @@ def tt_mxfp4_swiglu_matvec(packed, n, k, x_bf16, m, h_bf16, stream=None):
 def tt_bf16_swiglu_matvec(wg, wu, n, k, x_bf16, m, h_bf16, stream=None):
     _check("tt_bf16_swiglu_matvec", load().tt_bf16_swiglu_matvec(
         _ptr(wg), _ptr(wu), n, k, _ptr(x_bf16), m, _ptr(h_bf16), _stream(stream)))
+
+
+def tt_quantize_int4_grouped(w, n, k, group, codes, scales_f16, zp_u4, status_dev=None,
+                             stream=None):
+    _check("tt_quantize_int4_grouped", load().tt_quantize_int4_grouped(
+        _ptr(w), n, k, group, _ptr(codes), _ptr(scales_f16), _ptr(zp_u4), _ptr(status_dev),
+        _stream(stream)))
+
+
+def tt_int4_grouped_matvec(codes, scales_f16, zp_u4, n, k, group, x_bf16, m, y_bf16,
+                           stream=None):
+    _check("tt_int4_grouped_matvec", load().tt_int4_grouped_matvec(
+        _ptr(codes), _ptr(scales_f16), _ptr(zp_u4), n, k, group, _ptr(x_bf16), m, _ptr(y_bf16),
+        _stream(stream)))
+
+
+def tt_mxfp4_rows_packed_bytes(n, k) -> int:
+    return int(load().tt_mxfp4_rows_packed_bytes(n, k))
+
+
+def tt_mxfp4_pack_rows(codes, scales, n, k, packed, packed_bytes, stream=None):
+    _check("tt_mxfp4_pack_rows", load().tt_mxfp4_pack_rows(
+        _ptr(codes), _ptr(scales), n, k, _ptr(packed), packed_bytes, _stream(stream)))
+
+
+def tt_moe_workspace_bytes(hidden, inter, n_experts, top_k) -> int:
+    return int(load().tt_moe_workspace_bytes(hidden, inter, n_experts, top_k))
+
+
+def tt_moe_mxfp4_topk_mlp(x_bf16, hidden, inter, router_w_bf16, n_experts, top_k,
+                          gate_up_packed, down_packed, out_bf16, out_idx, out_prob, workspace,
+                          workspace_bytes, stream=None):
+    _check("tt_moe_mxfp4_topk_mlp", load().tt_moe_mxfp4_topk_mlp(
+        _ptr(x_bf16), hidden, inter, _ptr(router_w_bf16), n_experts, top_k,
+        _ptr(gate_up_packed), _ptr(down_packed), _ptr(out_bf16), _ptr(out_idx), _ptr(out_prob),
+        _ptr(workspace), workspace_bytes, _stream(stream)))

@@ -161,6 +161,72 @@ tt_status tt_bf16_swiglu_matvec(const uint16_t* wg, const uint16_t* wu,
                                 int64_t n, int64_t k, const uint16_t* x_bf16,
                                 int64_t m, uint16_t* h_bf16, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Packed single-matrix layout (MoE down projections): one record per row
+ * with its codes and scales, padded to 16 bytes.  Byte-for-byte
+ * rearrangement of canonical MXFP4; layout private, size public.
+ * Requires n >= 1, 32 <= k <= 16384, k % 32 == 0; packed 16-byte aligned.
+ * --------------------------------------------------------------------- */
+size_t tt_mxfp4_rows_packed_bytes(int64_t n, int64_t k);
+tt_status tt_mxfp4_pack_rows(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k,
+                             void* packed, size_t packed_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * MoE MLP at batch 1  [DL2 router/expert operators; SHIP MoE drift devlog
+ * (block-scaled matvec over the selected experts), "final ship" (exact
+ * routing; expert routing on the decode hot path)]
+ *
+ *   logit[e] = x . W_r[e]            (bf16 inputs; the fp32 logit is the
+ *                                     rounding of the exact dot product)
+ *   idx      = the top_k experts by logit, descending, ties to the lower
+ *              index; p = softmax of their logits
+ *   h_j      = silu(Wg[idx_j] x) * (Wu[idx_j] x)          (fp32, inter)
+ *   out      = bf16_rne( sum_j p_j * Wd[idx_j] h_j )      (hidden)
+ * Experts are stacked: gate_up_packed holds E buffers of
+ * tt_mxfp4_swiglu_packed_bytes(inter, hidden) bytes (gate = the swiglu gate
+ * rows, packed without postscales); down_packed holds E buffers of
+ * tt_mxfp4_rows_packed_bytes(hidden, inter) bytes.  router_w_bf16 [E][hidden].
+ * out_idx int32 [top_k], out_prob fp32 [top_k] (device).  workspace: device,
+ * >= tt_moe_workspace_bytes(...) bytes, 16-byte aligned; the call owns it
+ * until the stream reaches the end of the call.
+ * Requires hidden, inter multiples of 32, hidden <= 16384, inter <= 8192,
+ * 1 <= top_k <= min(E, 8), E <= 256.  Router logits must be finite.
+ * --------------------------------------------------------------------- */
+size_t tt_moe_workspace_bytes(int64_t hidden, int64_t inter, int32_t n_experts, int32_t top_k);
+tt_status tt_moe_mxfp4_topk_mlp(const uint16_t* x_bf16, int64_t hidden, int64_t inter,
+                                const uint16_t* router_w_bf16, int32_t n_experts, int32_t top_k,
+                                const void* gate_up_packed, const void* down_packed,
+                                uint16_t* out_bf16, int32_t* out_idx, float* out_prob,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Grouped affine INT4  [SHIP 97.87 tok/s notes: dense_int4_layers="all" for
+ * Q/K/V/O; fixes list: "correct affine INT4 partial-group quantization"]
+ *
+ * Quantiser, per row and group [g*G, min((g+1)*G, k)) (the last group may be
+ * partial and uses only its own elements):
+ *   s  = fp16 round-to-nearest-even of (max - min) / 15, computed in fp64;
+ *   zp = clamp(rint(-min / s), 0, 15);  q = clamp(rint(w / s) + zp, 0, 15)
+ *   (rint = nearest, ties to even).  A group with s == 0 stores zp = q = 0.
+ *   A group holding NaN/Inf (scale 0x7E00), or whose scale overflows fp16,
+ *   stores zp = q = 0 and OR-s TT_ERR_NONFINITE into *status_dev.
+ * w fp32 [n][k]; codes [n][k/2] (low nibble = even k); scales_f16
+ * [n][ceil(k/G)]; zp_u4 [n][ceil(ceil(k/G)/2)] (low nibble = even group).
+ * Requires k even, G even >= 2.  Setup step.
+ * --------------------------------------------------------------------- */
+tt_status tt_quantize_int4_grouped(const float* w, int64_t n, int64_t k, int32_t group,
+                                   uint8_t* codes, uint16_t* scales_f16, uint8_t* zp_u4,
+                                   int32_t* status_dev, void* stream);
+
+/* y[i][r] = bf16_rne( sum_g s[r][g] * sum_{k in g} (q[r][k] - zp[r][g]) * x[i][k] )
+   with fp32 accumulation; canonical INT4 buffers as above; x [m][k],
+   y [m][n].  Requires 32 <= k <= 8192, k % 32 == 0, G % 32 == 0, 1 <= m <= 8;
+   codes and x 16-byte aligned. */
+tt_status tt_int4_grouped_matvec(const uint8_t* codes, const uint16_t* scales_f16,
+                                 const uint8_t* zp_u4, int64_t n, int64_t k, int32_t group,
+                                 const uint16_t* x_bf16, int64_t m, uint16_t* y_bf16,
+                                 void* stream);
+
 #ifdef __cplusplus
 }
 #endif

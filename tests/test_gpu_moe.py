@@ -1,0 +1,73 @@
+"""GPU parity of the MoE layer: router logits -> top-k (bit-exact indices,
+ties to the lower index) -> softmax -> selected experts' MXFP4 gate/up
+SwiGLU and down, weighted sum (float tolerance of tests/parity.py)."""
+import numpy as np
+import pytest
+
+import oracle
+from bit_weight_only_mxfp4_gb300 import synth
+
+from . import gpu_util as gu
+from .parity import assert_float_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    gu.ensure_lib()
+    assert gu.device_error() == 0
+
+
+def _case(E, H, I, K, wid, tie_rows=None):
+    r = synth.moe_router_inputs(wid, 0, H, E)
+    x, wr = r["x"], r["wr"]
+    if tie_rows:
+        for a, b in tie_rows:
+            wr[b] = wr[a]
+    gus, dns = [], []
+    for e in range(E):
+        g, d = synth.moe_expert_weights(wid, 0, e, H, I)
+        gus.append(g)
+        dns.append(d)
+    gup, dnp, (gc, gs, dc, ds) = gu.build_moe_experts(gus, dns, H, I)
+    out, idx, prob = gu.run_moe(x, wr, K, gup, dnp, H, I)
+    ref, ridx, rp, rlg, st = oracle.moe_mlp(x, wr, K, gc, gs, dc, ds)
+    assert st == oracle.OK
+    return out, idx, prob, ref, ridx, rp, rlg
+
+
+@pytest.mark.parametrize("E,H,I,K", [(6, 64, 96, 3), (8, 320, 640, 4), (32, 1024, 512, 4),
+                                     (5, 2880, 2880, 1), (16, 256, 2048, 8)])
+def test_moe_small_shapes(E, H, I, K):
+    out, idx, prob, ref, ridx, rp, rlg = _case(E, H, I, K, 98)
+    assert list(idx) == list(ridx)
+    np.testing.assert_allclose(prob, rp, rtol=2e-6, atol=1e-7)
+    assert_float_parity(out, ref, f"moe E={E} H={H} I={I} k={K}")
+    assert gu.device_error() == 0
+
+
+def test_moe_router_exact_ties_go_to_lower_index():
+    # duplicated router rows give bit-identical logits on both sides
+    E, H, I, K = 8, 256, 128, 4
+    r = synth.moe_router_inputs(99, 0, H, E)
+    lg = oracle.router_logits(r["x"], r["wr"])
+    top = int(np.argmax(lg))
+    ties = [(top, e) for e in range(E) if e != top][:3]
+    out, idx, prob, ref, ridx, rp, rlg = _case(E, H, I, K, 99, tie_rows=ties)
+    assert list(idx) == list(ridx)
+    assert sorted(idx) == sorted([top] + [b for _, b in ties])
+    assert list(idx) == sorted(idx)  # equal logits -> ascending index
+    np.testing.assert_allclose(prob, 0.25, rtol=1e-6)
+    assert_float_parity(out, ref, "moe ties")
+
+
+def test_moe_full_gptoss_layer():
+    c = synth.MOE
+    out, idx, prob, ref, ridx, rp, rlg = _case(c.experts, c.hidden, c.inter, c.top_k, c.wid)
+    srt = np.sort(rlg.astype(np.float64))[::-1]
+    margin = srt[c.top_k - 1] - srt[c.top_k]
+    assert margin > 0, "4th/5th logits tie in fp32: the case would not pin the order"
+    assert list(idx) == list(ridx)
+    np.testing.assert_allclose(prob, rp, rtol=2e-6, atol=1e-7)
+    assert_float_parity(out, ref, "moe gpt-oss-20b layer")
