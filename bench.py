@@ -208,7 +208,7 @@ def main():
     ap.add_argument("--impl", default="thinmx", choices=["thinmx", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--only", default=None, choices=["gate_up"],
+    ap.add_argument("--only", default=None, choices=["gate_up", "moe", "int4"],
                     help="run one small workload only (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -238,11 +238,16 @@ def main():
         pg.barrier()
     thinmx.load()
 
-    if args.only == "gate_up":
+    if args.only:
         hbm, peak_kind, _ = peaks()
-        r = single_gate_up(torch, synth, loader, thinmx, device, hbm, copies=4,
-                           reps=args.steps)
-        print(json.dumps({"only": "gate_up", **r}))
+        if args.only == "gate_up":
+            r = single_gate_up(torch, synth, loader, thinmx, device, hbm, copies=4,
+                               reps=args.steps)
+        elif args.only == "int4":
+            r = int4_workload(torch, synth, thinmx, device, hbm, 0, reps=args.steps)
+        else:
+            r = moe_workload(torch, synth, loader, thinmx, device, hbm, reps=args.steps)
+        print(json.dumps({"only": args.only, **r}))
         return 0
 
     cfg = synth.STACK
@@ -446,10 +451,86 @@ def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
                          "TFLOPs": round(4 * m * s.n * s.k / (ms * 1e-3) / 1e12, 2)}
         del g
     out[s.name] = sweep
-    out["peak"] = {"hbm_gbs": hbm, "source": peak_kind}
     del packs, base
     torch.cuda.empty_cache()
+    out.update(int4_workload(torch, synth, thinmx, device, hbm, l2))
+    torch.cuda.empty_cache()
+    out.update(moe_workload(torch, synth, loader, thinmx, device, hbm))
+    torch.cuda.empty_cache()
+    out["peak"] = {"hbm_gbs": hbm, "source": peak_kind}
     return out
+
+
+def int4_workload(torch, synth, thinmx, device, hbm, l2, reps=50):
+    """Grouped INT4 QKV projection (K=2880, N=5120, G=128) at M=1, cycling
+    through weight copies whose total exceeds twice the L2 size."""
+    c = synth.QKV
+    ng = (c.k + c.group - 1) // c.group
+    w = synth.torch_normal((c.n, c.k), synth.WEIGHT_STD, c.wid, 0, 0, device)
+    codes = torch.empty((c.n, c.k // 2), dtype=torch.uint8, device=device)
+    scales = torch.empty((c.n, ng), dtype=torch.int16, device=device)
+    zp = torch.empty((c.n, (ng + 1) // 2), dtype=torch.uint8, device=device)
+    thinmx.tt_quantize_int4_grouped(w, c.n, c.k, c.group, codes, scales, zp)
+    del w
+    per = c.n * c.k // 2 + c.n * ng * 2 + c.n * ((ng + 1) // 2) + 2 * c.k + 2 * c.n
+    copies = max(4, int(2 * l2 // per) + 2)
+    bufs = []
+    for i in range(copies):
+        x = synth.torch_normal((1, c.k), 1.0, c.wid, i, 1, device).to(torch.bfloat16)
+        y = torch.empty((1, c.n), dtype=torch.bfloat16, device=device)
+        bufs.append((codes.clone(), scales.clone(), zp.clone(), x, y))
+    g = capture(torch, lambda: [thinmx.tt_int4_grouped_matvec(a, b, z, c.n, c.k, c.group, x, 1, y)
+                                for a, b, z, x, y in bufs])
+    ms = time_graph(torch, g, reps) / copies
+    del bufs, g
+    return {c.name: {"us": round(ms * 1e3, 3), "GBps": round(per / (ms * 1e-3) / 1e9, 1),
+                     "frac": round(per / (ms * 1e-3) / 1e9 / hbm, 4), "bytes": per,
+                     "rotating_copies": copies}}
+
+
+def moe_workload(torch, synth, loader, thinmx, device, hbm, reps=20):
+    """gpt-oss-20b-shaped MoE stack: 24 layers, 32 MXFP4 experts each
+    (hidden = inter = 2880), top-4; one call per layer, all weights resident
+    (~10 GB, far beyond L2)."""
+    c = synth.MOE
+    H, I, E, K = c.hidden, c.inter, c.experts, c.top_k
+    sw = thinmx.tt_mxfp4_swiglu_packed_bytes(I, H)
+    rw = thinmx.tt_mxfp4_rows_packed_bytes(H, I)
+    layers = []
+    for l in range(c.layers):
+        gu = torch.empty(E * sw, dtype=torch.uint8, device=device)
+        dn = torch.empty(E * rw, dtype=torch.uint8, device=device)
+        for e in range(E):
+            w = synth.torch_normal((2 * I, H), synth.WEIGHT_STD, c.wid, l, 100 + 2 * e, device)
+            gc, gs = loader.quantize_mxfp4(w)
+            thinmx.tt_mxfp4_pack_swiglu(gc[:I], gs[:I], None, gc[I:], gs[I:], None, I, H,
+                                        gu[e * sw:], sw)
+            w = synth.torch_normal((H, I), synth.WEIGHT_STD, c.wid, l, 101 + 2 * e, device)
+            dc, ds = loader.quantize_mxfp4(w)
+            thinmx.tt_mxfp4_pack_rows(dc, ds, H, I, dn[e * rw:], rw)
+            del w, gc, gs, dc, ds
+        wr = synth.torch_normal((E, H), synth.WEIGHT_STD, c.wid, l, 1, device).to(torch.bfloat16)
+        x = synth.torch_normal((H,), 1.0, c.wid, l, 0, device).to(torch.bfloat16)
+        layers.append((gu, dn, wr, x))
+    out = torch.empty(H, dtype=torch.bfloat16, device=device)
+    idx = torch.empty(K, dtype=torch.int32, device=device)
+    prob = torch.empty(K, dtype=torch.float32, device=device)
+    wsb = thinmx.tt_moe_workspace_bytes(H, I, E, K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+    torch.cuda.synchronize()
+
+    def step():
+        for gu, dn, wr, x in layers:
+            thinmx.tt_moe_mxfp4_topk_mlp(x, H, I, wr, E, K, gu, dn, out, idx, prob, ws, wsb)
+
+    g = capture(torch, step)
+    ms = time_graph(torch, g, reps) / c.layers
+    per = E * H * 2 + K * (2 * I * (H // 2 + H // 32) + H * (I // 2 + I // 32)) + 2 * H + 2 * H
+    del layers, g
+    return {c.name: {"us_per_layer": round(ms * 1e3, 3),
+                     "GBps": round(per / (ms * 1e-3) / 1e9, 1),
+                     "frac": round(per / (ms * 1e-3) / 1e9 / hbm, 4), "bytes_per_layer": per,
+                     "layers": c.layers, "kernels_per_layer": 3}}
 
 
 def reference_arm(args, world, rank):
