@@ -58,6 +58,8 @@ inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
 constexpr int64_t kMaxK = 16384;
+static_assert(TT_MOE_STATIC_MAX_TOPK_INTER == tt::kMoeStaticMaxHFloats,
+              "header limit and scratch array size must agree");
 
 // Programmatic dependent launch on the hot-path kernels.
 constexpr bool kPdl = true;
@@ -209,6 +211,36 @@ tt_status tt_moe_mxfp4_topk_mlp(const uint16_t* x_bf16, int64_t hidden, int64_t 
       x_bf16, int(hidden), int(inter), router_w_bf16, int(n_experts), int(top_k),
       static_cast<const uint8_t*>(gate_up_packed), static_cast<const uint8_t*>(down_packed),
       out_bf16, out_idx, out_prob, workspace, as_stream(stream), kPdl);
+  if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+tt_status tt_moe_mxfp4_topk_mlp_static(const uint16_t* x_bf16, int64_t hidden, int64_t inter,
+                                       const uint16_t* router_w_bf16, int32_t n_experts,
+                                       int32_t top_k, const void* gate_up_packed,
+                                       const void* down_packed, uint16_t* out_bf16,
+                                       int32_t* out_idx, float* out_prob, void* stream) {
+  if (hidden < 32 || hidden % 32 != 0 || hidden > kMaxK) return TT_ERR_SHAPE;
+  if (inter < 32 || inter % 32 != 0 || inter > 8192) return TT_ERR_SHAPE;
+  if (n_experts < 1 || n_experts > 256 || top_k < 1 || top_k > 8 || top_k > n_experts)
+    return TT_ERR_SHAPE;
+  if (int64_t(top_k) * inter > TT_MOE_STATIC_MAX_TOPK_INTER) return TT_ERR_SIZE;
+  if (!x_bf16 || !router_w_bf16 || !gate_up_packed || !down_packed || !out_bf16 || !out_idx ||
+      !out_prob)
+    return TT_ERR_NULL;
+  if (!aligned(x_bf16, 16) || !aligned(router_w_bf16, 16) || !aligned(gate_up_packed, 16) ||
+      !aligned(down_packed, 16) || !aligned(out_bf16, 2) || !aligned(out_idx, 4) ||
+      !aligned(out_prob, 4))
+    return TT_ERR_ALIGN;
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  cudaError_t e = tt::moe_static_scratch(&scratch, &scratch_bytes);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (scratch_bytes < tt_moe_workspace_bytes(hidden, inter, n_experts, top_k)) return TT_ERR_SIZE;
+  e = tt::launch_moe(x_bf16, int(hidden), int(inter), router_w_bf16, int(n_experts), int(top_k),
+                     static_cast<const uint8_t*>(gate_up_packed),
+                     static_cast<const uint8_t*>(down_packed), out_bf16, out_idx, out_prob,
+                     scratch, as_stream(stream), kPdl);
   if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
   return from_cuda(e);
 }

@@ -44,6 +44,10 @@ size_t moe_workspace_bytes(int64_t hidden, int64_t inter, int n_experts, int top
 cudaError_t launch_moe(const uint16_t* x, int hidden, int inter, const uint16_t* wr, int E,
                        int top_k, const uint8_t* gu, const uint8_t* dn, uint16_t* out,
                        int32_t* out_idx, float* out_prob, void* ws, cudaStream_t s, bool pdl);
+// The library-owned MoE scratch (a static device array) of the current
+// device: its address (looked up on the first call on each device) and size.
+constexpr int kMoeStaticMaxHFloats = 32768;  // top_k * inter limit
+cudaError_t moe_static_scratch(void** ptr, size_t* bytes);
 
 // gemv_bf16.cu
 cudaError_t launch_swiglu_bf16(const uint16_t* wg, const uint16_t* wu, int n, int k,

@@ -21,6 +21,8 @@
 //                       it starts), prefetches its down rows before waiting on
 //                       the gate/up kernel, then out[r] = sum_j p_j * W_dn[e_j][r] . h_j
 //                       with h_j split into an exact f16 hi + lo pair.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 #include "layout.cuh"
@@ -548,6 +550,45 @@ cudaError_t launch_moe(const uint16_t* x, int hidden, int inter, const uint16_t*
     default: return cudaErrorInvalidValue;
   }
   return e;
+}
+
+// ---------------------------------------------------------------------------
+// Scratch for the MoE entry point that takes no workspace from its caller.
+//
+// Some callers cannot hand the library device memory: a plugin inside a host
+// that owns the whole device pool and exposes no allocator, a real-time loop
+// whose rules forbid allocator calls (they can synchronise the device or
+// fragment the pool), or a binding with no access to a CUDA allocator.  For
+// them the MoE layer runs on this fixed array instead: the router logits and
+// the experts' fp32 SwiGLU outputs of one call: 1 KB + 32768 fp32 = 129 KB,
+// enough for top_k * inter <= 32768 (gpt-oss-20b's 4 x 2880 uses 11520).
+// Every GPU that loads the library holds it until the process exits.  All calls share it, so two such
+// calls that overlap on the GPU (different streams, no ordering) race.
+// Nothing in it needs clearing: each call writes every element it reads.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_moe_static_scratch[kLogitsBytes + kMoeStaticMaxHFloats * 4];
+
+namespace {
+std::mutex g_static_mu;
+void* g_static_ptr[64];
+}  // namespace
+
+cudaError_t moe_static_scratch(void** ptr, size_t* bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    // Once per device, with that device current: the array's device address.
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_moe_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_ptr[dev] = p;
+  }
+  *ptr = g_static_ptr[dev];
+  *bytes = sizeof(g_moe_static_scratch);
+  return cudaSuccess;
 }
 
 }  // namespace tt

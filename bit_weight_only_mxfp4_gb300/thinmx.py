@@ -46,6 +46,8 @@ SIGNATURES = {
     "tt_moe_workspace_bytes": (_SZ, [_I64, _I64, _I32, _I32]),
     "tt_moe_mxfp4_topk_mlp": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P,
                                               _P, _SZ, _P]),
+    "tt_moe_mxfp4_topk_mlp_static": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _P,
+                                                     _P, _P, _P]),
     "tt_quantize_int4_grouped": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
     "tt_int4_grouped_matvec": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _P]),
 }
@@ -177,3 +179,18 @@ def tt_moe_mxfp4_topk_mlp(x_bf16, hidden, inter, router_w_bf16, n_experts, top_k
         _ptr(x_bf16), hidden, inter, _ptr(router_w_bf16), n_experts, top_k,
         _ptr(gate_up_packed), _ptr(down_packed), _ptr(out_bf16), _ptr(out_idx), _ptr(out_prob),
         _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+# Largest top_k * inter the workspace-free MoE call accepts (its fixed scratch).
+TT_MOE_STATIC_MAX_TOPK_INTER = 32768
+
+
+def tt_moe_mxfp4_topk_mlp_static(x_bf16, hidden, inter, router_w_bf16, n_experts, top_k,
+                                 gate_up_packed, down_packed, out_bf16, out_idx, out_prob,
+                                 stream=None):
+    """The MoE layer on the library's own fixed scratch: for callers that
+    cannot allocate device memory (see include/thinmx.h)."""
+    _check("tt_moe_mxfp4_topk_mlp_static", load().tt_moe_mxfp4_topk_mlp_static(
+        _ptr(x_bf16), hidden, inter, _ptr(router_w_bf16), n_experts, top_k,
+        _ptr(gate_up_packed), _ptr(down_packed), _ptr(out_bf16), _ptr(out_idx), _ptr(out_prob),
+        _stream(stream)))

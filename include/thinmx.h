@@ -200,6 +200,31 @@ tt_status tt_moe_mxfp4_topk_mlp(const uint16_t* x_bf16, int64_t hidden, int64_t 
                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * MoE MLP without a caller workspace.  (No counterpart on the ThinTensor
+ * pages: an addition of this library.)
+ *
+ * Same computation, arguments and requirements as tt_moe_mxfp4_topk_mlp,
+ * minus the workspace.  It is for callers that cannot give the library
+ * device memory: plugins inside a host that owns the device pool and offers
+ * no allocator, real-time loops that forbid allocator calls (an allocation
+ * can synchronise the device or fragment the pool), or bindings without a
+ * CUDA allocator.  The call allocates nothing; it runs on a fixed array
+ * inside the library (static device memory, held by every GPU that loads
+ * the library until the process exits) sized for top_k * inter <=
+ * TT_MOE_STATIC_MAX_TOPK_INTER; larger requests return TT_ERR_SIZE before
+ * any launch.  The first call on each device looks the array's address up
+ * (cudaGetSymbolAddress), so make it before any stream capture.  All calls
+ * share the array: two calls that can overlap on the GPU (different
+ * streams without ordering between them) race and give wrong results.
+ * --------------------------------------------------------------------- */
+#define TT_MOE_STATIC_MAX_TOPK_INTER 32768
+tt_status tt_moe_mxfp4_topk_mlp_static(const uint16_t* x_bf16, int64_t hidden, int64_t inter,
+                                       const uint16_t* router_w_bf16, int32_t n_experts,
+                                       int32_t top_k, const void* gate_up_packed,
+                                       const void* down_packed, uint16_t* out_bf16,
+                                       int32_t* out_idx, float* out_prob, void* stream);
+
+/* ------------------------------------------------------------------------
  * Grouped affine INT4  [SHIP 97.87 tok/s notes: dense_int4_layers="all" for
  * Q/K/V/O; fixes list: "correct affine INT4 partial-group quantization"]
  *
