@@ -48,6 +48,21 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback", {}
 
 
+def tensor_peak_tflops():
+    """Dense f16/bf16 tensor peak (TFLOP/s): the measured bf16 burst figure
+    when the pool's measurements exist, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            v = d.get("bf16_tflops")
+            if v:
+                return float(v)
+        except Exception:
+            pass
+    return FALLBACK_BF16_TFLOPS
+
+
 class Clocks:
     """nvidia-smi sampling during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -208,7 +223,7 @@ def main():
     ap.add_argument("--impl", default="thinmx", choices=["thinmx", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--only", default=None, choices=["gate_up", "moe", "int4"],
+    ap.add_argument("--only", default=None, choices=["gate_up", "moe", "int4", "sweep"],
                     help="run one small workload only (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -243,6 +258,8 @@ def main():
         if args.only == "gate_up":
             r = single_gate_up(torch, synth, loader, thinmx, device, hbm, copies=4,
                                reps=args.steps)
+        elif args.only == "sweep":
+            r = secondary_sweep(torch, synth, loader, thinmx, device, hbm)
         elif args.only == "int4":
             r = int4_workload(torch, synth, thinmx, device, hbm, 0, reps=args.steps)
         else:
@@ -419,11 +436,26 @@ def single_gate_up(torch, synth, loader, thinmx, device, hbm, copies=None, reps=
 
 
 def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
-    """Single gate/up layer (rotating copies > 2x L2) and the Phi-4 batch sweep."""
+    """Single gate/up layer (rotating copies > 2x L2), the Phi-4 batch sweep,
+    the INT4 QKV projection and the MoE stack."""
     out = dict(single_gate_up(torch, synth, loader, thinmx, device, hbm))
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    out.update(secondary_sweep(torch, synth, loader, thinmx, device, hbm))
+    torch.cuda.empty_cache()
+    out.update(int4_workload(torch, synth, thinmx, device, hbm, l2))
+    torch.cuda.empty_cache()
+    out.update(moe_workload(torch, synth, loader, thinmx, device, hbm))
+    torch.cuda.empty_cache()
+    out["peak"] = {"hbm_gbs": hbm, "source": peak_kind,
+                   "tensor_tflops": tensor_peak_tflops()}
+    return out
 
-    # Phi-4 gate/up batch sweep
+
+def secondary_sweep(torch, synth, loader, thinmx, device, hbm, reps=20):
+    """Phi-4 gate/up (K=5120, N=17920) over the batch sizes: CUDA-core kernel
+    for m <= 8, tcgen05 tensor-core kernel above; weight copies > 2x L2."""
+    tensor_peak = tensor_peak_tflops()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
     s = synth.SWEEP
     wg = synth.torch_normal((s.n, s.k), synth.WEIGHT_STD, s.wid, 0, 0, device)
     wu = synth.torch_normal((s.n, s.k), synth.WEIGHT_STD, s.wid, 0, 1, device)
@@ -436,29 +468,23 @@ def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
     packs = [base] + [base.clone() for _ in range(copies - 1)]
     sweep = {}
     for m in s.ms:
-        if m > 8:
-            sweep[str(m)] = {"status": "tensor-core path not built yet"}
-            continue
         xs = [synth.torch_normal((m, s.k), 1.0, s.wid, 0, 2, device).to(torch.bfloat16)
               for _ in range(copies)]
         hs = [torch.empty((m, s.n), dtype=torch.bfloat16, device=device) for _ in range(copies)]
         g = capture(torch, lambda: [thinmx.tt_mxfp4_swiglu_matvec(p, s.n, s.k, x, m, h)
                                     for p, x, h in zip(packs, xs, hs)])
-        ms = time_graph(torch, g, 20) / copies
+        ms = time_graph(torch, g, reps) / copies
         b = gate_up_bytes(s.n, s.k, m)
+        tflops = 4 * m * s.n * s.k / (ms * 1e-3) / 1e12
         sweep[str(m)] = {"us": round(ms * 1e3, 3), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
                          "frac": round(b / (ms * 1e-3) / 1e9 / hbm, 4),
-                         "TFLOPs": round(4 * m * s.n * s.k / (ms * 1e-3) / 1e12, 2)}
+                         "TFLOPs": round(tflops, 2),
+                         "path": "tcgen05 kind::f16" if m > 8 else "cuda-core"}
+        if m > 8:  # against the dense f16/bf16 tensor peak as well
+            sweep[str(m)]["tensor_frac"] = round(tflops / tensor_peak, 4)
         del g
-    out[s.name] = sweep
     del packs, base
-    torch.cuda.empty_cache()
-    out.update(int4_workload(torch, synth, thinmx, device, hbm, l2))
-    torch.cuda.empty_cache()
-    out.update(moe_workload(torch, synth, loader, thinmx, device, hbm))
-    torch.cuda.empty_cache()
-    out["peak"] = {"hbm_gbs": hbm, "source": peak_kind}
-    return out
+    return {s.name: sweep}
 
 
 def int4_workload(torch, synth, thinmx, device, hbm, l2, reps=50):

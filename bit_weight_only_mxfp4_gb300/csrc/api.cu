@@ -147,10 +147,11 @@ tt_status tt_mxfp4_swiglu_matvec(const void* packed, int64_t n, int64_t k,
   if (m < 1 || m > 64) return TT_ERR_SHAPE;
   if (!packed || !x_bf16 || !h_bf16) return TT_ERR_NULL;
   if (!aligned(packed, 16) || !aligned(x_bf16, 16) || !aligned(h_bf16, 2)) return TT_ERR_ALIGN;
-  if (m > 8) return TT_ERR_UNSUPPORTED;
   const cudaError_t e =
-      tt::launch_swiglu_mxfp4_cc(static_cast<const uint8_t*>(packed), int(n), int(k), x_bf16,
-                                 int(m), h_bf16, as_stream(stream), kPdl);
+      m > 8 ? tt::launch_swiglu_mxfp4_tc(static_cast<const uint8_t*>(packed), int(n), int(k),
+                                         x_bf16, int(m), h_bf16, as_stream(stream), kPdl)
+            : tt::launch_swiglu_mxfp4_cc(static_cast<const uint8_t*>(packed), int(n), int(k),
+                                         x_bf16, int(m), h_bf16, as_stream(stream), kPdl);
   if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
   return from_cuda(e);
 }

@@ -92,12 +92,19 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Waits for the phase with the given parity to complete; false if it did not
 // within kWaitLimitNs.
+// Suspend-time hint of the bounded wait (0: plain try_wait polling).
+#ifndef TT_WAIT_HINT_NS
+#define TT_WAIT_HINT_NS 0
+#endif
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  for (uint32_t it = 1;; ++it) {
+    if (TT_WAIT_HINT_NS > 0 ? mbar_try_wait_sleep(bar, parity, TT_WAIT_HINT_NS)
+                            : mbar_try_wait(bar, parity))
+      return true;
+    if ((it & 15u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 

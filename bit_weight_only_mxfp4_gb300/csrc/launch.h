@@ -34,6 +34,11 @@ cudaError_t launch_quantize_int4(const float* w, int64_t n, int64_t k, int group
 cudaError_t launch_swiglu_mxfp4_cc(const uint8_t* packed, int n, int k, const uint16_t* x,
                                    int m, uint16_t* h, cudaStream_t s, bool pdl);
 
+// tc_swiglu.cu — tcgen05 gate/up SwiGLU, m in [9, 64], k % 64 == 0
+cudaError_t launch_swiglu_mxfp4_tc(const uint8_t* packed, int n, int k, const uint16_t* x,
+                                   int m, uint16_t* h, cudaStream_t s, bool pdl);
+int tc_swiglu_smem_bytes(int m, int k);
+
 // gemv_int4.cu — grouped affine INT4 matvec, m in [1, 8]
 cudaError_t launch_int4_matvec(const uint8_t* codes, const uint16_t* scales, const uint8_t* zp,
                                int n, int k, int group, const uint16_t* x, int m, uint16_t* y,

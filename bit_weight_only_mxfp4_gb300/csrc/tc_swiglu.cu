@@ -1,0 +1,467 @@
+// Tensor-core (tcgen05) MXFP4 gate/up SwiGLU for batches m = 9..64.
+//
+// At m >= 16 the gate/up product is a real dense contraction (config:
+// Phi-4 sizes, K = 5120, N = 17920), so it runs on the 5th-generation tensor
+// cores.  The pages' prior art is Triton's tl.dot_scaled over the selected
+// experts, with fast_math off because lossy accumulation broke the MoE
+// trajectory (stardance.hackclub.com/projects/29750, MoE drift devlog); here
+// the products are exact and accumulate in fp32 in tensor memory.
+//
+// Layout of the computation (swap-AB): one CTA owns 128 output rows (gate
+// rows n0..n0+127 and the matching up rows) and all m batch rows.
+//   A = W tile   [128 rows x 64 k]  f16, K-major, 128-byte swizzle
+//   B = x tile   [N     x 64 k]     f16, K-major, 128-byte swizzle, N = m
+//                                    rounded up to 16 (pad rows are zero)
+//   D_g, D_u     [128 x N] fp32 in tensor memory (2N columns)
+// Warps 0-7 produce: thread t decodes half a k-tile (one 32-weight block) of
+// row t % 128 for gate and up: cvt.rn.f16x2.e2m1x2, then an exact HMUL2 by
+// 2^(X_block - X_row) where X_row is the row's largest block exponent (so the
+// f16 values stay in range and exact), stored in the swizzled layout; and
+// converts its share of the x tile (bf16 -> f16; |x| must stay below 65504,
+// larger values raise TT_ERR_UNSUPPORTED in the device error word).
+// Warp 9 brings each k-tile in with three TMA loads (gate codes 128 x 32 B,
+// up codes 128 x 32 B, both strided by the packed record size, and the x
+// tile, whose padding rows TMA fills with zeros) into a ring of raw slots.
+// Warp 8 allocates tensor memory, waits for each stage and issues the
+// tcgen05.mma (M=128, N, K=16) x 4 per matrix per stage, then tcgen05.commit
+// releases the stage.  Warps 0-3 finally read D with tcgen05.ld (warp w owns
+// TMEM lanes 32w..32w+31 = rows), scale by 2^X_row and the postscale, apply
+// silu(g)*u and store bf16.
+#include <cuda.h>  // CUtensorMap (types only; the encoder comes from the runtime's driver entry point)
+
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+#include "layout.cuh"
+
+namespace tt {
+namespace {
+
+constexpr int kGroupWarps = 8;                  // one producer group: 256 threads
+constexpr int kGroups = 2;                       // groups decode alternate k-tiles
+constexpr int kProdWarps = kGroupWarps * kGroups;
+constexpr int kMmaWarp = kProdWarps;             // tensor memory + MMA issue
+constexpr int kTmaWarp = kProdWarps + 1;         // TMA loads
+constexpr int kThreads = (kProdWarps + 2) * 32;  // 576
+constexpr int kTileRows = 128;
+constexpr int kTileK = 64;                      // f16: 128 bytes = one swizzle row
+constexpr int kStages = 3;
+constexpr int kErrUnsupported = 5;              // TT_ERR_UNSUPPORTED
+
+// ---- tcgen05 / descriptor helpers ------------------------------------------
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (tcgen05 descriptor version 1).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);          // start address
+  d |= uint64_t(1u) << 16;                        // leading byte offset (16 B; unused)
+  d |= uint64_t((1024u >> 4) & 0x3FFFu) << 32;    // stride byte offset: 1024 B
+  d |= uint64_t(1u) << 46;                        // descriptor version
+  d |= uint64_t(2u) << 61;                        // layout: 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: A, B f16, D f32, both K-major.
+__device__ __forceinline__ uint32_t idesc_f16(int n) {
+  return (1u << 4)                        // D format f32
+         | (0u << 7) | (0u << 10)         // A, B format f16
+         | (uint32_t(n >> 3) << 17)       // N / 8
+         | (uint32_t(kTileRows >> 4) << 24);  // M / 16
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// f16x2 (2^e, 2^e) for an exponent e <= 0; e < -24 underflows to zero.
+__device__ __forceinline__ uint32_t pow2_f16x2(int e) {
+  uint32_t h;
+  if (e >= -14) h = uint32_t(e + 15) << 10;               // normal
+  else if (e >= -24) h = 1u << (e + 24);                  // subnormal
+  else h = 0u;
+  return h | (h << 16);
+}
+
+// Physical offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte
+// swizzled tile (8-row groups of 1024 bytes).
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return uint32_t(r) * 128u + (uint32_t(c ^ (r & 7)) << 4);
+}
+
+// 2-D TMA load of a box at (c0 inner, c1 outer) into shared memory,
+// completion as tx bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory plan of one CTA (offsets from a 1024-aligned base).
+struct TcPlan {
+  static constexpr int kRaw = 4;  // k-tiles in flight (raw slots)
+  int np;          // MMA N (batch rows padded to 16)
+  int nblk;        // k / 32
+  int a_bytes;     // one A tile: 128 x 128 B
+  int stage_bytes; // A_g + A_u + B, 1024-aligned
+  int raw_bytes;   // one raw slot: gate 4 KB + up 4 KB + x np x 128 B
+  int off_raw, off_scale, off_xr, off_bar, off_tmem, total;
+  __host__ __device__ TcPlan(int m, int k) {
+    np = (m + 15) & ~15;
+    nblk = k >> 5;
+    a_bytes = kTileRows * 128;
+    stage_bytes = (2 * a_bytes + np * 128 + 1023) & ~1023;
+    raw_bytes = (2 * kTileRows * 32 + np * 128 + 127) & ~127;
+    off_raw = kStages * stage_bytes;
+    off_scale = off_raw + kRaw * raw_bytes;
+    off_xr = off_scale + 2 * kTileRows * nblk;
+    off_bar = (off_xr + 2 * kTileRows * 4 + 7) & ~7;
+    off_tmem = off_bar + (2 * kStages + 2 * kRaw + 1) * 8;
+    total = off_tmem + 16 + 1024;  // + alignment slack of the dynamic base
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_swiglu_kernel(const __grid_constant__ CUtensorMap map_w,
+                     const __grid_constant__ CUtensorMap map_x, const uint8_t* __restrict__ packed,
+                     int n, int k, int m, uint16_t* __restrict__ h, int32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const SwigluRecord L(k);
+  const TcPlan P(m, k);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (sbase - smem_u32(smem_raw));
+  uint8_t* sscale = base + P.off_scale;                        // [2][128][nblk]
+  int* sxr = reinterpret_cast<int*>(base + P.off_xr);          // [2][128]
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(base + P.off_bar);
+  uint64_t* a_empty = a_full + kStages;
+  uint64_t* raw_full = a_empty + kStages;
+  uint64_t* raw_empty = raw_full + TcPlan::kRaw;
+  uint64_t* done = raw_empty + TcPlan::kRaw;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + P.off_tmem);
+  const int n0 = blockIdx.x * kTileRows;
+  const int nkt = k / kTileK;
+  const uint32_t tcols = (2 * P.np <= 32) ? 32u : (2 * P.np <= 64 ? 64u : 128u);
+  const uint32_t raw_tx = uint32_t(2 * kTileRows * 32 + P.np * 128);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&a_full[s]), kGroupWarps * 32);
+      mbar_init(smem_u32(&a_empty[s]), 1);
+    }
+    for (int d = 0; d < TcPlan::kRaw; ++d) {
+      mbar_init(smem_u32(&raw_full[d]), 1);
+      mbar_init(smem_u32(&raw_empty[d]), kGroupWarps * 32);
+    }
+    mbar_init(smem_u32(done), 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), tcols);
+  // Per-row block scales into shared memory and each row's largest block
+  // exponent: gate rows by threads 0-127, up rows by 128-255.
+  if (warp < kGroupWarps) {
+    const int t = threadIdx.x, r = t & 127, which = t >> 7;
+    const bool valid = n0 + r < n;
+    const uint8_t* src =
+        packed + (int64_t)(valid ? n0 + r : 0) * L.bytes + (which ? L.up_scales() : L.gate_scales());
+    uint8_t* dst = sscale + (which * kTileRows + r) * P.nblk;
+    int xmax = -1000;
+    for (int b = 0; b < P.nblk; ++b) {
+      const uint32_t sb = valid ? src[b] : 0u;
+      dst[b] = uint8_t(sb);
+      if (sb != 255u) xmax = max(xmax, int(sb) - 127);
+    }
+    sxr[which * kTileRows + r] = xmax < -127 ? -127 : xmax;
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  pdl_allow_next_grid();
+
+  auto raw_slot = [&](int d) { return sbase + uint32_t(P.off_raw + d * P.raw_bytes); };
+
+  if (warp == kTmaWarp) {
+    // ---------------- TMA loads ----------------
+    if (lane == 0) {
+      const int pre = min(TcPlan::kRaw, nkt);
+      // weights do not depend on the previous kernel: start them before waiting
+      for (int kt = 0; kt < pre; ++kt) {
+        const uint32_t dst = raw_slot(kt), bar = smem_u32(&raw_full[kt]);
+        mbar_arrive_expect_tx(bar, raw_tx);
+        tma_load_2d(dst, &map_w, kt * 32, n0, bar);
+        tma_load_2d(dst + 4096, &map_w, k / 2 + kt * 32, n0, bar);
+      }
+      pdl_wait_prior_grid();  // x is produced by the previous kernel
+      for (int kt = 0; kt < pre; ++kt)
+        tma_load_2d(raw_slot(kt) + 8192, &map_x, kt * kTileK, 0, smem_u32(&raw_full[kt]));
+      bool ok = true;
+      for (int kt = pre; kt < nkt; ++kt) {
+        const int d = kt % TcPlan::kRaw;
+        ok = mbar_wait_bounded(smem_u32(&raw_empty[d]), uint32_t(((kt / TcPlan::kRaw) - 1) & 1));
+        if (!ok) break;
+        const uint32_t dst = raw_slot(d), bar = smem_u32(&raw_full[d]);
+        mbar_arrive_expect_tx(bar, raw_tx);
+        tma_load_2d(dst, &map_w, kt * 32, n0, bar);
+        tma_load_2d(dst + 4096, &map_w, k / 2 + kt * 32, n0, bar);
+        tma_load_2d(dst + 8192, &map_x, kt * kTileK, 0, bar);
+      }
+      if (!ok) flag_error(err, kErrTimeout);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(P.np);
+      bool ok = true;
+      for (int kt = 0; kt < nkt && ok; ++kt) {
+        const int s = kt % kStages;
+        ok = mbar_wait_bounded(smem_u32(&a_full[s]), uint32_t((kt / kStages) & 1));
+        if (!ok) break;
+        fence_after_sync();
+        const uint32_t ag = sbase + uint32_t(s * P.stage_bytes);
+        const uint32_t au = ag + uint32_t(P.a_bytes);
+        const uint32_t bx = au + uint32_t(P.a_bytes);
+#pragma unroll
+        for (int kk = 0; kk < kTileK / 16; ++kk) {
+          const uint32_t koff = uint32_t(kk * 32);  // 16 f16 = 32 bytes along K
+          const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
+          mma_f16(tmem, smem_desc_sw128(ag + koff), smem_desc_sw128(bx + koff), idesc, acc);
+          mma_f16(tmem + uint32_t(P.np), smem_desc_sw128(au + koff), smem_desc_sw128(bx + koff),
+                  idesc, acc);
+        }
+        mma_commit(smem_u32(&a_empty[s]));  // stage s free once these MMAs are done
+      }
+      if (!ok) flag_error(err, kErrTimeout);
+      mma_commit(smem_u32(done));
+      // Wait for our own MMAs before tensor memory can be released.
+      (void)mbar_wait_bounded(smem_u32(done), 0u);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- producers: decode W, convert x ----------------
+    // group g decodes k-tiles g, g + kGroups, ...; thread t of the group owns
+    // half a k-tile (one 32-weight block) of row t % 128
+    const int g = warp / kGroupWarps;
+    const int t = threadIdx.x - g * kGroupWarps * 32, r = t & 127, half = t >> 7;
+    const int xg = sxr[r], xu = sxr[kTileRows + r];
+    bool ok = true;
+    for (int kt = g; kt < nkt; kt += kGroups) {
+      const int s = kt % kStages, d = kt % TcPlan::kRaw;
+      ok = mbar_wait_bounded(smem_u32(&raw_full[d]), uint32_t((kt / TcPlan::kRaw) & 1));
+      if (ok && kt >= kStages)
+        ok = mbar_wait_bounded(smem_u32(&a_empty[s]), uint32_t(((kt / kStages) - 1) & 1));
+      if (!ok) break;
+      const uint8_t* rw = base + P.off_raw + d * P.raw_bytes;
+      uint8_t* stage = base + s * P.stage_bytes;
+      // W: one 32-weight block per matrix -> 4 swizzled 16-byte chunks each
+#pragma unroll
+      for (int mat = 0; mat < 2; ++mat) {
+        const uint4 c = *reinterpret_cast<const uint4*>(rw + mat * 4096 + r * 32 + half * 16);
+        const uint32_t sb = sscale[(mat * kTileRows + r) * P.nblk + kt * 2 + half];
+        const uint32_t f = sb == 255u ? 0x7E007E00u : pow2_f16x2(int(sb) - 127 - (mat ? xu : xg));
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+        uint8_t* a = stage + mat * P.a_bytes;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t h0, h1, h2, h3;
+          e2m1x8_to_f16x2(w[q], h0, h1, h2, h3);
+          *reinterpret_cast<uint4*>(a + sw128(r, half * 4 + q)) =
+              make_uint4(hmul2(h0, f), hmul2(h1, f), hmul2(h2, f), hmul2(h3, f));
+        }
+      }
+      // x: bf16 -> f16 (|x| < 65504; larger values are flagged)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = t + j * kGroupWarps * 32;  // row c / 8, 16-byte piece c % 8
+        const int row = c >> 3, piece = c & 7;
+        if (row < P.np) {
+          const uint4 v = *reinterpret_cast<const uint4*>(rw + 8192 + row * 128 + piece * 16);
+          const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[4];
+          bool big = false;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = bf16_bits_to_f32(vw[e] & 0xFFFFu), hi = bf16_bits_to_f32(vw[e] >> 16);
+            big = big || fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+            o[e] = pack_f16x2_scaled(lo, hi, 1.0f);
+          }
+          if (big) flag_error(err, kErrUnsupported);
+          *reinterpret_cast<uint4*>(stage + 2 * P.a_bytes + sw128(row, piece)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      fence_proxy_async();
+      mbar_arrive(smem_u32(&a_full[s]));
+      mbar_arrive(smem_u32(&raw_empty[d]));
+    }
+    if (!ok) flag_error(err, kErrTimeout);
+  }
+
+  // ---------------- epilogue: warps 0-3, thread = row ----------------
+  if (warp < 4) {
+    const int r = threadIdx.x;
+    const bool ok = mbar_wait_bounded(smem_u32(done), 0u);
+    fence_after_sync();
+    if (ok) {
+      pdl_wait_prior_grid();  // (no-op if already waited) before writing h
+      const int nr = n0 + r;
+      const uint8_t* rec = packed + (int64_t)(nr < n ? nr : 0) * L.bytes;
+      const float sg = scalbnf(*reinterpret_cast<const float*>(rec + L.post), sxr[r]);
+      const float su =
+          scalbnf(*reinterpret_cast<const float*>(rec + L.post + 4), sxr[kTileRows + r]);
+      const uint32_t lane_base = uint32_t(warp * 32) << 16;
+      for (int c0 = 0; c0 < P.np; c0 += 16) {
+        float g[16], u[16];
+        tmem_ld16(tmem + lane_base + uint32_t(c0), g);
+        tmem_ld16(tmem + lane_base + uint32_t(P.np + c0), u);
+        if (nr < n) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int mm = c0 + i;
+            if (mm < m) {
+              __nv_bfloat16 b = __float2bfloat16_rn(silu_mul(g[i] * sg, u[i] * su));
+              h[(size_t)mm * n + nr] = *reinterpret_cast<uint16_t*>(&b);
+            }
+          }
+        }
+      }
+    } else if (lane == 0) {
+      flag_error(err, kErrTimeout);
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    fence_after_sync();
+    tmem_dealloc(tmem, tcols);
+  }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (the
+// library does not link the driver library directly).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+int tc_swiglu_smem_bytes(int m, int k) { return TcPlan(m, k).total; }
+
+cudaError_t launch_swiglu_mxfp4_tc(const uint8_t* packed, int n, int k, const uint16_t* x, int m,
+                                   uint16_t* h, cudaStream_t s, bool pdl) {
+  const DeviceInfo* di = device_info();
+  if (!di) return cudaErrorNoDevice;
+  if (k % kTileK != 0 || m < 1 || m > 64) return cudaErrorInvalidConfiguration;
+  const TcPlan P(m, k);
+  if (P.total > di->smem_optin) return cudaErrorInvalidConfiguration;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const SwigluRecord L(k);
+  CUtensorMap map_w, map_x;
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(L.bytes), cuuint64_t(n)};
+    const cuuint64_t strides[1] = {cuuint64_t(L.bytes)};
+    const cuuint32_t box[2] = {32u, cuuint32_t(kTileRows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    if (enc(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(k), cuuint64_t(m)};
+    const cuuint64_t strides[1] = {cuuint64_t(k) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(kTileK), cuuint32_t(P.np)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    if (enc(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(tc_swiglu_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, P.total);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n + kTileRows - 1) / kTileRows);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = P.total;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, tc_swiglu_kernel, map_w, map_x, packed, n, k, m, h,
+                            di->error_word);
+}
+
+}  // namespace tt

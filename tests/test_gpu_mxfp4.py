@@ -123,6 +123,9 @@ def _swiglu_case(n, k, m, postscale=True, wid=92, layer=0):
     (50, 5120, 1, False), (33, 8192, 1, True), (21, 16384, 1, True),
     (77, 2048, 2, True), (77, 2048, 3, False), (45, 5120, 4, True), (40, 2880, 8, True),
     (31, 1056, 5, True), (19, 6144, 6, False),
+    # tcgen05 tensor-core path (m >= 9, k % 64 == 0); ragged row tiles
+    (128, 128, 16, True), (130, 2048, 16, True), (300, 2880, 32, False), (256, 5120, 64, True),
+    (77, 1024, 9, True), (129, 4096, 40, True), (1000, 768, 63, True),
 ])
 def test_swiglu_matvec_shapes(n, k, m, post):
     h, ref, _, _ = _swiglu_case(n, k, m, post)
@@ -185,10 +188,22 @@ def test_swiglu_full_batch_sweep_sampled_rows():
     rows = np.sort(g.choice(c.n, 192, replace=False))
     rows = np.unique(np.concatenate([rows, [0, c.n - 1]]))
     hgc, hgs, huc, hus = gu.host(gc), gu.host(gs), gu.host(uc), gu.host(us)
-    for m in [1, 2, 4, 8]:
+    for m in [1, 2, 4, 8, 16, 32, 64]:
         x = synth.normal_bf16(synth.rng(c.wid, 0, 2), (m, c.k))
         h = gu.swiglu(packed, c.n, c.k, x)
         ref = oracle.mxfp4_swiglu_matvec((hgc[rows], hgs[rows], pg[rows]),
                                          (huc[rows], hus[rows], pu[rows]), x)
         assert_float_parity(h[:, rows], ref, f"sweep m={m}")
     torch.cuda.empty_cache()
+
+
+def test_tensor_path_rejects_k_not_multiple_of_64():
+    import torch
+    from bit_weight_only_mxfp4_gb300 import thinmx
+    n, k = 64, 96
+    packed = torch.zeros(thinmx.tt_mxfp4_swiglu_packed_bytes(n, k), dtype=torch.uint8, device="cuda")
+    x = torch.zeros((16, k), dtype=torch.int16, device="cuda")
+    h = torch.zeros((16, n), dtype=torch.int16, device="cuda")
+    with pytest.raises(thinmx.ThinmxError) as e:
+        thinmx.tt_mxfp4_swiglu_matvec(packed, n, k, x, 16, h)
+    assert e.value.status == 5  # TT_ERR_UNSUPPORTED, nothing launched
