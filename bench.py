@@ -239,8 +239,12 @@ def main():
     ap.add_argument("--impl", default="thinmx", choices=["thinmx", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--only", default=None, choices=["gate_up", "moe", "int4", "sweep"],
+    ap.add_argument("--only", default=None, choices=["gate_up", "bf16", "moe", "int4", "sweep"],
                     help="run one small workload only (for profiler captures)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="with --only moe: MoE layers to build (default: the full stack)")
+    ap.add_argument("--ms", default=None,
+                    help="with --only sweep: comma-separated batch sizes (default: all)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -274,12 +278,16 @@ def main():
         if args.only == "gate_up":
             r = single_gate_up(torch, synth, loader, thinmx, device, hbm, copies=4,
                                reps=args.steps)
+        elif args.only == "bf16":
+            r = single_bf16(torch, synth, thinmx, device, hbm, copies=2, reps=args.steps)
         elif args.only == "sweep":
-            r = secondary_sweep(torch, synth, loader, thinmx, device, hbm)
+            ms = tuple(int(v) for v in args.ms.split(",")) if args.ms else None
+            r = secondary_sweep(torch, synth, loader, thinmx, device, hbm, ms=ms)
         elif args.only == "int4":
             r = int4_workload(torch, synth, thinmx, device, hbm, 0, reps=args.steps)
         else:
-            r = moe_workload(torch, synth, loader, thinmx, device, hbm, reps=args.steps)
+            r = moe_workload(torch, synth, loader, thinmx, device, hbm, reps=args.steps,
+                             layers=args.layers)
         print(json.dumps({"only": args.only, **r}))
         return 0
 
@@ -449,6 +457,28 @@ def single_gate_up(torch, synth, loader, thinmx, device, hbm, copies=None, reps=
                      "rotating_copies": copies}}
 
 
+def single_bf16(torch, synth, thinmx, device, hbm, copies=2, reps=50):
+    """One SmolLM3 bf16 gate/up layer at M=1 (90 MB of weights per copy)."""
+    c = synth.STACK
+    per = 4 * c.n * c.k + 2 * c.k + 2 * c.n
+    bufs = []
+    for i in range(copies):
+        wg = synth.torch_normal((c.n, c.k), synth.WEIGHT_STD, c.wid, 24 + i, 0,
+                                device).to(torch.bfloat16)
+        wu = synth.torch_normal((c.n, c.k), synth.WEIGHT_STD, c.wid, 24 + i, 1,
+                                device).to(torch.bfloat16)
+        x = synth.torch_normal((1, c.k), 1.0, c.wid, 24 + i, 2, device).to(torch.bfloat16)
+        h = torch.empty((1, c.n), dtype=torch.bfloat16, device=device)
+        bufs.append((wg, wu, x, h))
+    g = capture(torch, lambda: [thinmx.tt_bf16_swiglu_matvec(wg, wu, c.n, c.k, x, 1, h)
+                                for wg, wu, x, h in bufs])
+    ms = time_graph(torch, g, reps) / copies
+    del bufs, g
+    return {"bf16_gate_up_k2048_n11008_m1": {
+        "us": round(ms * 1e3, 3), "GBps": round(per / (ms * 1e-3) / 1e9, 1),
+        "frac": round(per / (ms * 1e-3) / 1e9 / hbm, 4), "bytes": per, "rotating_copies": copies}}
+
+
 def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
     """Single gate/up layer (rotating copies > 2x L2), the Phi-4 batch sweep,
     the INT4 QKV projection and the MoE stack."""
@@ -465,7 +495,7 @@ def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
     return out
 
 
-def secondary_sweep(torch, synth, loader, thinmx, device, hbm, reps=20):
+def secondary_sweep(torch, synth, loader, thinmx, device, hbm, reps=20, ms=None):
     """Phi-4 gate/up (K=5120, N=17920) over the batch sizes: CUDA-core kernel
     for m <= 8, tcgen05 tensor-core kernel above; weight copies > 2x L2."""
     tensor_peak = tensor_peak_tflops()
@@ -481,7 +511,7 @@ def secondary_sweep(torch, synth, loader, thinmx, device, hbm, reps=20):
     copies = max(3, int(2 * l2 // per_w) + 1)
     packs = [base] + [base.clone() for _ in range(copies - 1)]
     sweep = {}
-    for m in s.ms:
+    for m in (ms or s.ms):
         xs = [synth.torch_normal((m, s.k), 1.0, s.wid, 0, 2, device).to(torch.bfloat16)
               for _ in range(copies)]
         hs = [torch.empty((m, s.n), dtype=torch.bfloat16, device=device) for _ in range(copies)]
@@ -528,7 +558,7 @@ def int4_workload(torch, synth, thinmx, device, hbm, l2, reps=50):
                      "rotating_copies": copies}}
 
 
-def moe_workload(torch, synth, loader, thinmx, device, hbm, reps=20):
+def moe_workload(torch, synth, loader, thinmx, device, hbm, reps=20, layers=None):
     """gpt-oss-20b-shaped MoE stack: 24 layers, 32 MXFP4 experts each
     (hidden = inter = 2880), top-4; one call per layer, all weights resident
     (~10 GB, far beyond L2)."""
@@ -536,8 +566,9 @@ def moe_workload(torch, synth, loader, thinmx, device, hbm, reps=20):
     H, I, E, K = c.hidden, c.inter, c.experts, c.top_k
     sw = thinmx.tt_mxfp4_swiglu_packed_bytes(I, H)
     rw = thinmx.tt_mxfp4_rows_packed_bytes(H, I)
+    n_layers = layers or c.layers
     layers = []
-    for l in range(c.layers):
+    for l in range(n_layers):
         gu = torch.empty(E * sw, dtype=torch.uint8, device=device)
         dn = torch.empty(E * rw, dtype=torch.uint8, device=device)
         for e in range(E):
@@ -556,7 +587,7 @@ def moe_workload(torch, synth, loader, thinmx, device, hbm, reps=20):
     idx = torch.empty(K, dtype=torch.int32, device=device)
     prob = torch.empty(K, dtype=torch.float32, device=device)
     wsb = thinmx.tt_moe_workspace_bytes(H, I, E, K)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=device)  # counters start at zero
     torch.cuda.synchronize()
 
     def step():
@@ -564,13 +595,13 @@ def moe_workload(torch, synth, loader, thinmx, device, hbm, reps=20):
             thinmx.tt_moe_mxfp4_topk_mlp(x, H, I, wr, E, K, gu, dn, out, idx, prob, ws, wsb)
 
     g = capture(torch, step)
-    ms = time_graph(torch, g, reps) / c.layers
+    ms = time_graph(torch, g, reps) / n_layers
     per = E * H * 2 + K * (2 * I * (H // 2 + H // 32) + H * (I // 2 + I // 32)) + 2 * H + 2 * H
     del layers, g
     return {c.name: {"us_per_layer": round(ms * 1e3, 3),
                      "GBps": round(per / (ms * 1e-3) / 1e9, 1),
                      "frac": round(per / (ms * 1e-3) / 1e9 / hbm, 4), "bytes_per_layer": per,
-                     "layers": c.layers, "kernels_per_layer": 3}}
+                     "layers": n_layers, "kernels_per_layer": 1}}
 
 
 def reference_arm(args, world, rank):

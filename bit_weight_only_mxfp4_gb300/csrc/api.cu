@@ -58,7 +58,8 @@ inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
 constexpr int64_t kMaxK = 16384;
-static_assert(TT_MOE_STATIC_MAX_TOPK_INTER == tt::kMoeStaticMaxHFloats,
+constexpr int64_t kMoeMaxHidden = 8192;
+static_assert(TT_MOE_STATIC_MAX_HIDDEN == tt::kMoeStaticMaxHidden,
               "header limit and scratch array size must agree");
 
 // Programmatic dependent launch on the hot-path kernels.
@@ -170,7 +171,7 @@ tt_status tt_bf16_swiglu_matvec(const uint16_t* wg, const uint16_t* wu, int64_t 
 
 size_t tt_mxfp4_rows_packed_bytes(int64_t n, int64_t k) {
   if (n < 1 || k < 32 || k % 32 != 0 || k > kMaxK || n > kMaxRows) return 0;
-  return size_t(n) * size_t(tt::RowRecord(int(k)).bytes);
+  return size_t(tt::ColSlices(n, int(k)).bytes);
 }
 
 tt_status tt_mxfp4_pack_rows(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k,
@@ -184,7 +185,7 @@ tt_status tt_mxfp4_pack_rows(const uint8_t* codes, const uint8_t* scales, int64_
 }
 
 size_t tt_moe_workspace_bytes(int64_t hidden, int64_t inter, int32_t n_experts, int32_t top_k) {
-  if (hidden < 32 || inter < 32 || n_experts < 1 || n_experts > 256 || top_k < 1 || top_k > 8 ||
+  if (hidden < 32 || hidden > kMoeMaxHidden || inter < 32 || n_experts < 1 || n_experts > 256 || top_k < 1 || top_k > 8 ||
       top_k > n_experts)
     return 0;
   return tt::moe_workspace_bytes(hidden, inter, n_experts, top_k);
@@ -195,7 +196,7 @@ tt_status tt_moe_mxfp4_topk_mlp(const uint16_t* x_bf16, int64_t hidden, int64_t 
                                 const void* gate_up_packed, const void* down_packed,
                                 uint16_t* out_bf16, int32_t* out_idx, float* out_prob,
                                 void* workspace, size_t workspace_bytes, void* stream) {
-  if (hidden < 32 || hidden % 32 != 0 || hidden > kMaxK) return TT_ERR_SHAPE;
+  if (hidden < 32 || hidden % 32 != 0 || hidden > kMoeMaxHidden) return TT_ERR_SHAPE;
   if (inter < 32 || inter % 32 != 0 || inter > 8192) return TT_ERR_SHAPE;
   if (n_experts < 1 || n_experts > 256 || top_k < 1 || top_k > 8 || top_k > n_experts)
     return TT_ERR_SHAPE;
@@ -221,11 +222,11 @@ tt_status tt_moe_mxfp4_topk_mlp_static(const uint16_t* x_bf16, int64_t hidden, i
                                        int32_t top_k, const void* gate_up_packed,
                                        const void* down_packed, uint16_t* out_bf16,
                                        int32_t* out_idx, float* out_prob, void* stream) {
-  if (hidden < 32 || hidden % 32 != 0 || hidden > kMaxK) return TT_ERR_SHAPE;
+  if (hidden < 32 || hidden % 32 != 0 || hidden > kMoeMaxHidden) return TT_ERR_SHAPE;
   if (inter < 32 || inter % 32 != 0 || inter > 8192) return TT_ERR_SHAPE;
   if (n_experts < 1 || n_experts > 256 || top_k < 1 || top_k > 8 || top_k > n_experts)
     return TT_ERR_SHAPE;
-  if (int64_t(top_k) * inter > TT_MOE_STATIC_MAX_TOPK_INTER) return TT_ERR_SIZE;
+  if (hidden > TT_MOE_STATIC_MAX_HIDDEN) return TT_ERR_SIZE;
   if (!x_bf16 || !router_w_bf16 || !gate_up_packed || !down_packed || !out_bf16 || !out_idx ||
       !out_prob)
     return TT_ERR_NULL;

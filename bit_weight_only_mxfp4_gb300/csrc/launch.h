@@ -44,14 +44,21 @@ cudaError_t launch_int4_matvec(const uint8_t* codes, const uint16_t* scales, con
                                int n, int k, int group, const uint16_t* x, int m, uint16_t* y,
                                cudaStream_t s, bool pdl);
 
-// moe.cu — router, top-k, gathered gate/up and down of the selected experts
+// moe.cu / moe_fused.cu — router, top-k, the selected experts' gate/up and
+// down as one cooperative kernel (moe_fused.cu); plan that does not fit the
+// shared memory: cudaErrorInvalidConfiguration
 size_t moe_workspace_bytes(int64_t hidden, int64_t inter, int n_experts, int top_k);
+size_t moe_fused_workspace_bytes(int64_t hidden);
 cudaError_t launch_moe(const uint16_t* x, int hidden, int inter, const uint16_t* wr, int E,
                        int top_k, const uint8_t* gu, const uint8_t* dn, uint16_t* out,
                        int32_t* out_idx, float* out_prob, void* ws, cudaStream_t s, bool pdl);
+cudaError_t launch_moe_fused(const uint16_t* x, int hidden, int inter, const uint16_t* wr, int E,
+                             int top_k, const uint8_t* gu, const uint8_t* dn, uint16_t* out,
+                             int32_t* out_idx, float* out_prob, void* ws, cudaStream_t s,
+                             bool pdl);
 // The library-owned MoE scratch (a static device array) of the current
 // device: its address (looked up on the first call on each device) and size.
-constexpr int kMoeStaticMaxHFloats = 32768;  // top_k * inter limit
+constexpr int kMoeStaticMaxHidden = 4096;  // hidden limit of the static scratch
 cudaError_t moe_static_scratch(void** ptr, size_t* bytes);
 
 // gemv_bf16.cu

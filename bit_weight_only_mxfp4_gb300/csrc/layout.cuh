@@ -30,15 +30,30 @@ struct SwigluRecord {
   __host__ __device__ int up_scales() const { return k + nblk; }
 };
 
-// Packed single-matrix ("rows") layout used for the MoE down projection:
-//   [codes k/2 B][scales k/32 B][pad to 16]
-struct RowRecord {
-  int k, nblk, bytes;
-  __host__ __device__ explicit RowRecord(int k_) : k(k_), nblk(k_ >> 5) {
-    bytes = (k / 2 + nblk + 15) & ~15;
+// Packed single-matrix layout used for the MoE down projections, sliced by
+// COLUMNS so that a CTA owning a 16-wide slice of the reduction index (the
+// experts' SwiGLU outputs it computed itself) reads that slice of every row
+// as one contiguous run:
+//
+//   codes : [k/16 slices][n rows][8 B]   (the row's canonical code bytes
+//                                         8s .. 8s+7, i.e. k = 16s .. 16s+15)
+//   scales: [k/32 blocks][n rows][1 B]   (the row's E8M0 byte of block b)
+//
+// each region padded to 16 bytes.  Codes and scales keep their bytes.
+struct ColSlices {
+  int64_t n;
+  int k, nslice, nblk;
+  int64_t codes_bytes, scales_off, bytes;
+  __host__ __device__ ColSlices(int64_t n_, int k_) : n(n_), k(k_), nslice(k_ >> 4), nblk(k_ >> 5) {
+    codes_bytes = (n * (k >> 1) + 15) & ~int64_t(15);
+    scales_off = codes_bytes;
+    bytes = scales_off + ((n * nblk + 15) & ~int64_t(15));
   }
-  __host__ __device__ int codes() const { return 0; }
-  __host__ __device__ int scales() const { return k >> 1; }
+  // byte offset of (slice s, row r)'s 8 code bytes / of (block b, row r)'s scale
+  __host__ __device__ int64_t code_at(int s, int64_t r) const { return ((int64_t)s * n + r) * 8; }
+  __host__ __device__ int64_t scale_at(int b, int64_t r) const {
+    return scales_off + (int64_t)b * n + r;
+  }
 };
 
 }  // namespace tt

@@ -127,21 +127,26 @@ __global__ void pack_swiglu_kernel(const uint8_t* __restrict__ gc, const uint8_t
   }
 }
 
+// One thread per output byte of the column-sliced layout (ColSlices).
 __global__ void pack_rows_kernel(const uint8_t* __restrict__ codes,
                                  const uint8_t* __restrict__ scales, int64_t n, int k,
                                  uint8_t* __restrict__ packed) {
-  const RowRecord L(k);
-  const int64_t total = n * L.bytes;
+  const ColSlices L(n, k);
   const int half = k >> 1;
-  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < L.bytes;
        t += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = t / L.bytes;
-    const int o = int(t - r * L.bytes);
     uint32_t v = 0;
-    if (o < half)
-      v = codes[r * half + o];
-    else if (o < half + L.nblk)
-      v = scales[r * L.nblk + (o - half)];
+    if (t < n * half) {  // codes: t = (slice * n + row) * 8 + byte
+      const int64_t sr = t >> 3;
+      const int sl = int(sr / n);
+      const int64_t r = sr - (int64_t)sl * n;
+      v = codes[r * half + sl * 8 + (t & 7)];
+    } else if (t >= L.scales_off && t < L.scales_off + n * L.nblk) {
+      const int64_t o = t - L.scales_off;  // block * n + row
+      const int b = int(o / n);
+      const int64_t r = o - (int64_t)b * n;
+      v = scales[r * L.nblk + b];
+    }
     packed[t] = uint8_t(v);
   }
 }
@@ -245,7 +250,7 @@ cudaError_t launch_pack_swiglu(const uint8_t* gc, const uint8_t* gs, const float
 
 cudaError_t launch_pack_rows(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k,
                              uint8_t* packed, cudaStream_t s) {
-  const int64_t work = n * RowRecord(int(k)).bytes;
+  const int64_t work = ColSlices(n, int(k)).bytes;
   pack_rows_kernel<<<grid_for(work, 256), 256, 0, s>>>(codes, scales, n, int(k), packed);
   return cudaGetLastError();
 }

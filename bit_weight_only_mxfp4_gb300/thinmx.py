@@ -182,7 +182,7 @@ def tt_moe_mxfp4_topk_mlp(x_bf16, hidden, inter, router_w_bf16, n_experts, top_k
 
 
 # Largest top_k * inter the workspace-free MoE call accepts (its fixed scratch).
-TT_MOE_STATIC_MAX_TOPK_INTER = 32768
+TT_MOE_STATIC_MAX_HIDDEN = 4096
 
 
 def tt_moe_mxfp4_topk_mlp_static(x_bf16, hidden, inter, router_w_bf16, n_experts, top_k,

@@ -162,9 +162,12 @@ tt_status tt_bf16_swiglu_matvec(const uint16_t* wg, const uint16_t* wu,
                                 int64_t m, uint16_t* h_bf16, void* stream);
 
 /* ------------------------------------------------------------------------
- * Packed single-matrix layout (MoE down projections): one record per row
- * with its codes and scales, padded to 16 bytes.  Byte-for-byte
- * rearrangement of canonical MXFP4; layout private, size public.
+ * Packed single-matrix layout (MoE down projections), sliced by columns:
+ * for each 16-wide slice of k, the 8 code bytes of every row in row order,
+ * then for each 32-block the E8M0 byte of every row; each part padded to 16
+ * bytes.  A kernel that owns one slice of the reduction index reads it as
+ * one contiguous run.  Byte-for-byte rearrangement of canonical MXFP4;
+ * layout private, size public.
  * Requires n >= 1, 32 <= k <= 16384, k % 32 == 0; packed 16-byte aligned.
  * --------------------------------------------------------------------- */
 size_t tt_mxfp4_rows_packed_bytes(int64_t n, int64_t k);
@@ -187,9 +190,20 @@ tt_status tt_mxfp4_pack_rows(const uint8_t* codes, const uint8_t* scales, int64_
  * rows, packed without postscales); down_packed holds E buffers of
  * tt_mxfp4_rows_packed_bytes(hidden, inter) bytes.  router_w_bf16 [E][hidden].
  * out_idx int32 [top_k], out_prob fp32 [top_k] (device).  workspace: device,
- * >= tt_moe_workspace_bytes(...) bytes, 16-byte aligned; the call owns it
- * until the stream reaches the end of the call.
- * Requires hidden, inter multiples of 32, hidden <= 16384, inter <= 8192,
+ * >= tt_moe_workspace_bytes(...) bytes, 16-byte aligned, ZERO-FILLED before
+ * its first use (e.g. cudaMemsetAsync once after allocating it); the call
+ * owns it until the stream reaches the end of the call and leaves it ready
+ * for the next call.  Its first 64 bytes are the kernel's grid-wide
+ * counters: after a call that reported TT_ERR_TIMEOUT through
+ * tt_device_error_read, zero the workspace again before reusing it.
+ * The layer runs as one cooperative kernel of one CTA per SM: router
+ * partial sums, expert choice in every CTA, each CTA computing a 16-wide
+ * slice range of the selected experts' h and multiplying it into the
+ * matching down columns, then a fixed-order sum of the per-CTA partial
+ * outputs (two grid-wide counters in the workspace).  A shape whose
+ * shared-memory plan does not fit one CTA per SM returns TT_ERR_UNSUPPORTED
+ * before any launch.
+ * Requires hidden, inter multiples of 32, hidden <= 8192, inter <= 8192,
  * 1 <= top_k <= min(E, 8), E <= 256.  Router logits must be finite.
  * --------------------------------------------------------------------- */
 size_t tt_moe_workspace_bytes(int64_t hidden, int64_t inter, int32_t n_experts, int32_t top_k);
@@ -210,14 +224,17 @@ tt_status tt_moe_mxfp4_topk_mlp(const uint16_t* x_bf16, int64_t hidden, int64_t 
  * can synchronise the device or fragment the pool), or bindings without a
  * CUDA allocator.  The call allocates nothing; it runs on a fixed array
  * inside the library (static device memory, held by every GPU that loads
- * the library until the process exits) sized for top_k * inter <=
- * TT_MOE_STATIC_MAX_TOPK_INTER; larger requests return TT_ERR_SIZE before
- * any launch.  The first call on each device looks the array's address up
+ * the library until the process exits, zero at load: 16,448 bytes of
+ * counters and router partials + 256 * 4 * TT_MOE_STATIC_MAX_HIDDEN bytes
+ * of partial outputs) sized for hidden <= TT_MOE_STATIC_MAX_HIDDEN; larger
+ * requests return TT_ERR_SIZE before any launch.  After a TT_ERR_TIMEOUT
+ * from this entry point its counters may be left set: the process must not
+ * reuse it.  The first call on each device looks the array's address up
  * (cudaGetSymbolAddress), so make it before any stream capture.  All calls
  * share the array: two calls that can overlap on the GPU (different
  * streams without ordering between them) race and give wrong results.
  * --------------------------------------------------------------------- */
-#define TT_MOE_STATIC_MAX_TOPK_INTER 32768
+#define TT_MOE_STATIC_MAX_HIDDEN 4096
 tt_status tt_moe_mxfp4_topk_mlp_static(const uint16_t* x_bf16, int64_t hidden, int64_t inter,
                                        const uint16_t* router_w_bf16, int32_t n_experts,
                                        int32_t top_k, const void* gate_up_packed,

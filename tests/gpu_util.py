@@ -86,7 +86,7 @@ def run_moe(x, wr, top_k, gu_packed, dn_packed, hidden, inter):
     idx = torch.empty(top_k, dtype=torch.int32, device="cuda")
     prob = torch.empty(top_k, dtype=torch.float32, device="cuda")
     wsb = thinmx.tt_moe_workspace_bytes(hidden, inter, E, top_k)
-    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
     thinmx.tt_moe_mxfp4_topk_mlp(dev(x), hidden, inter, dev(wr), E, top_k, gu_packed, dn_packed,
                                  out, idx, prob, ws, wsb)
     torch.cuda.synchronize()

@@ -38,7 +38,13 @@ def _case(E, H, I, K, wid, tie_rows=None):
 
 
 @pytest.mark.parametrize("E,H,I,K", [(6, 64, 96, 3), (8, 320, 640, 4), (32, 1024, 512, 4),
-                                     (5, 2880, 2880, 1), (16, 256, 2048, 8)])
+                                     (5, 2880, 2880, 1), (16, 256, 2048, 8),
+                                     (8, 4096, 1024, 8),
+                                     # the down columns come in two row chunks of 3584 and
+                                     # 1024 rows (shared memory too small for whole columns)
+                                     (4, 4608, 1024, 4),
+                                     # more experts than lanes: the general top-k path
+                                     (64, 256, 128, 4)])
 def test_moe_small_shapes(E, H, I, K):
     out, idx, prob, ref, ridx, rp, rlg = _case(E, H, I, K, 98)
     assert list(idx) == list(ridx)
@@ -71,3 +77,29 @@ def test_moe_full_gptoss_layer():
     assert list(idx) == list(ridx)
     np.testing.assert_allclose(prob, rp, rtol=2e-6, atol=1e-7)
     assert_float_parity(out, ref, "moe gpt-oss-20b layer")
+
+
+def test_moe_workspace_reused_across_calls_and_left_zeroed():
+    """Consecutive calls on one workspace (the grid-wide counters must come
+    back to zero after each call) give the same bits as fresh workspaces."""
+    import torch
+    from bit_weight_only_mxfp4_gb300 import thinmx
+    E, H, I, K = 8, 320, 640, 4
+    gus, dns = zip(*[synth.moe_expert_weights(41, 0, e, H, I) for e in range(E)])
+    gup, dnp, _ = gu.build_moe_experts(list(gus), list(dns), H, I)
+    wsb = thinmx.tt_moe_workspace_bytes(H, I, E, K)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    for layer in range(3):
+        r = synth.moe_router_inputs(41, layer, H, E)
+        ref_out, ref_idx, ref_prob = gu.run_moe(r["x"], r["wr"], K, gup, dnp, H, I)
+        out = torch.empty(H, dtype=torch.int16, device="cuda")
+        idx = torch.empty(K, dtype=torch.int32, device="cuda")
+        prob = torch.empty(K, dtype=torch.float32, device="cuda")
+        thinmx.tt_moe_mxfp4_topk_mlp(gu.dev(r["x"]), H, I, gu.dev(r["wr"]), E, K, gup, dnp, out,
+                                     idx, prob, ws, wsb)
+        torch.cuda.synchronize()
+        assert np.array_equal(gu.host(out, np.uint16), ref_out)
+        assert list(gu.host(idx)) == list(ref_idx)
+        assert np.array_equal(gu.host(prob), ref_prob)
+        assert not gu.host(ws[:64]).any()
+    assert gu.device_error() == 0

@@ -49,8 +49,9 @@ def test_static_scratch_moe_matches_workspace_moe_twice():
 
 def test_static_scratch_moe_rejects_oversize_before_launch():
     A = 1 << 20  # never dereferenced: the size check comes first
-    H, E = 256, 8
-    inter, top_k = 8192, 8  # valid shape, but top_k * inter beyond the fixed scratch
-    assert top_k * inter > thinmx.TT_MOE_STATIC_MAX_TOPK_INTER
-    st = thinmx.load().tt_moe_mxfp4_topk_mlp_static(A, H, inter, A, E, top_k, A, A, A, A, A, None)
+    E, top_k, inter = 8, 4, 256
+    hidden = 8192  # a valid shape, but beyond what the fixed scratch holds
+    assert hidden > thinmx.TT_MOE_STATIC_MAX_HIDDEN
+    st = thinmx.load().tt_moe_mxfp4_topk_mlp_static(A, hidden, inter, A, E, top_k, A, A, A, A, A,
+                                                    None)
     assert st == 8  # TT_ERR_SIZE
