@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, (NB <= 3 ? 2 : 1))
   if (!TT_M1_LATE_TRIGGER) pdl_allow_next_grid();
   // Weights do not depend on the previous kernel: start streaming them now.
   if (lane == 0)
-    for (int j = 0; j < min(slots, nitems); ++j) ring.issue(j, first_of(j), count_of(first_of(j)));
+    for (int j = 0; j < min(slots, nitems); ++j) ring.issue_to(j, first_of(j), count_of(first_of(j)));
   pdl_wait_prior_grid();
 
   // x is read from global memory once per CTA (not once per warp: thousands
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, (NB <= 3 ? 2 : 1))
   EpilogueBatch ep;
 
   for (int j = 0; j < nitems; ++j) {
-    const uint8_t* slot = ring.wait(j);
+    const uint8_t* slot = ring.wait_next();
     if (slot == nullptr) {
       if (lane == 0) flag_error(err, kErrTimeout);
       ring.drain(j, nitems);
@@ -207,8 +207,9 @@ __global__ void __launch_bounds__(kThreads, (NB <= 3 ? 2 : 1))
     __syncwarp();
     if (lane == 0 && j + slots < nitems) {
       const int f = first_of(j + slots);
-      ring.issue(j + slots, f, count_of(f));
+      ring.issue_to(ring.cur, f, count_of(f));  // the slot just consumed
     }
+    ring.advance();
     if constexpr (RPC == 2) {
       // lanes 0-7: g0, 8-15: u0, 16-23: g1, 24-31: u1
       const float v = warp_sum4(ag[0], au[0], ag[1], au[1], lane);
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   }
   // Weights do not depend on the previous kernel: start streaming them now.
   if (lane == 0)
-    for (int j = 0; j < min(slots, nitems); ++j) ring.issue(j, first_of(j), count_of(first_of(j)));
+    for (int j = 0; j < min(slots, nitems); ++j) ring.issue_to(j, first_of(j), count_of(first_of(j)));
   pdl_wait_prior_grid();
 
   // x: one global read per CTA, CTA-wide max |x| -> exact power-of-two
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   EpilogueBatch ep;
 
   for (int j = 0; j < nitems; ++j) {
-    const uint8_t* slot = ring.wait(j);
+    const uint8_t* slot = ring.wait_next();
     if (slot == nullptr) {
       if (lane == 0) flag_error(err, kErrTimeout);
       ring.drain(j, nitems);
@@ -362,8 +363,9 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     __syncwarp();
     if (lane == 0 && j + slots < nitems) {
       const int f = first_of(j + slots);
-      ring.issue(j + slots, f, count_of(f));
+      ring.issue_to(ring.cur, f, count_of(f));  // the slot just consumed
     }
+    ring.advance();
     if constexpr (RPC == 2) {
       // lanes 0-7: g0, 8-15: u0, 16-23: g1, 24-31: u1
       const float v = warp_sum4(ag[0], au[0], ag[1], au[1], lane);
@@ -594,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   pdl_allow_next_grid();
   if (lane == 0)
-    for (int j = 0; j < min(slots, nrec); ++j) ring.issue(j, r0 + warp + j * kWarps, 1);
+    for (int j = 0; j < min(slots, nrec); ++j) ring.issue_to(j, r0 + warp + j * kWarps, 1);
   pdl_wait_prior_grid();
 
   // Per-row max |x| -> prescale exponent; then convert x into shared memory.
@@ -633,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int nchunk = (nblk + 31) / 32;
   for (int j = 0; j < nrec; ++j) {
-    const uint8_t* rec = ring.wait(j);
+    const uint8_t* rec = ring.wait_next();
     if (rec == nullptr) {
       if (lane == 0) flag_error(err, kErrTimeout);
       ring.drain(j, nrec);
@@ -669,7 +671,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float pg = *reinterpret_cast<const float*>(rec + L.post);
     const float pu = *reinterpret_cast<const float*>(rec + L.post + 4);
     __syncwarp();
-    if (lane == 0 && j + slots < nrec) ring.issue(j + slots, r0 + warp + (j + slots) * kWarps, 1);
+    if (lane == 0 && j + slots < nrec) ring.issue_to(ring.cur, r0 + warp + (j + slots) * kWarps, 1);
+    ring.advance();
     const int r = r0 + warp + j * kWarps;
 #pragma unroll
     for (int i = 0; i < MT; ++i) {
@@ -763,7 +766,12 @@ cudaError_t launch_threads(Kern kern, int grid, int threads, int smem, cudaStrea
 
 // Shared memory of one CTA of the x-in-shared-memory kernel: at most half an
 // SM, so that the next kernel's CTA fits beside it.
-constexpr int kHalfSmBudget = 110 * 1024;
+// Shared memory of one m = 1 CTA: half an SM, so that the next kernel's CTA
+// (programmatic dependent launch) fits beside it.
+#ifndef TT_M1_SMEM_BUDGET
+#define TT_M1_SMEM_BUDGET (110 * 1024)
+#endif
+constexpr int kHalfSmBudget = TT_M1_SMEM_BUDGET;
 
 template <int NB, int RPC, int WARPS>
 cudaError_t run_m1x(const DeviceInfo& di, const uint8_t* packed, int n, int k, const uint16_t* x,

@@ -390,10 +390,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
   const int nit = nq > warp ? (nq - warp + kFWarps - 1) / kFWarps : 0;
   uint8_t* wbase = gring + (size_t)warp * P.gslots * Lg.bytes;
   uint64_t* wbars = gbars + warp * kMaxGuSlots;
-  auto issue_gu = [&](int t) {  // lane 0: item t of this warp -> slot t % gslots
-    const int q = qa + warp + t * kFWarps;
-    const int j = q / inter, r = q - j * inter;
-    const int sl = t % P.gslots;
+  // next record to request: (expert j_iss, row r_iss), advanced by kFWarps
+  // records per request without a division
+  int j_iss = (qa + warp) / inter, r_iss = (qa + warp) - j_iss * inter;
+  auto issue_gu = [&](int sl) {  // lane 0: the next record of this warp -> slot sl
+    const int j = j_iss, r = r_iss;
+    r_iss += kFWarps;
+    if (r_iss >= inter) {
+      r_iss -= inter;
+      ++j_iss;
+    }
     const uint32_t bar = smem_u32(&wbars[sl]);
     mbar_arrive_expect_tx(bar, uint32_t(Lg.bytes));
     bulk_g2s(smem_u32(wbase + (size_t)sl * Lg.bytes),
@@ -414,7 +420,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
              policy);
   };
   if (lane == 0)
-    for (int t = 0; t < min(P.gslots, nit); ++t) issue_gu(t);
+    for (int t = 0; t < min(P.gslots, nit); ++t) issue_gu(t);  // item t -> slot t
   if (threadIdx.x == 32) {
     const int n0 = min(P.dslots, nitems_d);
     for (int k = 0; k < n0; ++k) issue_dn(k);
@@ -425,13 +431,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
   float acc[kRowsPerThread];
 #pragma unroll
   for (int m = 0; m < kRowsPerThread; ++m) acc[m] = 0.f;
-  int kd = 0;  // this warp's next down item
+  // this warp's next down item kd = (chunk kd_ch, slice kd_i), in slot kd_s
+  // with mbarrier parity kd_ph, on its kd_pass-th use of that slot
+  int kd = 0, kd_ch = 0, kd_i = 0, kd_s = 0, kd_pass = 0;
+  uint32_t kd_ph = 0;
   // Down item kd for this thread's rows (t + 512 m of the item's row chunk);
   // the last of the 16 warps to finish a slot refills it.
   auto do_down = [&]() {
-    const int ch = kd / nhb, i = kd - ch * nhb;
+    const int ch = kd_ch, i = kd_i;
     const int r0 = ch * P.rc, nr = min(P.rc, hidden - r0);
-    const int s = kd % P.dslots;
+    const int s = kd_s;
     const uint8_t* slot = dring + (size_t)s * P.item;
     float hv[16];
 #pragma unroll
@@ -463,7 +472,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     __syncwarp();
     // dcons[s] only grows: the consumers of the p-th item in slot s draw
     // 16 p .. 16 p + 15, and the one that draws the last value refills it
-    if (lane == 0 && atomicAdd(&dcons[s], 1) == kFWarps * (kd / P.dslots) + kFWarps - 1) {
+    if (lane == 0 && atomicAdd(&dcons[s], 1) == kFWarps * kd_pass + kFWarps - 1) {
       const int nk = kd + P.dslots;
       if (nk < nitems_d) {
         issue_dn(nk);
@@ -471,20 +480,27 @@ __global__ void __launch_bounds__(kFThreads, 1)
       }
     }
     ++kd;
+    if (++kd_i == nhb) {
+      kd_i = 0;
+      ++kd_ch;
+    }
+    if (++kd_s == P.dslots) {
+      kd_s = 0;
+      ++kd_pass;
+      kd_ph ^= 1u;
+    }
   };
   auto down_ready = [&]() -> bool {  // warp-uniform, non-blocking
-    const int i = kd % nhb;
-    bool ok = mbar_test_wait(smem_u32(&hbars[i]), 0u) &&
-              mbar_test_wait(smem_u32(&dbars[kd % P.dslots]), uint32_t((kd / P.dslots) & 1));
+    bool ok = mbar_test_wait(smem_u32(&hbars[kd_i]), 0u) &&
+              mbar_test_wait(smem_u32(&dbars[kd_s]), kd_ph);
     return __all_sync(0xffffffffu, ok);
   };
 
   bool failed = false;
-  int t = 0;
+  int t = 0, sl = 0;  // record t of this warp sits in ring slot sl with parity gph
+  uint32_t gph = 0;
   for (; t < nit; ++t) {
-    const int sl = t % P.gslots;
-    const bool ok =
-        mbar_wait_sleep_bounded(smem_u32(&wbars[sl]), uint32_t((t / P.gslots) & 1), 256u);
+    const bool ok = mbar_wait_sleep_bounded(smem_u32(&wbars[sl]), gph, 256u);
     if (!__all_sync(0xffffffffu, ok)) {
       failed = true;
       break;
@@ -513,7 +529,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const float pg = *reinterpret_cast<const float*>(rec + Lg.post);
     const float pu = *reinterpret_cast<const float*>(rec + Lg.post + 4);
     __syncwarp();
-    if (lane == 0 && t + P.gslots < nit) issue_gu(t + P.gslots);
+    if (lane == 0 && t + P.gslots < nit) issue_gu(sl);  // record t + gslots into this slot
+    if (++sl == P.gslots) {
+      sl = 0;
+      gph ^= 1u;
+    }
     const float v = warp_sum2(ag, au, lane);  // lanes 0-15: g, 16-31: u
     const float g = __shfl_sync(0xffffffffu, v, 0) * inv * pg;
     const float u = __shfl_sync(0xffffffffu, v, 16) * inv * pu;
@@ -534,10 +554,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
   } else {
     // the remaining slices, waiting for them (bounded)
     while (kd < nitems_d) {
-      const int i = kd % nhb;
-      bool ok = mbar_wait_sleep_bounded(smem_u32(&hbars[i]), 0u, 256u);
-      ok = ok && mbar_wait_sleep_bounded(smem_u32(&dbars[kd % P.dslots]),
-                                         uint32_t((kd / P.dslots) & 1), 256u);
+      bool ok = mbar_wait_sleep_bounded(smem_u32(&hbars[kd_i]), 0u, 256u);
+      ok = ok && mbar_wait_sleep_bounded(smem_u32(&dbars[kd_s]), kd_ph, 256u);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) *sfail = 1;
         break;

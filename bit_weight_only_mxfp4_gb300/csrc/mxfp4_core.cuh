@@ -48,7 +48,9 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float v) {
 
 // Per-warp ring of bulk-copy slots.  Item j of the warp is a "unit" of up to
 // `rpc` consecutive records starting at record first(j); one bulk copy
-// brings the whole unit into slot j % slots.
+// brings the whole unit into slot j % slots.  Items are consumed in order:
+// the ring tracks the slot and mbarrier parity of the next one (no integer
+// division on the per-record path).
 struct WarpRing {
   uint8_t* base;
   uint64_t* bars;
@@ -57,6 +59,8 @@ struct WarpRing {
   int rec_bytes;
   const uint8_t* packed;
   uint64_t policy;
+  int cur = 0;           // slot of the next item to consume
+  uint32_t phase = 0;    // mbarrier parity of that item
 
   __device__ void init(int lane) {
     if (lane == 0) {
@@ -65,23 +69,26 @@ struct WarpRing {
     }
     __syncwarp();
   }
-  // lane 0 only: copy `count` records starting at record `first` into the
-  // slot of item j.
-  __device__ void issue(int j, int first, int count) {
-    const int s = j % slots;
+  // lane 0 only: copy `count` records starting at record `first` into slot s.
+  __device__ void issue_to(int s, int first, int count) {
     const uint32_t bar = smem_u32(&bars[s]);
     const uint32_t bytes = uint32_t(count * rec_bytes);
     mbar_arrive_expect_tx(bar, bytes);
     bulk_g2s(smem_u32(base + (size_t)s * slot_bytes), packed + (int64_t)first * rec_bytes, bytes,
              bar, policy);
   }
-  // Returns the slot of item j once its copy has landed, nullptr after a
-  // timeout (warp-uniform).
-  __device__ const uint8_t* wait(int j) {
-    const int s = j % slots;
-    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), uint32_t((j / slots) & 1));
+  // The next item's slot once its copy has landed, nullptr after a timeout
+  // (warp-uniform).  Refill that slot with issue_to(cur, ...), then advance().
+  __device__ const uint8_t* wait_next() {
+    const bool ok = mbar_wait_bounded(smem_u32(&bars[cur]), phase);
     if (!__all_sync(0xffffffffu, ok)) return nullptr;
-    return base + (size_t)s * slot_bytes;
+    return base + (size_t)cur * slot_bytes;
+  }
+  __device__ void advance() {
+    if (++cur == slots) {
+      cur = 0;
+      phase ^= 1u;
+    }
   }
   // After a timeout at item j: give the copies already issued a bounded
   // chance to land before the CTA may exit.
