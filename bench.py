@@ -293,7 +293,8 @@ def main():
             ms = tuple(int(v) for v in args.ms.split(",")) if args.ms else None
             r = secondary_sweep(torch, synth, loader, thinmx, device, hbm, ms=ms)
         elif args.only == "int4":
-            r = int4_workload(torch, synth, thinmx, device, hbm, 0, reps=args.steps)
+            l2 = torch.cuda.get_device_properties(device).L2_cache_size
+            r = int4_workload(torch, synth, thinmx, device, hbm, l2, reps=args.steps)
         else:
             r = moe_workload(torch, synth, loader, thinmx, device, hbm, reps=args.steps,
                              layers=args.layers)
