@@ -79,3 +79,38 @@ def test_validation_before_launch(lib):
     assert _st("tt_mxfp4_pack_swiglu", A, A, None, A, A, None, 16, 64, A, 100, s) == 8
     # empty quantise is a no-op
     assert _st("tt_quantize_mxfp4", None, 0, 64, None, None, None, s) == 0
+
+
+def test_moe_validation_before_launch(lib):
+    A = 1 << 20  # never dereferenced: every case fails validation first
+    s = None
+    ws = _st("tt_moe_workspace_bytes", 2880, 2880, 32, 4)
+    assert ws >= 64 + 256 * 2880 * 4  # counters + one partial vector per CTA
+    assert _st("tt_moe_workspace_bytes", 8224, 2880, 32, 4) == 0  # hidden beyond 8192
+    assert _st("tt_moe_workspace_bytes", 2880, 2880, 4, 8) == 0   # top_k > n_experts
+    call = lambda H, I, E, K, x=A, wsp=A, wsb=ws: _st(
+        "tt_moe_mxfp4_topk_mlp", x, H, I, A, E, K, A, A, A, A, A, wsp, wsb, s)
+    assert call(2880, 2880, 32, 4, wsb=ws - 1) == 8          # workspace too small
+    assert call(8224, 2880, 32, 4, wsb=1 << 30) == 2          # hidden beyond 8192
+    assert call(2880, 8224, 32, 4, wsb=1 << 30) == 2          # inter beyond 8192
+    assert call(2880, 2880, 32, 9) == 2                       # top_k beyond 8
+    assert call(2880, 2880, 257, 4) == 2                      # more than 256 experts
+    assert call(2880, 2880, 32, 0) == 2
+    assert call(2880, 2880, 32, 4, x=None) == 1
+    assert call(2880, 2880, 32, 4, wsp=None) == 1
+    assert call(2880, 2880, 32, 4, x=A + 8) == 3              # x not 16-byte aligned
+    assert call(2880, 2880, 32, 4, wsp=A + 4) == 3            # workspace not 16-byte aligned
+
+
+def test_int4_validation_before_launch(lib):
+    A = 1 << 20
+    s = None
+    call = lambda n, k, g, m, codes=A, x=A: _st("tt_int4_grouped_matvec", codes, A, A, n, k, g,
+                                                 x, m, A, s)
+    assert call(5120, 2880, 128, 9) == 2      # m beyond 8
+    assert call(5120, 2880, 100, 1) == 2      # group not a multiple of 32
+    assert call(5120, 2890, 128, 1) == 2      # k not a multiple of 32
+    assert call(5120, 16384, 128, 1) == 2     # k beyond 8192
+    assert call(0, 2880, 128, 1) == 2
+    assert call(5120, 2880, 128, 1, codes=None) == 1
+    assert call(5120, 2880, 128, 1, x=A + 2) == 3
