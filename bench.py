@@ -346,10 +346,25 @@ def main():
     x_dev = torch.empty((L, cfg.k), dtype=torch.bfloat16, device=device)
     h_dev = torch.empty((L, cfg.n), dtype=torch.bfloat16, device=device)
 
+    # each layer's call with its device addresses, resolved once (the binding
+    # takes raw addresses as well as tensors)
+    xs_ptr = [x_dev[i:i + 1].data_ptr() for i in range(L)]
+    hs_ptr = [h_dev[i:i + 1].data_ptr() for i in range(L)]
+    stream = torch.cuda.current_stream().cuda_stream
+    calls = []
+    for i, (kind, w, _, _) in enumerate(layers):
+        if kind == "mxfp4":
+            calls.append((thinmx.tt_mxfp4_swiglu_matvec,
+                          (w.data_ptr(), cfg.n, cfg.k, xs_ptr[i], 1, hs_ptr[i], stream)))
+        else:
+            calls.append((thinmx.tt_bf16_swiglu_matvec,
+                          (w[0].data_ptr(), w[1].data_ptr(), cfg.n, cfg.k, xs_ptr[i], 1,
+                           hs_ptr[i], stream)))
+
     def e2e_step():
         x_dev.copy_(x_host, non_blocking=True)
-        for i, lay in enumerate(layers):
-            run_layer(thinmx, cfg, lay, x_dev[i:i + 1], h_dev[i:i + 1])
+        for fn, a in calls:
+            fn(*a)
         h_host.copy_(h_dev, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 

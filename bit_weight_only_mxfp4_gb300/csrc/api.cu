@@ -1,6 +1,7 @@
 // The C ABI (include/thinmx.h): host-side validation, then one launch on
 // the caller's stream.  Nothing here allocates device memory or
 // synchronises, except the diagnostic tt_device_error_read.
+#include <map>
 #include <mutex>
 
 #include "thinmx.h"
@@ -26,6 +27,7 @@ const DeviceInfo* device_info() {
   std::lock_guard<std::mutex> lock(g_info_mu);
   if (!g_info_ok[dev]) {
     DeviceInfo d;
+    d.device = dev;
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return nullptr;
     if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
@@ -38,6 +40,18 @@ const DeviceInfo* device_info() {
     g_info_ok[dev] = true;
   }
   return &g_info[dev];
+}
+
+cudaError_t ensure_dynamic_smem(const void* kern, int device, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> granted;
+  std::lock_guard<std::mutex> lock(mu);
+  int& g = granted[{kern, device}];
+  if (g >= bytes) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) g = bytes;
+  return e;
 }
 
 }  // namespace tt

@@ -196,7 +196,7 @@ cudaError_t run(const DeviceInfo& di, const uint8_t* codes, const uint16_t* scal
   const int smem = MT * 4 * (k >> 5) * 16 + MT * kWarps * 4 + MT * 4;
   if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
   auto kern = int4_matvec_kernel<CPL, MT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem(di, kern, smem);
   if (e != cudaSuccess) return e;
   int grid = 2 * di.sms;
   const int need = (n + kWarps * kRowsPerIter - 1) / (kWarps * kRowsPerIter);

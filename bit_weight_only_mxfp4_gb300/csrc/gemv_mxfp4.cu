@@ -739,7 +739,7 @@ cudaError_t run_m1(const DeviceInfo& di, const uint8_t* packed, int n, int k, co
   const int smem = kWarps * slots * (slot_bytes + 8) + 2 * k;  // ring, barriers, x
   if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
   auto kern = swiglu_mxfp4_m1_kernel<NB, RPC>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem(di, kern, smem);
   if (e != cudaSuccess) return e;
   int grid = ctas_per_sm * di.sms;
   const int units = (n + RPC - 1) / RPC;
@@ -785,7 +785,7 @@ cudaError_t run_m1x(const DeviceInfo& di, const uint8_t* packed, int n, int k, c
   const int smem = WARPS * slots * (slot_bytes + 8) + fixed;
   if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
   auto kern = swiglu_mxfp4_m1x_kernel<NB, RPC, WARPS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem(di, kern, smem);
   if (e != cudaSuccess) return e;
   int grid = TT_M1X_CTAS_PER_SM * di.sms;
   const int units = (n + RPC - 1) / RPC;
@@ -812,7 +812,7 @@ cudaError_t run_m1s(const DeviceInfo& di, const uint8_t* packed, int n, int k, c
   const int smem = slots * per_slot;
   if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
   auto kern = swiglu_mxfp4_m1s_kernel<NB, R>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem(di, kern, smem);
   if (e != cudaSuccess) return e;
   int grid = di.sms;
   const int units = (n + R - 1) / R;
@@ -834,7 +834,7 @@ cudaError_t run_mt(const DeviceInfo& di, const uint8_t* packed, int n, int k, in
   if (slots > 6) slots = 6;
   const int smem = kWarps * slots * (L.bytes + 8) + xs_bytes;
   auto kern = swiglu_mxfp4_mt_kernel<MT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem(di, kern, smem);
   if (e != cudaSuccess) return e;
   const int grid = n < di.sms ? n : di.sms;
   return launch_pdl_m(kern, grid, smem, s, pdl, packed, n, k, m, x, h, slots, di.error_word);

@@ -9,12 +9,23 @@
 namespace tt {
 
 struct DeviceInfo {
+  int device = 0;
   int sms = 0;
   int smem_optin = 0;
   int32_t* error_word = nullptr;  // the library's device error word
 };
 // Cached per device; returns nullptr if the device cannot be queried.
 const DeviceInfo* device_info();
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) only when a kernel needs
+// more dynamic shared memory on this device than was already granted: the
+// attribute call costs about a microsecond of host time, too much on the
+// per-call path of kernels that take a few microseconds.
+cudaError_t ensure_dynamic_smem(const void* kern, int device, int bytes);
+template <typename Kern>
+cudaError_t ensure_smem(const DeviceInfo& di, Kern kern, int bytes) {
+  return ensure_dynamic_smem(reinterpret_cast<const void*>(kern), di.device, bytes);
+}
 
 // quantize.cu
 cudaError_t launch_quantize_mxfp4(const float* w, int64_t n, int64_t k, uint8_t* codes,

@@ -652,7 +652,7 @@ cudaError_t launch_moe_fused(const uint16_t* x, int hidden, int inter, const uin
 
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t r =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.total);
+        ensure_smem(*di, kern, plan.total);
     if (r != cudaSuccess) return r;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -46,7 +46,10 @@ constexpr int kTmaWarp = kProdWarps + 1;         // TMA loads
 constexpr int kThreads = (kProdWarps + 2) * 32;  // 576
 constexpr int kTileRows = 128;
 constexpr int kTileK = 64;                      // f16: 128 bytes = one swizzle row
-constexpr int kStages = 3;
+#ifndef TT_TC_STAGES
+#define TT_TC_STAGES 2
+#endif
+constexpr int kStages = TT_TC_STAGES;  // decoded A/B stages
 constexpr int kErrUnsupported = 5;              // TT_ERR_UNSUPPORTED
 
 // ---- tcgen05 / descriptor helpers ------------------------------------------
@@ -152,24 +155,25 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 
 // Shared-memory plan of one CTA (offsets from a 1024-aligned base).
 struct TcPlan {
-  static constexpr int kRaw = 4;  // k-tiles in flight (raw slots)
+  static constexpr int kMaxRaw = 8;  // raw slots: k-tiles of packed weights in flight
+  int nraw;
   int np;          // MMA N (batch rows padded to 16)
   int nblk;        // k / 32
   int a_bytes;     // one A tile: 128 x 128 B
   int stage_bytes; // A_g + A_u + B, 1024-aligned
   int raw_bytes;   // one raw slot: gate 4 KB + up 4 KB + x np x 128 B
   int off_raw, off_scale, off_xr, off_bar, off_tmem, total;
-  __host__ __device__ TcPlan(int m, int k) {
+  __host__ __device__ TcPlan(int m, int k, int nraw_) : nraw(nraw_) {
     np = (m + 15) & ~15;
     nblk = k >> 5;
     a_bytes = kTileRows * 128;
     stage_bytes = (2 * a_bytes + np * 128 + 1023) & ~1023;
     raw_bytes = (2 * kTileRows * 32 + np * 128 + 127) & ~127;
     off_raw = kStages * stage_bytes;
-    off_scale = off_raw + kRaw * raw_bytes;
+    off_scale = off_raw + nraw * raw_bytes;
     off_xr = off_scale + 2 * kTileRows * nblk;
     off_bar = (off_xr + 2 * kTileRows * 4 + 7) & ~7;
-    off_tmem = off_bar + (2 * kStages + 2 * kRaw + 1) * 8;
+    off_tmem = off_bar + (2 * kStages + 2 * kMaxRaw + 1) * 8;
     total = off_tmem + 16 + 1024;  // + alignment slack of the dynamic base
   }
 };
@@ -177,10 +181,10 @@ struct TcPlan {
 __global__ void __launch_bounds__(kThreads, 1)
     tc_swiglu_kernel(const __grid_constant__ CUtensorMap map_w,
                      const __grid_constant__ CUtensorMap map_x, const uint8_t* __restrict__ packed,
-                     int n, int k, int m, uint16_t* __restrict__ h, int32_t* err) {
+                     int n, int k, int m, int nraw, uint16_t* __restrict__ h, int32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   const SwigluRecord L(k);
-  const TcPlan P(m, k);
+  const TcPlan P(m, k, nraw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (sbase - smem_u32(smem_raw));
@@ -189,8 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* a_full = reinterpret_cast<uint64_t*>(base + P.off_bar);
   uint64_t* a_empty = a_full + kStages;
   uint64_t* raw_full = a_empty + kStages;
-  uint64_t* raw_empty = raw_full + TcPlan::kRaw;
-  uint64_t* done = raw_empty + TcPlan::kRaw;
+  uint64_t* raw_empty = raw_full + TcPlan::kMaxRaw;
+  uint64_t* done = raw_empty + TcPlan::kMaxRaw;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + P.off_tmem);
   const int n0 = blockIdx.x * kTileRows;
   const int nkt = k / kTileK;
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&a_full[s]), kGroupWarps * 32);
       mbar_init(smem_u32(&a_empty[s]), 1);
     }
-    for (int d = 0; d < TcPlan::kRaw; ++d) {
+    for (int d = 0; d < P.nraw; ++d) {
       mbar_init(smem_u32(&raw_full[d]), 1);
       mbar_init(smem_u32(&raw_empty[d]), kGroupWarps * 32);
     }
@@ -237,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kTmaWarp) {
     // ---------------- TMA loads ----------------
     if (lane == 0) {
-      const int pre = min(TcPlan::kRaw, nkt);
+      const int pre = min(P.nraw, nkt);
       // weights do not depend on the previous kernel: start them before waiting
       for (int kt = 0; kt < pre; ++kt) {
         const uint32_t dst = raw_slot(kt), bar = smem_u32(&raw_full[kt]);
@@ -250,8 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(raw_slot(kt) + 8192, &map_x, kt * kTileK, 0, smem_u32(&raw_full[kt]));
       bool ok = true;
       for (int kt = pre; kt < nkt; ++kt) {
-        const int d = kt % TcPlan::kRaw;
-        ok = mbar_wait_bounded(smem_u32(&raw_empty[d]), uint32_t(((kt / TcPlan::kRaw) - 1) & 1));
+        const int d = kt % P.nraw;
+        ok = mbar_wait_bounded(smem_u32(&raw_empty[d]), uint32_t(((kt / P.nraw) - 1) & 1));
         if (!ok) break;
         const uint32_t dst = raw_slot(d), bar = smem_u32(&raw_full[d]);
         mbar_arrive_expect_tx(bar, raw_tx);
@@ -300,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int xg = sxr[r], xu = sxr[kTileRows + r];
     bool ok = true;
     for (int kt = g; kt < nkt; kt += kGroups) {
-      const int s = kt % kStages, d = kt % TcPlan::kRaw;
-      ok = mbar_wait_bounded(smem_u32(&raw_full[d]), uint32_t((kt / TcPlan::kRaw) & 1));
+      const int s = kt % kStages, d = kt % P.nraw;
+      ok = mbar_wait_bounded(smem_u32(&raw_full[d]), uint32_t((kt / P.nraw) & 1));
       if (ok && kt >= kStages)
         ok = mbar_wait_bounded(smem_u32(&a_empty[s]), uint32_t(((kt / kStages) - 1) & 1));
       if (!ok) break;
@@ -414,15 +418,23 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-int tc_swiglu_smem_bytes(int m, int k) { return TcPlan(m, k).total; }
+// Deepest raw ring (most k-tiles of packed weights in flight) that fits.
+static int pick_nraw(int m, int k, int limit) {
+  for (int r = TcPlan::kMaxRaw; r >= 2; --r)
+    if (TcPlan(m, k, r).total <= limit) return r;
+  return 0;
+}
+
+int tc_swiglu_smem_bytes(int m, int k) { return TcPlan(m, k, 2).total; }
 
 cudaError_t launch_swiglu_mxfp4_tc(const uint8_t* packed, int n, int k, const uint16_t* x, int m,
                                    uint16_t* h, cudaStream_t s, bool pdl) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorNoDevice;
   if (k % kTileK != 0 || m < 1 || m > 64) return cudaErrorInvalidConfiguration;
-  const TcPlan P(m, k);
-  if (P.total > di->smem_optin) return cudaErrorInvalidConfiguration;
+  const int nraw = pick_nraw(m, k, di->smem_optin);
+  if (nraw == 0) return cudaErrorInvalidConfiguration;
+  const TcPlan P(m, k, nraw);
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const SwigluRecord L(k);
@@ -447,8 +459,7 @@ cudaError_t launch_swiglu_mxfp4_tc(const uint8_t* packed, int n, int k, const ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(tc_swiglu_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, P.total);
+  cudaError_t e = ensure_smem(*di, tc_swiglu_kernel, P.total);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((n + kTileRows - 1) / kTileRows);
@@ -460,7 +471,7 @@ cudaError_t launch_swiglu_mxfp4_tc(const uint8_t* packed, int n, int k, const ui
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, tc_swiglu_kernel, map_w, map_x, packed, n, k, m, h,
+  return cudaLaunchKernelEx(&cfg, tc_swiglu_kernel, map_w, map_x, packed, n, k, m, nraw, h,
                             di->error_word);
 }
 

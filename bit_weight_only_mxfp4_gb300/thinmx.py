@@ -62,6 +62,9 @@ class ThinmxError(RuntimeError):
 def load(path: str = LIB_PATH):
     """Load the CUDA library (raises if it has not been built)."""
     global _lib
+    lib = _lib
+    if lib is not None:  # fast path of every call after the first
+        return lib
     with _lock:
         if _lib is None:
             if not os.path.exists(path):
@@ -84,10 +87,24 @@ def _ptr(t):
     return t.data_ptr()
 
 
+_torch = None
+
+
+def _current_stream() -> int:
+    """Raw handle of torch's current CUDA stream on the current device."""
+    global _torch
+    if _torch is None:
+        import torch
+        _torch = torch
+    raw = getattr(_torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(_torch._C._cuda_getDevice())
+    return _torch.cuda.current_stream().cuda_stream
+
+
 def _stream(stream):
     if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        return _current_stream()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
