@@ -44,7 +44,10 @@ def _case(E, H, I, K, wid, tie_rows=None):
                                      # 1024 rows (shared memory too small for whole columns)
                                      (4, 4608, 1024, 4),
                                      # more experts than lanes: the general top-k path
-                                     (64, 256, 128, 4)])
+                                     (64, 256, 128, 4),
+                                     # the largest hidden (one gate/up slot per warp, two row
+                                     # chunks), every expert selected, a single expert
+                                     (2, 8192, 256, 2), (4, 1024, 512, 4), (1, 320, 640, 1)])
 def test_moe_small_shapes(E, H, I, K):
     out, idx, prob, ref, ridx, rp, rlg = _case(E, H, I, K, 98)
     assert list(idx) == list(ridx)
