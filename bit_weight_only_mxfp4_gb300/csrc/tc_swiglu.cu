@@ -39,11 +39,14 @@ namespace tt {
 namespace {
 
 constexpr int kGroupWarps = 8;                  // one producer group: 256 threads
-constexpr int kGroups = 2;                       // groups decode alternate k-tiles
+#ifndef TT_TC_GROUPS
+#define TT_TC_GROUPS 2
+#endif
+constexpr int kGroups = TT_TC_GROUPS;            // groups decode k-tiles in turn
 constexpr int kProdWarps = kGroupWarps * kGroups;
 constexpr int kMmaWarp = kProdWarps;             // tensor memory + MMA issue
 constexpr int kTmaWarp = kProdWarps + 1;         // TMA loads
-constexpr int kThreads = (kProdWarps + 2) * 32;  // 576
+constexpr int kThreads = (kProdWarps + 2) * 32;  // 576 with two groups
 constexpr int kTileRows = 128;
 constexpr int kTileK = 64;                      // f16: 128 bytes = one swizzle row
 #ifndef TT_TC_STAGES
