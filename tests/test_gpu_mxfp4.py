@@ -207,3 +207,20 @@ def test_tensor_path_rejects_k_not_multiple_of_64():
     with pytest.raises(thinmx.ThinmxError) as e:
         thinmx.tt_mxfp4_swiglu_matvec(packed, n, k, x, 16, h)
     assert e.value.status == 5  # TT_ERR_UNSUPPORTED, nothing launched
+
+
+def test_tensor_path_flags_activations_beyond_f16_range():
+    """The tensor path converts x to f16 for the MMA: an activation beyond
+    f16's range is reported through the device error word (no fault), and
+    the next call is unaffected."""
+    n, k, m = 128, 256, 16
+    h, ref, packed, d = _swiglu_case(n, k, m, True)
+    assert_float_parity(h, ref, "before")
+    assert gu.device_error() == 0
+    x = d["x"].copy()
+    x[3, 17] = synth.f32_to_bf16_bits(np.array([1.0e5], np.float32))[0]
+    gu.swiglu(packed, n, k, x)
+    assert gu.device_error() == 5   # TT_ERR_UNSUPPORTED; reading clears the word
+    assert gu.device_error() == 0
+    h2 = gu.swiglu(packed, n, k, d["x"])
+    assert np.array_equal(h2, h)
