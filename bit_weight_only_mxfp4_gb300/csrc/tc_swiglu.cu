@@ -49,8 +49,13 @@ constexpr int kTmaWarp = kProdWarps + 1;         // TMA loads
 constexpr int kThreads = (kProdWarps + 2) * 32;  // 576 with two groups
 constexpr int kTileRows = 128;
 constexpr int kTileK = 64;                      // f16: 128 bytes = one swizzle row
+// Decoded A/B stages and the most raw k-tiles in flight: 3 and 4 measured
+// best at m = 16..64 (2 stages, 8 raw slots or 3 producer groups were slower).
 #ifndef TT_TC_STAGES
-#define TT_TC_STAGES 2
+#define TT_TC_STAGES 3
+#endif
+#ifndef TT_TC_MAX_RAW
+#define TT_TC_MAX_RAW 4
 #endif
 constexpr int kStages = TT_TC_STAGES;  // decoded A/B stages
 constexpr int kErrUnsupported = 5;              // TT_ERR_UNSUPPORTED
@@ -158,7 +163,7 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 
 // Shared-memory plan of one CTA (offsets from a 1024-aligned base).
 struct TcPlan {
-  static constexpr int kMaxRaw = 8;  // raw slots: k-tiles of packed weights in flight
+  static constexpr int kMaxRaw = TT_TC_MAX_RAW;  // raw slots: packed k-tiles in flight
   int nraw;
   int np;          // MMA N (batch rows padded to 16)
   int nblk;        // k / 32
