@@ -97,33 +97,33 @@ __device__ __forceinline__ void warp_topk_softmax(const float* __restrict__ logi
 
 
 // The same for E <= 32 with one logit per lane (v: this lane's logit; lanes
-// >= E are ignored): top_k rounds of a warp arg-max, no per-lane arrays.
+// >= E are ignored).  Each lane counts the logits that beat its own (larger,
+// or equal with a lower index) over 31 independent shuffles, which gives its
+// rank in the total order; the ranks below top_k are the selection.  The
+// softmax terms are summed in rank order, as in the general version.
 __device__ __forceinline__ void warp_topk_softmax32(float v, int E, int top_k, int lane, int* idx,
                                                     float* prob) {
-  bool avail = lane < E;
-  float selv = 0.f;  // lane j keeps the j-th selected logit
-  for (int j = 0; j < top_k; ++j) {
-    float bv = v;
-    int be = avail ? lane : 0x7FFFFFFF;
+  const bool valid = lane < E;
+  const float mv = valid ? v : -INFINITY;
+  int rank = 0;
+  float vmax = mv;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      const bool take = oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be));
-      if (take) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if (lane == be) avail = false;
-    if (lane == j) selv = bv;
-    if (lane == 0) idx[j] = be;
+  for (int d = 1; d < 32; ++d) {
+    const int o = (lane + d) & 31;
+    const float ov = __shfl_sync(0xffffffffu, mv, o);
+    const bool ovalid = o < E;
+    rank += (ovalid && (ov > mv || (ov == mv && o < lane))) ? 1 : 0;
+    vmax = fmaxf(vmax, ovalid ? ov : -INFINITY);
   }
-  const float sel0 = __shfl_sync(0xffffffffu, selv, 0);  // the largest
-  const float ex = lane < top_k ? expf(selv - sel0) : 0.f;
+  const bool sel = valid && rank < top_k;
+  if (sel) idx[rank] = lane;
+  const float ex = sel ? expf(mv - vmax) : 0.f;  // vmax: the rank-0 logit
   float den = 0.f;
-  for (int j = 0; j < top_k; ++j) den += __shfl_sync(0xffffffffu, ex, j);
-  if (lane < top_k) prob[lane] = ex / den;
+  for (int j = 0; j < top_k; ++j) {
+    const unsigned m = __ballot_sync(0xffffffffu, sel && rank == j);
+    den += __shfl_sync(0xffffffffu, ex, __ffs(m) - 1);
+  }
+  if (sel) prob[rank] = ex / den;
 }
 
 }  // namespace tt

@@ -303,8 +303,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
       red_c[warp] = cc;
     }
     __syncthreads();
+    // warps past the task's chunks hold (0, 0), which a merge leaves as is
+    const int wused = min(kFWarps, (c1 - c0 + 31) >> 5);
     float ts = red_s[0], tc = red_c[0];
-    for (int w = 1; w < kFWarps; ++w) comp_merge(ts, tc, red_s[w], red_c[w]);
+    for (int w = 1; w < wused; ++w) comp_merge(ts, tc, red_s[w], red_c[w]);
     // one copy per CTA, so that no L2 line is read by every SM below
     for (int r = threadIdx.x; r < G; r += kFThreads) part[(size_t)r * T + t] = make_float2(ts, tc);
     __syncthreads();
