@@ -38,6 +38,8 @@
 //
 // Every wait (counters, mbarriers) is bounded in time; a timeout sets the
 // library's error word and the CTA leaves after its own copies have landed.
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
 #include "layout.cuh"
@@ -629,7 +631,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   }
 }
 
-int g_coop_pdl_state = 0;  // 0 unknown, 1 cooperative + PDL accepted, 2 refused
+std::atomic<int> g_coop_pdl_state{0};  // 0 unknown, 1 cooperative + PDL accepted, 2 refused
 
 }  // namespace
 
