@@ -38,7 +38,10 @@
 namespace tt {
 namespace {
 
-constexpr int kGroupWarps = 8;                  // one producer group: 256 threads
+#ifndef TT_TC_GROUP_WARPS
+#define TT_TC_GROUP_WARPS 8
+#endif
+constexpr int kGroupWarps = TT_TC_GROUP_WARPS;  // one producer group: 8 warps = 256 threads
 #ifndef TT_TC_GROUPS
 #define TT_TC_GROUPS 2
 #endif
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), tcols);
   // Per-row block scales into shared memory and each row's largest block
   // exponent: gate rows by threads 0-127, up rows by 128-255.
-  if (warp < kGroupWarps) {
+  if (threadIdx.x < 2 * kTileRows) {
     const int t = threadIdx.x, r = t & 127, which = t >> 7;
     const bool valid = n0 + r < n;
     const uint8_t* src =
@@ -306,9 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- producers: decode W, convert x ----------------
     // group g decodes k-tiles g, g + kGroups, ...; thread t of the group owns
-    // half a k-tile (one 32-weight block) of row t % 128
+    // part t / 128 of the k-tile (kPartK weights) of row t % 128
+    constexpr int kParts = kGroupWarps * 32 / kTileRows;  // 2 (8 warps) or 4 (16 warps)
+    constexpr int kPartK = kTileK / kParts;              // weights per part: 32 or 16
+    constexpr int kPartWords = kPartK / 8;                // 32-bit code words per part
     const int g = warp / kGroupWarps;
-    const int t = threadIdx.x - g * kGroupWarps * 32, r = t & 127, half = t >> 7;
+    const int t = threadIdx.x - g * kGroupWarps * 32, r = t & 127, part = t >> 7;
     const int xg = sxr[r], xu = sxr[kTileRows + r];
     bool ok = true;
     for (int kt = g; kt < nkt; kt += kGroups) {
@@ -319,19 +325,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const uint8_t* rw = base + P.off_raw + d * P.raw_bytes;
       uint8_t* stage = base + s * P.stage_bytes;
-      // W: one 32-weight block per matrix -> 4 swizzled 16-byte chunks each
+      // W: kPartK weights per matrix -> kPartWords swizzled 16-byte chunks each
 #pragma unroll
       for (int mat = 0; mat < 2; ++mat) {
-        const uint4 c = *reinterpret_cast<const uint4*>(rw + mat * 4096 + r * 32 + half * 16);
-        const uint32_t sb = sscale[(mat * kTileRows + r) * P.nblk + kt * 2 + half];
+        const uint8_t* src = rw + mat * 4096 + r * 32 + part * (kPartK / 2);
+        uint32_t w[kPartWords];
+        if constexpr (kPartWords == 4) {
+          const uint4 c = *reinterpret_cast<const uint4*>(src);
+          w[0] = c.x;
+          w[1] = c.y;
+          w[2] = c.z;
+          w[3] = c.w;
+        } else {
+          const uint2 c = *reinterpret_cast<const uint2*>(src);
+          w[0] = c.x;
+          w[1] = c.y;
+        }
+        const uint32_t sb = sscale[(mat * kTileRows + r) * P.nblk + kt * 2 + (part * kPartK) / 32];
         const uint32_t f = sb == 255u ? 0x7E007E00u : pow2_f16x2(int(sb) - 127 - (mat ? xu : xg));
-        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
         uint8_t* a = stage + mat * P.a_bytes;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < kPartWords; ++q) {
           uint32_t h0, h1, h2, h3;
           e2m1x8_to_f16x2(w[q], h0, h1, h2, h3);
-          *reinterpret_cast<uint4*>(a + sw128(r, half * 4 + q)) =
+          *reinterpret_cast<uint4*>(a + sw128(r, part * kPartWords + q)) =
               make_uint4(hmul2(h0, f), hmul2(h1, f), hmul2(h2, f), hmul2(h3, f));
         }
       }
