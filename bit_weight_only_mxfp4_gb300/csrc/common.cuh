@@ -103,39 +103,21 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete; false if it did not
-// within kWaitLimitNs.
-// Suspend-time hint of the bounded wait (0: plain try_wait polling).
+// Suspend-time hint of the bounded wait (0: plain try_wait).  try_wait
+// already suspends the thread until the phase completes or a hardware time
+// limit passes (measured: polls that come back unsatisfied are rare), so
+// neither a hint, a back-off between polls nor a non-blocking poll loop
+// changed the time or the instruction count.
 #ifndef TT_WAIT_HINT_NS
 #define TT_WAIT_HINT_NS 0
 #endif
 
-// Back-off between polls of a bounded wait (0: none): a polling warp sleeps
-// instead of taking issue slots from the warps that have data to work on.
-#ifndef TT_WAIT_BACKOFF_NS
-#define TT_WAIT_BACKOFF_NS 0
-#endif
-
-// Poll period of the bounded wait when polling with the non-blocking test
-// (0: the blocking try_wait form).
-#ifndef TT_WAIT_POLL_NS
-#define TT_WAIT_POLL_NS 0
-#endif
-
+// Waits for the phase with the given parity to complete; false if it did not
+// within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  if (TT_WAIT_POLL_NS > 0) {
-    if (mbar_test_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-      __nanosleep(TT_WAIT_POLL_NS);
-      if (mbar_test_wait(bar, parity)) return true;
-      if ((it & 15u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    }
-  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (TT_WAIT_BACKOFF_NS > 0) __nanosleep(TT_WAIT_BACKOFF_NS);
     if (TT_WAIT_HINT_NS > 0 ? mbar_try_wait_sleep(bar, parity, TT_WAIT_HINT_NS)
                             : mbar_try_wait(bar, parity))
       return true;

@@ -13,16 +13,17 @@
 //   B = x tile   [N     x 64 k]     f16, K-major, 128-byte swizzle, N = m
 //                                    rounded up to 16 (pad rows are zero)
 //   D_g, D_u     [128 x N] fp32 in tensor memory (2N columns)
-// Warps 0-7 produce: thread t decodes half a k-tile (one 32-weight block) of
-// row t % 128 for gate and up: cvt.rn.f16x2.e2m1x2, then an exact HMUL2 by
+// Warps 0-15 produce, in two groups of 8 that take the k-tiles in turn:
+// thread t of a group decodes half a k-tile (one 32-weight block) of row
+// t % 128 for gate and up: cvt.rn.f16x2.e2m1x2, then an exact HMUL2 by
 // 2^(X_block - X_row) where X_row is the row's largest block exponent (so the
 // f16 values stay in range and exact), stored in the swizzled layout; and
 // converts its share of the x tile (bf16 -> f16; |x| must stay below 65504,
 // larger values raise TT_ERR_UNSUPPORTED in the device error word).
-// Warp 9 brings each k-tile in with three TMA loads (gate codes 128 x 32 B,
+// Warp 17 brings each k-tile in with three TMA loads (gate codes 128 x 32 B,
 // up codes 128 x 32 B, both strided by the packed record size, and the x
 // tile, whose padding rows TMA fills with zeros) into a ring of raw slots.
-// Warp 8 allocates tensor memory, waits for each stage and issues the
+// Warp 16 allocates tensor memory, waits for each stage and issues the
 // tcgen05.mma (M=128, N, K=16) x 4 per matrix per stage, then tcgen05.commit
 // releases the stage.  Warps 0-3 finally read D with tcgen05.ld (warp w owns
 // TMEM lanes 32w..32w+31 = rows), scale by 2^X_row and the postscale, apply
