@@ -18,8 +18,10 @@
 // t % 128 for gate and up: cvt.rn.f16x2.e2m1x2, then an exact HMUL2 by
 // 2^(X_block - X_row) where X_row is the row's largest block exponent (so the
 // f16 values stay in range and exact), stored in the swizzled layout; and
-// converts its share of the x tile (bf16 -> f16; |x| must stay below 65504,
-// larger values raise TT_ERR_UNSUPPORTED in the device error word).
+// converts its share of the x tile to f16 after an exact power-of-two
+// prescale per x row that lifts a row whose first k-tile stays below 1 to
+// [1, 2) (a scaled value beyond 65504 raises TT_ERR_UNSUPPORTED in the
+// device error word).
 // Warp 17 brings each k-tile in with three TMA loads (gate codes 128 x 32 B,
 // up codes 128 x 32 B, both strided by the packed record size, and the x
 // tile, whose padding rows TMA fills with zeros) into a ring of raw slots.
@@ -165,6 +167,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Barrier among the producer warps only (warps 0 .. kProdWarps-1).
+__device__ __forceinline__ void producer_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kProdWarps * 32) : "memory");
+}
+
 // Shared-memory plan of one CTA (offsets from a 1024-aligned base).
 struct TcPlan {
   static constexpr int kMaxRaw = TT_TC_MAX_RAW;  // raw slots: packed k-tiles in flight
@@ -174,7 +181,7 @@ struct TcPlan {
   int a_bytes;     // one A tile: 128 x 128 B
   int stage_bytes; // A_g + A_u + B, 1024-aligned
   int raw_bytes;   // one raw slot: gate 4 KB + up 4 KB + x np x 128 B
-  int off_raw, off_scale, off_xr, off_bar, off_tmem, total;
+  int off_raw, off_scale, off_xr, off_sx, off_bar, off_tmem, total;
   __host__ __device__ TcPlan(int m, int k, int nraw_) : nraw(nraw_) {
     np = (m + 15) & ~15;
     nblk = k >> 5;
@@ -184,7 +191,8 @@ struct TcPlan {
     off_raw = kStages * stage_bytes;
     off_scale = off_raw + nraw * raw_bytes;
     off_xr = off_scale + 2 * kTileRows * nblk;
-    off_bar = (off_xr + 2 * kTileRows * 4 + 7) & ~7;
+    off_sx = off_xr + 2 * kTileRows * 4;  // [64] x row maxima, [64] x row exponents
+    off_bar = (off_sx + 2 * 64 * 4 + 7) & ~7;
     off_tmem = off_bar + (2 * kStages + 2 * kMaxRaw + 1) * 8;
     total = off_tmem + 16 + 1024;  // + alignment slack of the dynamic base
   }
@@ -202,6 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base = smem_raw + (sbase - smem_u32(smem_raw));
   uint8_t* sscale = base + P.off_scale;                        // [2][128][nblk]
   int* sxr = reinterpret_cast<int*>(base + P.off_xr);          // [2][128]
+  uint32_t* xmax = reinterpret_cast<uint32_t*>(base + P.off_sx); // [64] max |x| bits per x row
+  int* sxs = reinterpret_cast<int*>(xmax + 64);                  // [64] x row prescale exponents
   uint64_t* a_full = reinterpret_cast<uint64_t*>(base + P.off_bar);
   uint64_t* a_empty = a_full + kStages;
   uint64_t* raw_full = a_empty + kStages;
@@ -228,19 +238,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), tcols);
   // Per-row block scales into shared memory and each row's largest block
   // exponent: gate rows by threads 0-127, up rows by 128-255.
+  if (threadIdx.x < 64) xmax[threadIdx.x] = 0u;
   if (threadIdx.x < 2 * kTileRows) {
     const int t = threadIdx.x, r = t & 127, which = t >> 7;
     const bool valid = n0 + r < n;
     const uint8_t* src =
         packed + (int64_t)(valid ? n0 + r : 0) * L.bytes + (which ? L.up_scales() : L.gate_scales());
     uint8_t* dst = sscale + (which * kTileRows + r) * P.nblk;
-    int xmax = -1000;
+    int emax = -1000;
     for (int b = 0; b < P.nblk; ++b) {
       const uint32_t sb = valid ? src[b] : 0u;
       dst[b] = uint8_t(sb);
-      if (sb != 255u) xmax = max(xmax, int(sb) - 127);
+      if (sb != 255u) emax = max(emax, int(sb) - 127);
     }
-    sxr[which * kTileRows + r] = xmax < -127 ? -127 : xmax;
+    sxr[which * kTileRows + r] = emax < -127 ? -127 : emax;
   }
   fence_before_sync();
   __syncthreads();
@@ -317,7 +328,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = warp / kGroupWarps;
     const int t = threadIdx.x - g * kGroupWarps * 32, r = t & 127, part = t >> 7;
     const int xg = sxr[r], xu = sxr[kTileRows + r];
-    bool ok = true;
+    // An x row whose first k-tile stays below 1 in magnitude is scaled up by
+    // an exact power of two 2^sxs[i] that brings that tile's max to [1, 2),
+    // so that small activations keep their bits in f16; rows at or above 1
+    // are not scaled, and the epilogue divides the factor back out.
+    bool ok = mbar_wait_bounded(smem_u32(&raw_full[0]), 0u);
+    if (ok) {
+      const uint8_t* rw0 = base + P.off_raw;
+      for (int c = threadIdx.x; c < P.np * 8; c += kProdWarps * 32) {
+        const int row = c >> 3, piece = c & 7;
+        const uint4 v = *reinterpret_cast<const uint4*>(rw0 + 8192 + row * 128 + piece * 16);
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+        float mx = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(vw[e] & 0xFFFFu)),
+                               fabsf(bf16_bits_to_f32(vw[e] >> 16))));
+        atomicMax(&xmax[row], __float_as_uint(mx));  // non-negative: bits order as values
+      }
+    }
+    producer_bar_sync();
+    if (threadIdx.x < P.np) {
+      const float mx = __uint_as_float(xmax[threadIdx.x]);
+      sxs[threadIdx.x] = mx > 0.f ? min(max(f16_prescale_exponent(mx) - 14, 0), 127) : 0;
+    }
+    producer_bar_sync();
     for (int kt = g; kt < nkt; kt += kGroups) {
       const int s = kt % kStages, d = kt % P.nraw;
       ok = mbar_wait_bounded(smem_u32(&raw_full[d]), uint32_t((kt / P.nraw) & 1));
@@ -353,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(hmul2(h0, f), hmul2(h1, f), hmul2(h2, f), hmul2(h3, f));
         }
       }
-      // x: bf16 -> f16 (|x| < 65504; larger values are flagged)
+      // x: bf16 * 2^sxs[row] -> f16 (scaled values beyond 65504 are flagged)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int c = t + j * kGroupWarps * 32;  // row c / 8, 16-byte piece c % 8
@@ -361,11 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row < P.np) {
           const uint4 v = *reinterpret_cast<const uint4*>(rw + 8192 + row * 128 + piece * 16);
           const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+          const float two_s = scalbnf(1.0f, sxs[row]);
           uint32_t o[4];
           bool big = false;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float lo = bf16_bits_to_f32(vw[e] & 0xFFFFu), hi = bf16_bits_to_f32(vw[e] >> 16);
+            const float lo = bf16_bits_to_f32(vw[e] & 0xFFFFu) * two_s;  // exact
+            const float hi = bf16_bits_to_f32(vw[e] >> 16) * two_s;
             big = big || fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
             o[e] = pack_f16x2_scaled(lo, hi, 1.0f);
           }
@@ -390,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       pdl_wait_prior_grid();  // (no-op if already waited) before writing h
       const int nr = n0 + r;
       const uint8_t* rec = packed + (int64_t)(nr < n ? nr : 0) * L.bytes;
-      const float sg = scalbnf(*reinterpret_cast<const float*>(rec + L.post), sxr[r]);
-      const float su =
-          scalbnf(*reinterpret_cast<const float*>(rec + L.post + 4), sxr[kTileRows + r]);
+      const float pg = *reinterpret_cast<const float*>(rec + L.post);
+      const float pu = *reinterpret_cast<const float*>(rec + L.post + 4);
+      const int eg = sxr[r], eu = sxr[kTileRows + r];
       const uint32_t lane_base = uint32_t(warp * 32) << 16;
       for (int c0 = 0; c0 < P.np; c0 += 16) {
         float g[16], u[16];
@@ -403,6 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i) {
             const int mm = c0 + i;
             if (mm < m) {
+              // exact power-of-two factors: the row's block exponent and the
+              // x row's prescale, folded into the postscale
+              const float sg = scalbnf(pg, eg - sxs[mm]), su = scalbnf(pu, eu - sxs[mm]);
               __nv_bfloat16 b = __float2bfloat16_rn(silu_mul(g[i] * sg, u[i] * su));
               h[(size_t)mm * n + nr] = *reinterpret_cast<uint16_t*>(&b);
             }

@@ -224,3 +224,29 @@ def test_tensor_path_flags_activations_beyond_f16_range():
     assert gu.device_error() == 0
     h2 = gu.swiglu(packed, n, k, d["x"])
     assert np.array_equal(h2, h)
+
+
+def test_tensor_path_small_activations_keep_precision():
+    """The tensor path lifts an x row whose first k-tile stays below 1 by an
+    exact power of two before the f16 conversion, so rows of tiny activations
+    (which f16 alone would flush) match the oracle row by row."""
+    n, k, m = 160, 1024, 16
+    d = synth.gate_up_inputs(95, 0, n, k, m=m)
+    xf = synth.bf16_bits_to_f32(d["x"]).copy()
+    for i in range(m):
+        xf[i] *= np.float32(2.0 ** (-3 * i))          # rows down to 2^-45
+    xf[5, :64] *= np.float32(2.0 ** -12)               # first tile far below the rest
+    xf[7] = 0.0                                         # an all-zero row
+    x = synth.f32_to_bf16_bits(xf)
+    gc, gs, _ = gu.quantize(d["wg"])
+    uc, us, _ = gu.quantize(d["wu"])
+    packed = gu.pack_swiglu(gc, gs, gu.dev(d["pg"]), uc, us, gu.dev(d["pu"]), n, k)
+    h = gu.swiglu(packed, n, k, x)
+    assert gu.device_error() == 0
+    ref = oracle.mxfp4_swiglu_matvec((gu.host(gc), gu.host(gs), d["pg"]),
+                                     (gu.host(uc), gu.host(us), d["pu"]), x)
+    for i in range(m):
+        if i == 7:
+            assert not np.any(bf16_to_f64(h[i]))
+            continue
+        assert_float_parity(h[i], ref[i], f"row {i} scaled by 2^-{3 * i}")
