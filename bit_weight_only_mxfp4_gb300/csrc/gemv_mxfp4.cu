@@ -59,9 +59,10 @@ constexpr int kThreads = kWarps * 32;
 #endif
 
 // ---------------------------------------------------------------------------
-// m = 1, x staged once per CTA in shared memory as f16 (prescaled by 2^sx),
-// laid out chunk-major: 16-byte chunk q (0..3) of block b at xs[q*nblk + b],
-// so a warp reading blocks b..b+31 touches 32 consecutive 16-byte words.
+// m = 1, x staged once per CTA in shared memory as f16 (each 32-block
+// prescaled by its own power of two), laid out chunk-major: 16-byte chunk q
+// (0..3) of block b at xs[q*nblk + b], so a warp reading blocks b..b+31
+// touches 32 consecutive 16-byte words.
 // Keeping x out of registers lets WARPS warps per CTA stay resident while
 // the next kernel's CTA (programmatic dependent launch) shares the SM.
 // NB = number of 1024-wide K chunks; RPC = records per bulk copy.
@@ -89,9 +90,8 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   ring.bars = reinterpret_cast<uint64_t*>(smem + ring_bytes) + warp * slots;
   ring.packed = packed;
   ring.policy = l2_evict_first_policy();
-  uint4* xraw = reinterpret_cast<uint4*>(smem + ring_bytes + (size_t)WARPS * slots * 8);
-  uint4* xs = xraw + (k >> 3);
-  float* red = reinterpret_cast<float*>(xs + (k >> 3));
+  uint4* xs = reinterpret_cast<uint4*>(smem + ring_bytes + (size_t)WARPS * slots * 8);
+  float* xinv = reinterpret_cast<float*>(xs + (k >> 3));  // [nblk] 2^-s of each x block
   ring.init(lane);
 
   auto first_of = [&](int j) { return r0 + (warp + j * WARPS) * RPC; };
@@ -112,39 +112,40 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     for (int j = 0; j < min(slots, nitems); ++j) ring.issue_to(j, first_of(j), count_of(first_of(j)));
   pdl_wait_prior_grid();
 
-  // x: one global read per CTA, CTA-wide max |x| -> exact power-of-two
-  // prescale, then f16 in the chunk-major layout.
+  // x: one global read per CTA.  Each 32-block of x gets its own exact
+  // power-of-two prescale 2^s (its max |x| -> [2^14, 2^15)) and is stored as
+  // f16 in the chunk-major layout; four threads share a block (one 16-byte
+  // chunk each) and meet in two shuffles.  2^-s is folded into the block's
+  // E8M0 scale below.
   const int nchunk16 = k >> 3;
-  float mx = 0.f;
   const uint64_t x_policy = l2_evict_last_policy();
-  for (int c = threadIdx.x; c < nchunk16; c += THREADS) {
-    const uint4 v = ld_global_v4_hint(reinterpret_cast<const uint4*>(x) + c, x_policy);
-    xraw[c] = v;
-    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_bits_to_f32(v.x & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.x >> 16))),
-                         fmaxf(fabsf(bf16_bits_to_f32(v.y & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.y >> 16)))));
-    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_bits_to_f32(v.z & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.z >> 16))),
-                         fmaxf(fabsf(bf16_bits_to_f32(v.w & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.w >> 16)))));
-  }
-  mx = warp_max(mx);
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
-  float gmax = red[0];
-#pragma unroll
-  for (int w = 1; w < WARPS; ++w) gmax = fmaxf(gmax, red[w]);
-  const int sx = min(f16_prescale_exponent(gmax), 127);
-  const float two_s = scalbnf(1.0f, sx);
-  for (int c = threadIdx.x; c < nchunk16; c += THREADS) {
-    const uint4 v = xraw[c];
-    uint4 o;
-    o.x = pack_f16x2_scaled(bf16_bits_to_f32(v.x & 0xFFFFu), bf16_bits_to_f32(v.x >> 16), two_s);
-    o.y = pack_f16x2_scaled(bf16_bits_to_f32(v.y & 0xFFFFu), bf16_bits_to_f32(v.y >> 16), two_s);
-    o.z = pack_f16x2_scaled(bf16_bits_to_f32(v.z & 0xFFFFu), bf16_bits_to_f32(v.z >> 16), two_s);
-    o.w = pack_f16x2_scaled(bf16_bits_to_f32(v.w & 0xFFFFu), bf16_bits_to_f32(v.w >> 16), two_s);
-    xs[(c & 3) * L.nblk + (c >> 2)] = o;  // chunk q = c % 4 of block b = c / 4
+  for (int c0 = 0; c0 < nchunk16; c0 += THREADS) {  // uniform trip count
+    const int c = c0 + threadIdx.x;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (c < nchunk16) v = ld_global_v4_hint(reinterpret_cast<const uint4*>(x) + c, x_policy);
+    float mx = fmaxf(fmaxf(fmaxf(fabsf(bf16_bits_to_f32(v.x & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.x >> 16))),
+                           fmaxf(fabsf(bf16_bits_to_f32(v.y & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.y >> 16)))),
+                     fmaxf(fmaxf(fabsf(bf16_bits_to_f32(v.z & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.z >> 16))),
+                           fmaxf(fabsf(bf16_bits_to_f32(v.w & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.w >> 16)))));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (c < nchunk16) {
+      const int sb = min(f16_prescale_exponent(mx), 127);
+      const float two_s = scalbnf(1.0f, sb);
+      uint4 o;
+      o.x = pack_f16x2_scaled(bf16_bits_to_f32(v.x & 0xFFFFu), bf16_bits_to_f32(v.x >> 16), two_s);
+      o.y = pack_f16x2_scaled(bf16_bits_to_f32(v.y & 0xFFFFu), bf16_bits_to_f32(v.y >> 16), two_s);
+      o.z = pack_f16x2_scaled(bf16_bits_to_f32(v.z & 0xFFFFu), bf16_bits_to_f32(v.z >> 16), two_s);
+      o.w = pack_f16x2_scaled(bf16_bits_to_f32(v.w & 0xFFFFu), bf16_bits_to_f32(v.w >> 16), two_s);
+      xs[(c & 3) * L.nblk + (c >> 2)] = o;  // chunk q = c % 4 of block b = c / 4
+      if ((c & 3) == 0) xinv[c >> 2] = scalbnf(1.0f, -sb);  // exact power of two
+    }
   }
   __syncthreads();
   if (TT_M1_LATE_TRIGGER) pdl_allow_next_grid();
-  const float inv = scalbnf(1.0f, -sx);  // exact power of two
+  float xi[NB];  // this lane's blocks' 2^-s
+#pragma unroll
+  for (int i = 0; i < NB; ++i) xi[i] = 32 * i + lane < L.nblk ? xinv[32 * i + lane] : 0.f;
   EpilogueBatch ep;
 
   for (int j = 0; j < nitems; ++j) {
@@ -178,8 +179,8 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
             const uint8_t* rec = slot + rr * L.bytes;
             const uint4 cg = *reinterpret_cast<const uint4*>(rec + L.gate_codes() + b * 16);
             const uint4 cu = *reinterpret_cast<const uint4*>(rec + L.up_codes() + b * 16);
-            const float sg = e8m0_to_f32(rec[L.gate_scales() + b]);
-            const float su = e8m0_to_f32(rec[L.up_scales() + b]);
+            const float sg = e8m0_to_f32(rec[L.gate_scales() + b]) * xi[i];  // exact
+            const float su = e8m0_to_f32(rec[L.up_scales() + b]) * xi[i];
             ag[rr] = fmaf(dot32(cg, xv), sg, ag[rr]);
             au[rr] = fmaf(dot32(cu, xv), su, au[rr]);
           }
@@ -203,12 +204,12 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
       // lanes 0-7: g0, 8-15: u0, 16-23: g1, 24-31: u1
       const float v = warp_sum4(ag[0], au[0], ag[1], au[1], lane);
       if (ep.fill > 30) ep.flush(h);
-      ep.put(v, 0, 8, pg[0], pu[0], inv, first, lane);
-      if (count > 1) ep.put(v, 16, 24, pg[1], pu[1], inv, first + 1, lane);
+      ep.put(v, 0, 8, pg[0], pu[0], 1.0f, first, lane);
+      if (count > 1) ep.put(v, 16, 24, pg[1], pu[1], 1.0f, first + 1, lane);
     } else {
       const float v = warp_sum2(ag[0], au[0], lane);  // lanes 0-15: g, 16-31: u
       if (ep.fill > 31) ep.flush(h);
-      ep.put(v, 0, 16, pg[0], pu[0], inv, first, lane);
+      ep.put(v, 0, 16, pg[0], pu[0], 1.0f, first, lane);
     }
   }
   ep.flush(h);
@@ -388,7 +389,7 @@ cudaError_t run_m1x(const DeviceInfo& di, const uint8_t* packed, int n, int k, c
                     uint16_t* h, cudaStream_t s, bool pdl) {
   const SwigluRecord L(k);
   const int slot_bytes = RPC * L.bytes;
-  const int fixed = 4 * k + WARPS * 4 + 16;  // raw + f16 x, per-warp maxima
+  const int fixed = 2 * k + 4 * L.nblk + 16;  // f16 x, per-block factors
   int slots = (kHalfSmBudget - fixed) / (WARPS * (slot_bytes + 8));
   if (slots > TT_M1_SLOTS) slots = TT_M1_SLOTS;
   if (slots < 1) slots = 1;

@@ -250,3 +250,30 @@ def test_tensor_path_small_activations_keep_precision():
             assert not np.any(bf16_to_f64(h[i]))
             continue
         assert_float_parity(h[i], ref[i], f"row {i} scaled by 2^-{3 * i}")
+
+
+@pytest.mark.parametrize("k", [2048, 2880, 8192])
+def test_swiglu_m1_blocks_of_very_different_magnitude(k):
+    """The m = 1 kernel prescales each 32-block of x by its own power of two:
+    blocks spread over 2^-60 .. 2^60 (and an all-zero block) still match the
+    oracle, here with the output dominated by no single block."""
+    n = 96
+    d = synth.gate_up_inputs(96, 0, n, k, m=1)
+    g = synth.rng(96, 1)
+    nblk = k // 32
+    e = g.integers(-60, 61, nblk)
+    xf = synth.bf16_bits_to_f32(d["x"]).reshape(nblk, 32).copy()
+    xf *= np.ldexp(np.float32(1.0), e).astype(np.float32)[:, None]
+    xf[nblk // 2] = 0.0
+    # weights scaled by the inverse so that every block contributes alike
+    wg = (d["wg"].reshape(n, nblk, 32) * np.ldexp(np.float32(1.0), -e)[None, :, None]).reshape(n, k)
+    wu = (d["wu"].reshape(n, nblk, 32) * np.ldexp(np.float32(1.0), -e)[None, :, None]).reshape(n, k)
+    x = synth.f32_to_bf16_bits(xf.reshape(1, k))
+    gc, gs, _ = gu.quantize(wg.astype(np.float32))
+    uc, us, _ = gu.quantize(wu.astype(np.float32))
+    packed = gu.pack_swiglu(gc, gs, gu.dev(d["pg"]), uc, us, gu.dev(d["pu"]), n, k)
+    h = gu.swiglu(packed, n, k, x)
+    assert gu.device_error() == 0
+    ref = oracle.mxfp4_swiglu_matvec((gu.host(gc), gu.host(gs), d["pg"]),
+                                     (gu.host(uc), gu.host(us), d["pu"]), x)
+    assert_float_parity(h, ref, f"block magnitudes 2^-60..2^60, k={k}")
