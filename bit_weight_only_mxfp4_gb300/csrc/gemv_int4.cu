@@ -23,7 +23,6 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kRowsPerIter = 2;
 
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t bits) {
   uint32_t d;
@@ -57,7 +56,11 @@ __device__ __forceinline__ float chunk_dot(const uint4& c, uint32_t zz, const ui
   return (a0 + a1) + (a2 + a3);
 }
 
-template <int CPL, int MT>
+// RPW rows per warp and pass: all of a pass's codes, scales and zero points
+// are requested before the dependency wait (the first pass) or before the
+// previous pass is reduced (the others), so only the x staging and the math
+// follow the wait.
+template <int CPL, int MT, int RPW>
 __global__ void __launch_bounds__(kThreads, 2)
     int4_matvec_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
                        const uint8_t* __restrict__ zp, int n, int k, int group,
@@ -69,119 +72,127 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int zb = (ng + 1) >> 1;               // zero-point bytes per row
   const int gw = blockIdx.x * kWarps + warp;
   const int nw = gridDim.x * kWarps;
-  uint4* xs = reinterpret_cast<uint4*>(smem);  // [MT][4][nch]
-  float* red = reinterpret_cast<float*>(xs + (size_t)MT * 4 * nch);  // [MT][kWarps]
-  int* sxs = reinterpret_cast<int*>(red + MT * kWarps);              // [MT]
+  uint4* xs = reinterpret_cast<uint4*>(smem);                          // [MT][4][nch]
+  float* xinv = reinterpret_cast<float*>(xs + (size_t)MT * 4 * nch);  // [MT][nch]
 
   pdl_allow_next_grid();
 
-  // Codes of this warp's first rows do not depend on the previous kernel.
-  uint4 cw[kRowsPerIter][CPL];
+  // This warp's rows of one pass (row r + u * nw): codes, and per chunk the
+  // group's scale and f16x2 (1024 + zp).  None depends on the previous kernel.
+  // Wide rows (many chunks per lane) take their scales in the math loop
+  // instead, to stay within the registers.
+  constexpr bool kPre = CPL * RPW <= 12;
+  uint4 cw[RPW][CPL];
+  float sc[RPW][CPL];
+  uint32_t zz[RPW][CPL];
+  auto scale_of = [&](int row, int j) {
+    return row < n && j < nch
+               ? __half2float(__ushort_as_half(__ldg(scales + (size_t)row * ng + (j * 32) / group)))
+               : 0.f;
+  };
+  auto zz_of = [&](int row, int j) {
+    const int g = (j * 32) / group;
+    const uint32_t z =
+        row < n && j < nch ? (__ldg(zp + (size_t)row * zb + (g >> 1)) >> (4 * (g & 1))) & 15u : 0u;
+    return 0x64006400u + z * 0x00010001u;
+  };
   auto load_rows = [&](int r) {
 #pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u) {
+    for (int u = 0; u < RPW; ++u) {
       const int row = r + u * nw;
 #pragma unroll
       for (int c = 0; c < CPL; ++c) {
         const int j = c * 32 + lane;
-        cw[u][c] = (row < n && j < nch)
+        cw[u][c] = row < n && j < nch
                        ? __ldcs(reinterpret_cast<const uint4*>(codes + (size_t)row * (k >> 1)) + j)
                        : make_uint4(0, 0, 0, 0);
+        if constexpr (kPre) {
+          sc[u][c] = scale_of(row, j);
+          zz[u][c] = zz_of(row, j);
+        }
       }
     }
   };
   load_rows(gw);
   pdl_wait_prior_grid();
 
-  // x -> f16 (prescaled per row of x by a power of two) in pair order.
-  for (int i = 0; i < MT; ++i) {
-    float mx = 0.f;
-    if (i < m)
-      for (int t = threadIdx.x; t < (k >> 3); t += kThreads) {
-        const uint4 v = reinterpret_cast<const uint4*>(x + (size_t)i * k)[t];
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(wv[e] & 0xFFFFu)),
-                               fabsf(bf16_bits_to_f32(wv[e] >> 16))));
-      }
-    mx = warp_max(mx);
-    if (lane == 0) red[i * kWarps + warp] = mx;
-  }
-  __syncthreads();
-  if (threadIdx.x < MT) {
-    float mx = 0.f;
-    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red[threadIdx.x * kWarps + w]);
-    sxs[threadIdx.x] = min(f16_prescale_exponent(mx), 127);
-  }
-  __syncthreads();
-  for (int c = threadIdx.x; c < MT * (k >> 3); c += kThreads) {
+  // x -> f16 in pair order, each 32-chunk of each row prescaled by its own
+  // exact power of two 2^s (chunk max |x| -> [2^14, 2^15)); 2^-s is folded
+  // into the chunk's group scale below.  Four threads share a chunk (8
+  // values each) and meet in two shuffles.
+  const int n8 = MT * (k >> 3);
+  for (int c0 = 0; c0 < n8; c0 += kThreads) {  // uniform trip count
+    const int c = c0 + threadIdx.x;
     const int i = c / (k >> 3), t8 = c - i * (k >> 3);  // x[8*t8 .. 8*t8+7] of row i
-    uint4 o = make_uint4(0, 0, 0, 0);
-    if (i < m) {
-      const float two_s = scalbnf(1.0f, sxs[i]);
-      const uint4 v = reinterpret_cast<const uint4*>(x + (size_t)i * k)[t8];
-      const float e0 = bf16_bits_to_f32(v.x & 0xFFFFu), e1 = bf16_bits_to_f32(v.x >> 16);
-      const float e2 = bf16_bits_to_f32(v.y & 0xFFFFu), e3 = bf16_bits_to_f32(v.y >> 16);
-      const float e4 = bf16_bits_to_f32(v.z & 0xFFFFu), e5 = bf16_bits_to_f32(v.z >> 16);
-      const float e6 = bf16_bits_to_f32(v.w & 0xFFFFu), e7 = bf16_bits_to_f32(v.w >> 16);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (c < n8 && i < m) v = reinterpret_cast<const uint4*>(x + (size_t)i * k)[t8];
+    const float e0 = bf16_bits_to_f32(v.x & 0xFFFFu), e1 = bf16_bits_to_f32(v.x >> 16);
+    const float e2 = bf16_bits_to_f32(v.y & 0xFFFFu), e3 = bf16_bits_to_f32(v.y >> 16);
+    const float e4 = bf16_bits_to_f32(v.z & 0xFFFFu), e5 = bf16_bits_to_f32(v.z >> 16);
+    const float e6 = bf16_bits_to_f32(v.w & 0xFFFFu), e7 = bf16_bits_to_f32(v.w >> 16);
+    float mx = fmaxf(fmaxf(fmaxf(fabsf(e0), fabsf(e1)), fmaxf(fabsf(e2), fabsf(e3))),
+                     fmaxf(fmaxf(fabsf(e4), fabsf(e5)), fmaxf(fabsf(e6), fabsf(e7))));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (c < n8) {
+      const int sb = min(f16_prescale_exponent(mx), 127);
+      const float two_s = scalbnf(1.0f, sb);
+      uint4 o;
       o.x = pack_f16x2_scaled(e0, e4, two_s);
       o.y = pack_f16x2_scaled(e1, e5, two_s);
       o.z = pack_f16x2_scaled(e2, e6, two_s);
       o.w = pack_f16x2_scaled(e3, e7, two_s);
+      // word t = t8 % 4 of chunk j = t8 / 4
+      xs[((size_t)i * 4 + (t8 & 3)) * nch + (t8 >> 2)] = o;
+      if ((t8 & 3) == 0) xinv[(size_t)i * nch + (t8 >> 2)] = scalbnf(1.0f, -sb);  // exact
     }
-    // word t = t8 % 4 of chunk j = t8 / 4
-    xs[((size_t)i * 4 + (t8 & 3)) * nch + (t8 >> 2)] = o;
   }
   __syncthreads();
 
-  for (int r = gw; r < n; r += kRowsPerIter * nw) {
-    float acc[kRowsPerIter][MT];
+  for (int r = gw; r < n; r += RPW * nw) {
+    float acc[RPW][MT];
 #pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u)
+    for (int u = 0; u < RPW; ++u)
 #pragma unroll
       for (int i = 0; i < MT; ++i) acc[u][i] = 0.f;
 #pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u) {
-      const int row = r + u * nw;
-      if (row >= n) break;
+    for (int c = 0; c < CPL; ++c) {
+      const int j = c * 32 + lane;
+      if (j < nch) {
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        const int j = c * 32 + lane;
-        if (j < nch) {
-          const int g = (j * 32) / group;
-          const float sc = __half2float(__ushort_as_half(__ldg(scales + (size_t)row * ng + g)));
-          const uint32_t z = (__ldg(zp + (size_t)row * zb + (g >> 1)) >> (4 * (g & 1))) & 15u;
-          const uint32_t zz = 0x64006400u + z * 0x00010001u;  // f16x2 (1024 + z)
+        for (int i = 0; i < MT; ++i) {
+          if (i < m) {
+            uint32_t xv[16];
 #pragma unroll
-          for (int i = 0; i < MT; ++i) {
-            if (i < m) {
-              uint32_t xv[16];
+            for (int t = 0; t < 4; ++t) {
+              const uint4 q = xs[((size_t)i * 4 + t) * nch + j];
+              xv[4 * t + 0] = q.x;
+              xv[4 * t + 1] = q.y;
+              xv[4 * t + 2] = q.z;
+              xv[4 * t + 3] = q.w;
+            }
+            const float xi = xinv[(size_t)i * nch + j];
 #pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const uint4 q = xs[((size_t)i * 4 + t) * nch + j];
-                xv[4 * t + 0] = q.x;
-                xv[4 * t + 1] = q.y;
-                xv[4 * t + 2] = q.z;
-                xv[4 * t + 3] = q.w;
-              }
-              acc[u][i] = fmaf(chunk_dot(cw[u][c], zz, xv), sc, acc[u][i]);
+            for (int u = 0; u < RPW; ++u) {  // rows past n hold zero codes and scales
+              const int row = r + u * nw;
+              const float scv = kPre ? sc[u][c] : scale_of(row, j);
+              const uint32_t zzv = kPre ? zz[u][c] : zz_of(row, j);
+              acc[u][i] = fmaf(chunk_dot(cw[u][c], zzv, xv), scv * xi, acc[u][i]);
             }
           }
         }
       }
     }
-    // prefetch the next rows' codes before reducing these
-    const int rn = r + kRowsPerIter * nw;
-    load_rows(rn);
+    // request the next pass's rows before reducing these
+    load_rows(r + RPW * nw);
 #pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u) {
+    for (int u = 0; u < RPW; ++u) {
       const int row = r + u * nw;
 #pragma unroll
       for (int i = 0; i < MT; ++i) {
         const float v = warp_sum(acc[u][i]);
         if (lane == 0 && row < n && i < m) {
-          __nv_bfloat16 b = __float2bfloat16_rn(scalbnf(v, -sxs[i]));
+          __nv_bfloat16 b = __float2bfloat16_rn(v);
           y[(size_t)i * n + row] = *reinterpret_cast<uint16_t*>(&b);
         }
       }
@@ -189,17 +200,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-template <int CPL, int MT>
+template <int CPL, int MT, int RPW>
 cudaError_t run(const DeviceInfo& di, const uint8_t* codes, const uint16_t* scales,
                 const uint8_t* zp, int n, int k, int group, const uint16_t* x, int m,
                 uint16_t* y, cudaStream_t s, bool pdl) {
-  const int smem = MT * 4 * (k >> 5) * 16 + MT * kWarps * 4 + MT * 4;
+  const int smem = MT * 4 * (k >> 5) * 16 + MT * (k >> 5) * 4;
   if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
-  auto kern = int4_matvec_kernel<CPL, MT>;
+  auto kern = int4_matvec_kernel<CPL, MT, RPW>;
   cudaError_t e = ensure_smem(di, kern, smem);
   if (e != cudaSuccess) return e;
   int grid = 2 * di.sms;
-  const int need = (n + kWarps * kRowsPerIter - 1) / (kWarps * kRowsPerIter);
+  const int need = (n + kWarps * RPW - 1) / (kWarps * RPW);
   if (grid > need) grid = need;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -218,10 +229,17 @@ template <int CPL>
 cudaError_t run_m(const DeviceInfo& di, const uint8_t* codes, const uint16_t* scales,
                   const uint8_t* zp, int n, int k, int group, const uint16_t* x, int m,
                   uint16_t* y, cudaStream_t s, bool pdl) {
-  if (m == 1) return run<CPL, 1>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
-  if (m == 2) return run<CPL, 2>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
-  if (m <= 4) return run<CPL, 4>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
-  return run<CPL, 8>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+  if (m == 1) {
+    // three rows per warp when two would leave a second pass (and the
+    // registers allow it): the whole layer is then requested before the wait
+    if constexpr (CPL <= 4)
+      if (n > 2 * kWarps * 2 * di.sms)
+        return run<CPL, 1, 3>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+    return run<CPL, 1, 2>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+  }
+  if (m == 2) return run<CPL, 2, 2>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+  if (m <= 4) return run<CPL, 4, 2>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
+  return run<CPL, 8, 2>(di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
 }
 
 }  // namespace

@@ -96,6 +96,8 @@ def test_int4_quantize_full_qkv():
 @pytest.mark.parametrize("n,k,group,m", [
     (37, 2880, 128, 1), (64, 256, 64, 2), (100, 1024, 32, 3), (17, 8192, 128, 8),
     (50, 2880, 96, 4), (300, 4096, 256, 1), (5, 32, 32, 1),
+    # more rows than one pass of the grid covers (three rows per warp at m = 1)
+    (9001, 256, 64, 1), (9001, 256, 64, 3),
 ])
 def test_int4_matvec_shapes(n, k, group, m):
     d = synth.int4_inputs(97, 0, n, k, m)
@@ -118,3 +120,25 @@ def test_int4_matvec_full_qkv():
                              d["x"])
     assert_float_parity(y, ref, "int4 qkv 5120x2880")
     assert np.mean(y.ravel() == oracle.bf16_round_array(ref.ravel())) > 0.99
+
+
+def test_int4_matvec_chunks_of_very_different_magnitude():
+    """x is prescaled per 32-chunk by its own power of two: chunks spread over
+    2^-60 .. 2^60 (and an all-zero chunk).  The weights of each chunk are
+    scaled the other way as far as fp16 group scales allow (2^-10 .. 2^6), so
+    that many chunks contribute to the result."""
+    n, k, group = 64, 1024, 32
+    d = synth.int4_inputs(98, 0, n, k, 1)
+    g = synth.rng(98, 1)
+    e = g.integers(-60, 61, k // 32)
+    fx = np.repeat(np.ldexp(1.0, e), 32)
+    fw = np.repeat(np.ldexp(1.0, -np.clip(e, -6, 10)), 32)
+    xf = (synth.bf16_bits_to_f32(d["x"]).astype(np.float64) * fx).astype(np.float32)
+    xf[:, 64:96] = 0.0
+    x = synth.f32_to_bf16_bits(xf)
+    w = (d["w"].astype(np.float64) * fw).astype(np.float32)
+    codes, scales, zp = _check_quantize(w, group)
+    y = gpu_int4_matvec(codes, scales, zp, n, k, group, x)
+    ref = oracle.int4_matvec(gu.host(codes), gu.host(scales, np.uint16), gu.host(zp), group, x)
+    assert_float_parity(y, ref, "int4 chunk magnitudes 2^-60..2^60")
+    assert gu.device_error() == 0
