@@ -64,6 +64,7 @@ constexpr int kTileK = 64;                      // f16: 128 bytes = one swizzle 
 #define TT_TC_MAX_RAW 4
 #endif
 constexpr int kStages = TT_TC_STAGES;  // decoded A/B stages
+constexpr int kScaleBatch = 20;        // scale words per thread per load batch
 constexpr int kErrUnsupported = 5;              // TT_ERR_UNSUPPORTED
 
 // ---- tcgen05 / descriptor helpers ------------------------------------------
@@ -178,6 +179,7 @@ struct TcPlan {
   int nraw;
   int np;          // MMA N (batch rows padded to 16)
   int nblk;        // k / 32
+  int sstride;     // bytes per row of block scales in shared memory (odd word count)
   int a_bytes;     // one A tile: 128 x 128 B
   int stage_bytes; // A_g + A_u + B, 1024-aligned
   int raw_bytes;   // one raw slot: gate 4 KB + up 4 KB + x np x 128 B
@@ -185,12 +187,13 @@ struct TcPlan {
   __host__ __device__ TcPlan(int m, int k, int nraw_) : nraw(nraw_) {
     np = (m + 15) & ~15;
     nblk = k >> 5;
+    sstride = 4 * ((nblk >> 1) | 1);
     a_bytes = kTileRows * 128;
     stage_bytes = (2 * a_bytes + np * 128 + 1023) & ~1023;
     raw_bytes = (2 * kTileRows * 32 + np * 128 + 127) & ~127;
     off_raw = kStages * stage_bytes;
     off_scale = off_raw + nraw * raw_bytes;
-    off_xr = off_scale + 2 * kTileRows * nblk;
+    off_xr = off_scale + kTileRows * sstride;
     off_sx = off_xr + 2 * kTileRows * 4;  // [64] x row maxima, [64] x row exponents
     off_bar = (off_sx + 2 * 64 * 4 + 7) & ~7;
     off_tmem = off_bar + (2 * kStages + 2 * kMaxRaw + 1) * 8;
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (sbase - smem_u32(smem_raw));
-  uint8_t* sscale = base + P.off_scale;                        // [2][128][nblk]
+  uint8_t* sscale = base + P.off_scale;  // [128 rows][gate nblk | up nblk], row stride sstride
   int* sxr = reinterpret_cast<int*>(base + P.off_xr);          // [2][128]
   uint32_t* xmax = reinterpret_cast<uint32_t*>(base + P.off_sx); // [64] max |x| bits per x row
   int* sxs = reinterpret_cast<int*>(xmax + 64);                  // [64] x row prescale exponents
@@ -223,7 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tcols = (2 * P.np <= 32) ? 32u : (2 * P.np <= 64 ? 64u : 128u);
   const uint32_t raw_tx = uint32_t(2 * kTileRows * 32 + P.np * 128);
 
-  if (threadIdx.x == 0) {
+  auto raw_slot = [&](int d) { return sbase + uint32_t(P.off_raw + d * P.raw_bytes); };
+  const int pre = min(P.nraw, nkt);  // k-tiles requested before the main loop
+  if (threadIdx.x == kTmaWarp * 32) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&a_full[s]), kGroupWarps * 32);
       mbar_init(smem_u32(&a_empty[s]), 1);
@@ -234,21 +239,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(done), 1);
     fence_mbar_init();
+    // weights do not depend on the previous kernel: request the first
+    // k-tiles while the CTA loads its block scales (x follows the wait)
+    for (int kt = 0; kt < pre; ++kt) {
+      const uint32_t dst = raw_slot(kt), bar = smem_u32(&raw_full[kt]);
+      mbar_arrive_expect_tx(bar, raw_tx);
+      tma_load_2d(dst, &map_w, kt * 32, n0, bar);
+      tma_load_2d(dst + 4096, &map_w, k / 2 + kt * 32, n0, bar);
+    }
   }
   if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), tcols);
-  // Per-row block scales into shared memory and each row's largest block
-  // exponent: gate rows by threads 0-127, up rows by 128-255.
   if (threadIdx.x < 64) xmax[threadIdx.x] = 0u;
+  // Block scales of the CTA's rows.  A record keeps a row's gate and up
+  // scale bytes together (2 nblk bytes at a 16-byte aligned offset, a
+  // multiple of 4), so all threads copy them as 32-bit words, each batch's
+  // loads issued before its first store.  Rows past n read as zero.
+  {
+    const int nq = P.nblk >> 1;  // words per row
+    const int total = kTileRows * nq;
+    const int dr = kThreads / nq, dw = kThreads - dr * nq;  // index step in (row, word)
+    int row = threadIdx.x / nq, wd = threadIdx.x - row * nq;
+    for (int i0 = 0; i0 < total; i0 += kThreads * kScaleBatch) {
+      uint32_t v[kScaleBatch];
+      int lr = row, lw = wd;
+#pragma unroll
+      for (int i = 0; i < kScaleBatch; ++i) {
+        const int idx = i0 + threadIdx.x + i * kThreads;
+        v[i] = 0u;
+        if (idx < total && n0 + lr < n)
+          v[i] = __ldg(reinterpret_cast<const uint32_t*>(packed + (int64_t)(n0 + lr) * L.bytes +
+                                                         L.gate_scales()) + lw);
+        lw += dw;
+        lr += dr;
+        if (lw >= nq) {
+          lw -= nq;
+          ++lr;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kScaleBatch; ++i) {
+        const int idx = i0 + threadIdx.x + i * kThreads;
+        if (idx < total) *reinterpret_cast<uint32_t*>(sscale + row * P.sstride + 4 * wd) = v[i];
+        wd += dw;
+        row += dr;
+        if (wd >= nq) {
+          wd -= nq;
+          ++row;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // each row's largest block exponent (E8M0 255 is NaN and does not count):
+  // gate rows by threads 0-127, up rows by 128-255
   if (threadIdx.x < 2 * kTileRows) {
-    const int t = threadIdx.x, r = t & 127, which = t >> 7;
-    const bool valid = n0 + r < n;
-    const uint8_t* src =
-        packed + (int64_t)(valid ? n0 + r : 0) * L.bytes + (which ? L.up_scales() : L.gate_scales());
-    uint8_t* dst = sscale + (which * kTileRows + r) * P.nblk;
+    const int r = threadIdx.x & 127, which = threadIdx.x >> 7;
+    const uint8_t* src = sscale + r * P.sstride + which * P.nblk;
     int emax = -1000;
     for (int b = 0; b < P.nblk; ++b) {
-      const uint32_t sb = valid ? src[b] : 0u;
-      dst[b] = uint8_t(sb);
+      const uint32_t sb = src[b];
       if (sb != 255u) emax = max(emax, int(sb) - 127);
     }
     sxr[which * kTileRows + r] = emax < -127 ? -127 : emax;
@@ -259,19 +308,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_allow_next_grid();
 
-  auto raw_slot = [&](int d) { return sbase + uint32_t(P.off_raw + d * P.raw_bytes); };
-
   if (warp == kTmaWarp) {
     // ---------------- TMA loads ----------------
     if (lane == 0) {
-      const int pre = min(P.nraw, nkt);
-      // weights do not depend on the previous kernel: start them before waiting
-      for (int kt = 0; kt < pre; ++kt) {
-        const uint32_t dst = raw_slot(kt), bar = smem_u32(&raw_full[kt]);
-        mbar_arrive_expect_tx(bar, raw_tx);
-        tma_load_2d(dst, &map_w, kt * 32, n0, bar);
-        tma_load_2d(dst + 4096, &map_w, k / 2 + kt * 32, n0, bar);
-      }
+      // (the first k-tiles' weights were requested in the prologue)
       pdl_wait_prior_grid();  // x is produced by the previous kernel
       for (int kt = 0; kt < pre; ++kt)
         tma_load_2d(raw_slot(kt) + 8192, &map_x, kt * kTileK, 0, smem_u32(&raw_full[kt]));
@@ -377,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           w[0] = c.x;
           w[1] = c.y;
         }
-        const uint32_t sb = sscale[(mat * kTileRows + r) * P.nblk + kt * 2 + (part * kPartK) / 32];
+        const uint32_t sb = sscale[r * P.sstride + mat * P.nblk + kt * 2 + (part * kPartK) / 32];
         const uint32_t f = sb == 255u ? 0x7E007E00u : pow2_f16x2(int(sb) - 127 - (mat ? xu : xg));
         uint8_t* a = stage + mat * P.a_bytes;
 #pragma unroll
