@@ -43,7 +43,8 @@ cudaError_t launch_moe(const uint16_t* x, int hidden, int inter, const uint16_t*
 // need.
 // Every GPU that loads the library holds it until the process exits.  All calls share it, so two such
 // calls that overlap on the GPU (different streams, no ordering) race.
-// Each call writes every other element it reads, and leaves the counters zero.
+// Each call writes every other element it reads, and leaves the counters at
+// the next multiple of the grid size.
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char
     g_moe_static_scratch[kWsHOffset + kMaxMoeGrid * kMoeStaticMaxHidden * 4];

@@ -13,8 +13,9 @@ constexpr int kMaxRouterSplit = 8;  // router partial sums per expert (fused ker
 
 // Workspace: [counters 64 B][router partials, one replica per CTA:
 // kMaxMoeGrid x 256 x (s, c) fp32][output partials: kMaxMoeGrid x hidden
-// fp32].  The counters must be zero before the first call on a workspace;
-// the kernel leaves them zero again when it completes.
+// fp32].  The counters (two 64-bit words) must be zero before the first call
+// on a workspace; every call advances each by the grid size, and never
+// resets them.
 constexpr int kMaxMoeGrid = 256;
 constexpr int kMaxRouterTasks = 256;  // E * split <= max(E, grid) <= 256
 constexpr int kWsCounterBytes = 64;

@@ -133,27 +133,27 @@ bool make_plan(int hidden, int inter, int top_k, int G, int smem_limit, MoePlan&
   return false;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
 // *p += v with release semantics at GPU scope: the writes this CTA made
 // before the preceding __syncthreads are visible to whoever acquires *p.
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void red_release_add(uint64_t* p, uint64_t v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // Spins (bounded in time) until *p >= target.  One thread per CTA; the
 // acquire load orders the reads that follow it (with the __syncthreads that
 // comes after, for the whole CTA).
-__device__ bool wait_counter(const uint32_t* p, uint32_t target) {
-  if (ld_acquire_u32(p) >= target) return true;
+__device__ bool wait_counter(const uint64_t* p, uint64_t target) {
+  if (ld_acquire_u64(p) >= target) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     __nanosleep(32);
-    if (ld_acquire_u32(p) >= target) return true;
+    if (ld_acquire_u64(p) >= target) return true;
     if ((it & 63u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   const int G = gridDim.x;
   const int c = blockIdx.x;
 
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(ws);  // [0] router, [1] partials, [2] exit
+  uint64_t* cnt = reinterpret_cast<uint64_t*>(ws);  // [0] router, [1] partials
   float2* part = reinterpret_cast<float2*>(ws + kWsCounterBytes);  // [G][T] replicas
   float* opart = reinterpret_cast<float*>(ws + kWsHOffset);        // [G][hidden]
 
@@ -274,6 +274,17 @@ __global__ void __launch_bounds__(kFThreads, 1)
   __syncthreads();
   pdl_allow_next_grid();
   pdl_wait_prior_grid();  // x comes from the previous kernel
+  // The counters only grow, by G per call: the call's targets are the next
+  // multiples of G.  Read after the wait, so that the previous call on this
+  // workspace is complete; no CTA of this call adds to counter 1 before every
+  // CTA has read it, and a CTA that reads counter 0 after others added to it
+  // still rounds down to this call's base.
+  uint64_t tgt0 = 0, tgt1 = 0;
+  if (threadIdx.x == 0) {
+    const uint64_t b0 = ld_acquire_u64(&cnt[0]), b1 = ld_acquire_u64(&cnt[1]);
+    tgt0 = b0 - b0 % uint64_t(G) + uint64_t(G);
+    tgt1 = b1 - b1 % uint64_t(G) + uint64_t(G);
+  }
 
   // ---- phase A: router partials, written to every CTA's replica ----------
   const uint4* x4 = reinterpret_cast<const uint4*>(x);
@@ -353,7 +364,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   }
 
   // ---- routing decision (every CTA, same fixed-order fold) ---------------
-  if (threadIdx.x == 0) *sflag = wait_counter(&cnt[0], uint32_t(G)) ? 1 : 0;
+  if (threadIdx.x == 0) *sflag = wait_counter(&cnt[0], tgt0) ? 1 : 0;
   __syncthreads();
   if (*sflag == 0) {  // nothing of ours is in flight yet
     if (threadIdx.x == 0) flag_error(err, kErrTimeout);
@@ -585,7 +596,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   // ---- phase D: fixed-order sum of the partial vectors of our rows -------
   if (threadIdx.x == 0) {
     red_release_add(&cnt[1], 1u);  // after the CTA's partial-vector writes
-    *sflag = wait_counter(&cnt[1], uint32_t(G)) ? 1 : 0;
+    *sflag = wait_counter(&cnt[1], tgt1) ? 1 : 0;
   }
   __syncthreads();
   if (*sflag == 0) {
@@ -620,15 +631,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
     if (lane == 0) out[o0 + rr] = f32_to_bf16_rne(sum);
   }
 
-  // ---- the last CTA out resets the counters for the next call ------------
-  if (threadIdx.x == 0) {
-    const uint32_t prev = atomicAdd(&cnt[2], 1u);
-    if (prev == uint32_t(G - 1)) {
-      atomicExch(&cnt[0], 0u);
-      atomicExch(&cnt[1], 0u);
-      atomicExch(&cnt[2], 0u);
-    }
-  }
 }
 
 std::atomic<int> g_coop_pdl_state{0};  // 0 unknown, 1 cooperative + PDL accepted, 2 refused

@@ -82,9 +82,10 @@ def test_moe_full_gptoss_layer():
     assert_float_parity(out, ref, "moe gpt-oss-20b layer")
 
 
-def test_moe_workspace_reused_across_calls_and_left_zeroed():
-    """Consecutive calls on one workspace (the grid-wide counters must come
-    back to zero after each call) give the same bits as fresh workspaces."""
+def test_moe_workspace_reused_across_calls():
+    """Consecutive calls on one workspace give the same bits as fresh
+    workspaces; the two 64-bit grid-wide counters advance by the grid size
+    (one CTA per SM) per call and are never reset."""
     import torch
     from bit_weight_only_mxfp4_gb300 import thinmx
     E, H, I, K = 8, 320, 640, 4
@@ -92,6 +93,7 @@ def test_moe_workspace_reused_across_calls_and_left_zeroed():
     gup, dnp, _ = gu.build_moe_experts(list(gus), list(dns), H, I)
     wsb = thinmx.tt_moe_workspace_bytes(H, I, E, K)
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    sms = min(torch.cuda.get_device_properties(0).multi_processor_count, 256)
     for layer in range(3):
         r = synth.moe_router_inputs(41, layer, H, E)
         ref_out, ref_idx, ref_prob = gu.run_moe(r["x"], r["wr"], K, gup, dnp, H, I)
@@ -104,5 +106,7 @@ def test_moe_workspace_reused_across_calls_and_left_zeroed():
         assert np.array_equal(gu.host(out, np.uint16), ref_out)
         assert list(gu.host(idx)) == list(ref_idx)
         assert np.array_equal(gu.host(prob), ref_prob)
-        assert not gu.host(ws[:64]).any()
+        cnt = gu.host(ws[:16]).view(np.uint64)
+        assert list(cnt) == [(layer + 1) * sms] * 2
+        assert not gu.host(ws[16:64]).any()
     assert gu.device_error() == 0
