@@ -521,8 +521,9 @@ def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
 
 
 def secondary_sweep(torch, synth, loader, thinmx, device, hbm, reps=20, ms=None):
-    """Phi-4 gate/up (K=5120, N=17920) over the batch sizes: CUDA-core kernel
-    for m <= 8, tcgen05 tensor-core kernel above; weight copies > 2x L2."""
+    """Phi-4 gate/up (K=5120, N=17920) over the batch sizes: CUDA-core kernels
+    for m <= 3, tcgen05 tensor-core kernel from m = 4 (K % 64 == 0); weight
+    copies > 2x L2."""
     tensor_peak = tensor_peak_tflops()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     s = synth.SWEEP
@@ -545,11 +546,12 @@ def secondary_sweep(torch, synth, loader, thinmx, device, hbm, reps=20, ms=None)
         ms = time_graph(torch, g, reps) / copies
         b = gate_up_bytes(s.n, s.k, m)
         tflops = 4 * m * s.n * s.k / (ms * 1e-3) / 1e12
+        tc = m >= 4 and s.k % 64 == 0  # the library's dispatch at this size
         sweep[str(m)] = {"us": round(ms * 1e3, 3), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
                          "frac": round(b / (ms * 1e-3) / 1e9 / hbm, 4),
                          "TFLOPs": round(tflops, 2),
-                         "path": "tcgen05 kind::f16" if m > 8 else "cuda-core"}
-        if m > 8:  # against the dense f16/bf16 tensor peak as well
+                         "path": "tcgen05 kind::f16" if tc else "cuda-core"}
+        if tc:  # against the dense f16/bf16 tensor peak as well
             sweep[str(m)]["tensor_frac"] = round(tflops / tensor_peak, 4)
         del g
     del packs, base

@@ -1,8 +1,10 @@
-// Tensor-core (tcgen05) MXFP4 gate/up SwiGLU for batches m = 9..64.
+// Tensor-core (tcgen05) MXFP4 gate/up SwiGLU for batches m = 4..64
+// (k % 64 == 0; at m <= 8 only where its shared-memory plan fits).
 //
-// At m >= 16 the gate/up product is a real dense contraction (config:
-// Phi-4 sizes, K = 5120, N = 17920), so it runs on the 5th-generation tensor
-// cores.  The pages' prior art is Triton's tl.dot_scaled over the selected
+// From a few batch rows on, the gate/up product is a dense contraction
+// (config: Phi-4 sizes, K = 5120, N = 17920) whose cost on CUDA cores grows
+// with m (one fp32 FMA per weight and batch row), so it runs on the
+// 5th-generation tensor cores, where m = 4..16 cost the same.  The pages' prior art is Triton's tl.dot_scaled over the selected
 // experts, with fast_math off because lossy accumulation broke the MoE
 // trajectory (stardance.hackclub.com/projects/29750, MoE drift devlog); here
 // the products are exact and accumulate in fp32 in tensor memory.

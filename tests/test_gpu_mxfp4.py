@@ -121,9 +121,11 @@ def _swiglu_case(n, k, m, postscale=True, wid=92, layer=0):
 @pytest.mark.parametrize("n,k,m,post", [
     (37, 96, 1, True), (64, 32, 1, False), (129, 1024, 1, True), (300, 2880, 1, True),
     (50, 5120, 1, False), (33, 8192, 1, True), (21, 16384, 1, True),
-    (77, 2048, 2, True), (77, 2048, 3, False), (45, 5120, 4, True), (40, 2880, 8, True),
-    (31, 1056, 5, True), (19, 6144, 6, False),
-    # tcgen05 tensor-core path (m >= 9, k % 64 == 0); ragged row tiles
+    (77, 2048, 2, True), (77, 2048, 3, False),
+    # m = 4..8 with k % 64 != 0: CUDA cores
+    (31, 1056, 5, True), (37, 2080, 4, True), (29, 1120, 8, False),
+    # tcgen05 tensor-core path (m >= 4, k % 64 == 0); ragged row tiles
+    (45, 5120, 4, True), (40, 2880, 8, True), (19, 6144, 6, False),
     (128, 128, 16, True), (130, 2048, 16, True), (300, 2880, 32, False), (256, 5120, 64, True),
     (77, 1024, 9, True), (129, 4096, 40, True), (1000, 768, 63, True),
 ])
@@ -209,11 +211,12 @@ def test_tensor_path_rejects_k_not_multiple_of_64():
     assert e.value.status == 5  # TT_ERR_UNSUPPORTED, nothing launched
 
 
-def test_tensor_path_flags_activations_beyond_f16_range():
-    """The tensor path converts x to f16 for the MMA: an activation beyond
-    f16's range is reported through the device error word (no fault), and
-    the next call is unaffected."""
-    n, k, m = 128, 256, 16
+@pytest.mark.parametrize("m", [5, 16])
+def test_tensor_path_flags_activations_beyond_f16_range(m):
+    """The tensor path (m >= 4 with k % 64 == 0) converts x to f16 for the
+    MMA: an activation beyond f16's range is reported through the device
+    error word (no fault), and the next call is unaffected."""
+    n, k = 128, 256
     h, ref, packed, d = _swiglu_case(n, k, m, True)
     assert_float_parity(h, ref, "before")
     assert gu.device_error() == 0
@@ -277,3 +280,22 @@ def test_swiglu_m1_blocks_of_very_different_magnitude(k):
     ref = oracle.mxfp4_swiglu_matvec((gu.host(gc), gu.host(gs), d["pg"]),
                                      (gu.host(uc), gu.host(us), d["pu"]), x)
     assert_float_parity(h, ref, f"block magnitudes 2^-60..2^60, k={k}")
+
+
+def test_cuda_cores_serve_large_activations_where_k_is_not_a_multiple_of_64():
+    """m = 5 with k % 64 != 0 stays on the CUDA cores, whose prescale is taken
+    from the data itself: an activation of 1e5 is served exactly, with no
+    flag (the tensor path would flag it)."""
+    n, k, m = 96, 1056, 5
+    d = synth.gate_up_inputs(97, 0, n, k, m=m)
+    x = d["x"].copy()
+    x[3, 17] = synth.f32_to_bf16_bits(np.array([1.0e5], np.float32))[0]
+    gc, gs, _ = gu.quantize(d["wg"])
+    uc, us, _ = gu.quantize(d["wu"])
+    packed = gu.pack_swiglu(gc, gs, gu.dev(d["pg"]), uc, us, gu.dev(d["pu"]), n, k)
+    h = gu.swiglu(packed, n, k, x)
+    assert gu.device_error() == 0
+    ref = oracle.mxfp4_swiglu_matvec((gu.host(gc), gu.host(gs), d["pg"]),
+                                     (gu.host(uc), gu.host(us), d["pu"]), x)
+    for i in range(m):
+        assert_float_parity(h[i], ref[i], f"row {i}")
