@@ -398,34 +398,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int kt = g; kt < nkt; kt += kGroups) {
       const int s = kt % kStages, d = kt % P.nraw;
       ok = mbar_wait_bounded(smem_u32(&raw_full[d]), uint32_t((kt / P.nraw) & 1));
-      if (ok && kt >= kStages)
-        ok = mbar_wait_bounded(smem_u32(&a_empty[s]), uint32_t(((kt / kStages) - 1) & 1));
       if (!ok) break;
       const uint8_t* rw = base + P.off_raw + d * P.raw_bytes;
+      // Every load of the k-tile first, into registers: the stores below go
+      // to the same shared memory, so they would otherwise hold each later
+      // load back.  Then the raw slot is released, and only the stores wait
+      // for the stage to be free.
+      uint32_t w[2][kPartWords], sb[2];
+#pragma unroll
+      for (int mat = 0; mat < 2; ++mat) {
+        const uint8_t* src = rw + mat * 4096 + r * 32 + part * (kPartK / 2);
+        if constexpr (kPartWords == 4) {
+          const uint4 c = *reinterpret_cast<const uint4*>(src);
+          w[mat][0] = c.x;
+          w[mat][1] = c.y;
+          w[mat][2] = c.z;
+          w[mat][3] = c.w;
+        } else {
+          const uint2 c = *reinterpret_cast<const uint2*>(src);
+          w[mat][0] = c.x;
+          w[mat][1] = c.y;
+        }
+        sb[mat] = sscale[r * P.sstride + mat * P.nblk + kt * 2 + (part * kPartK) / 32];
+      }
+      uint4 xv[2];
+      int xe[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = t + j * kGroupWarps * 32;  // row c / 8, 16-byte piece c % 8
+        const int row = c >> 3, piece = c & 7;
+        xv[j] = make_uint4(0u, 0u, 0u, 0u);
+        xe[j] = 0;
+        if (row < P.np) {
+          xv[j] = *reinterpret_cast<const uint4*>(rw + 8192 + row * 128 + piece * 16);
+          xe[j] = sxs[row];
+        }
+      }
+      mbar_arrive(smem_u32(&raw_empty[d]));  // (release: the loads above are done)
+      if (kt >= kStages)
+        ok = mbar_wait_bounded(smem_u32(&a_empty[s]), uint32_t(((kt / kStages) - 1) & 1));
+      if (!ok) break;
       uint8_t* stage = base + s * P.stage_bytes;
       // W: kPartK weights per matrix -> kPartWords swizzled 16-byte chunks each
 #pragma unroll
       for (int mat = 0; mat < 2; ++mat) {
-        const uint8_t* src = rw + mat * 4096 + r * 32 + part * (kPartK / 2);
-        uint32_t w[kPartWords];
-        if constexpr (kPartWords == 4) {
-          const uint4 c = *reinterpret_cast<const uint4*>(src);
-          w[0] = c.x;
-          w[1] = c.y;
-          w[2] = c.z;
-          w[3] = c.w;
-        } else {
-          const uint2 c = *reinterpret_cast<const uint2*>(src);
-          w[0] = c.x;
-          w[1] = c.y;
-        }
-        const uint32_t sb = sscale[r * P.sstride + mat * P.nblk + kt * 2 + (part * kPartK) / 32];
-        const uint32_t f = sb == 255u ? 0x7E007E00u : pow2_f16x2(int(sb) - 127 - (mat ? xu : xg));
+        const uint32_t f =
+            sb[mat] == 255u ? 0x7E007E00u : pow2_f16x2(int(sb[mat]) - 127 - (mat ? xu : xg));
         uint8_t* a = stage + mat * P.a_bytes;
 #pragma unroll
         for (int q = 0; q < kPartWords; ++q) {
           uint32_t h0, h1, h2, h3;
-          e2m1x8_to_f16x2(w[q], h0, h1, h2, h3);
+          e2m1x8_to_f16x2(w[mat][q], h0, h1, h2, h3);
           *reinterpret_cast<uint4*>(a + sw128(r, part * kPartWords + q)) =
               make_uint4(hmul2(h0, f), hmul2(h1, f), hmul2(h2, f), hmul2(h3, f));
         }
@@ -433,12 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // x: bf16 * 2^sxs[row] -> f16 (scaled values beyond 65504 are flagged)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int c = t + j * kGroupWarps * 32;  // row c / 8, 16-byte piece c % 8
+        const int c = t + j * kGroupWarps * 32;
         const int row = c >> 3, piece = c & 7;
         if (row < P.np) {
-          const uint4 v = *reinterpret_cast<const uint4*>(rw + 8192 + row * 128 + piece * 16);
-          const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-          const float two_s = scalbnf(1.0f, sxs[row]);
+          const uint32_t vw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+          const float two_s = scalbnf(1.0f, xe[j]);
           uint32_t o[4];
           bool big = false;
 #pragma unroll
@@ -455,7 +477,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async();
       mbar_arrive(smem_u32(&a_full[s]));
-      mbar_arrive(smem_u32(&raw_empty[d]));
     }
     if (!ok) flag_error(err, kErrTimeout);
   }
