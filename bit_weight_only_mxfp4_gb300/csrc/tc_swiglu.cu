@@ -402,8 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* rw = base + P.off_raw + d * P.raw_bytes;
       // Every load of the k-tile first, into registers: the stores below go
       // to the same shared memory, so they would otherwise hold each later
-      // load back.  Then the raw slot is released, and only the stores wait
-      // for the stage to be free.
+      // load back.  Only the stores wait for the stage to be free.  The raw
+      // slot is released after the stores, which consume every loaded value,
+      // so no copy into the slot can overtake a load from it.
       uint32_t w[2][kPartWords], sb[2];
 #pragma unroll
       for (int mat = 0; mat < 2; ++mat) {
@@ -434,7 +435,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           xe[j] = sxs[row];
         }
       }
-      mbar_arrive(smem_u32(&raw_empty[d]));  // (release: the loads above are done)
       if (kt >= kStages)
         ok = mbar_wait_bounded(smem_u32(&a_empty[s]), uint32_t(((kt / kStages) - 1) & 1));
       if (!ok) break;
@@ -477,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async();
       mbar_arrive(smem_u32(&a_full[s]));
+      mbar_arrive(smem_u32(&raw_empty[d]));
     }
     if (!ok) flag_error(err, kErrTimeout);
   }
