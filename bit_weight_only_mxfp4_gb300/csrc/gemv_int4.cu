@@ -12,9 +12,11 @@
 // (q_i, q_{i+4}) of each 32-bit word become f16x2 (1024 + q) with one LOP3
 // against the exponent pattern 0x6400, and one HSUB2 of (1024 + zp) turns
 // them into the exact small integers q - zp; the products with x (f16 after
-// an exact power-of-two prescale, stored in shared memory in the same pair
-// order) accumulate in fp32 with fma.rn.f32.f16, and each chunk's sum is
-// scaled by its group's fp16 scale.
+// an exact power-of-two prescale per 32-chunk, stored in shared memory in the
+// same pair order) accumulate in fp32 with fma.rn.f32.f16, and each chunk's
+// sum is scaled by its group's fp16 scale times the chunk's inverse
+// prescale.  A warp requests its rows' codes, scales and zero points before
+// the dependency wait on the previous kernel.
 #include "common.cuh"
 #include "launch.h"
 

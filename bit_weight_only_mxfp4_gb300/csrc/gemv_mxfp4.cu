@@ -17,7 +17,8 @@
 //    kernel's tail;
 //  * lane l owns the 32-weight blocks l, l+32, l+64, ... of every row, so
 //    its slice of x is converted once (to f16 after an exact power-of-two
-//    prescale) and reused for every row;
+//    prescale, per 32-block at m = 1, per batch row at m = 2..8) and reused
+//    for every row;
 //  * E2M1 pairs are widened with cvt.rn.f16x2.e2m1x2 and multiplied into
 //    fp32 with fma.rn.f32.f16 (the e2m1 x f16 products are exact), the
 //    block's E8M0 scale is applied once per 32 products, and the split-K
