@@ -38,7 +38,7 @@ cudaError_t launch_moe(const uint16_t* x, int hidden, int inter, const uint16_t*
 // fragment the pool), or a binding with no access to a CUDA allocator.  For
 // them the MoE layer runs on this fixed array instead: the grid-wide
 // counters, router partials and the per-CTA output partial sums of one call:
-// 16,448 B + 256 x 4096 fp32 = 4.0 MB, enough for hidden <= 4096 (gpt-oss-20b
+// 524,352 B + 256 x 4096 fp32 = 4.7 MB, enough for hidden <= 4096 (gpt-oss-20b
 // uses 2880).  Static device memory starts zeroed, which is what the counters
 // need.
 // Every GPU that loads the library holds it until the process exits.  All calls share it, so two such

@@ -13,9 +13,10 @@ constexpr int kMaxRouterSplit = 8;  // router partial sums per expert (fused ker
 
 // Workspace: [counters 64 B][router partials, one replica per CTA:
 // kMaxMoeGrid x 256 x (s, c) fp32][output partials: kMaxMoeGrid x hidden
-// fp32].  The counters (two 64-bit words) must be zero before the first call
-// on a workspace; every call advances each by the grid size, and never
-// resets them.
+// fp32].  The whole workspace must be zero before the first call.  Counter 1
+// (64-bit) advances by the grid size per call and is never reset; the router
+// replicas mark an empty slot with zero bits and are cleared again by the
+// CTA that reads them.
 constexpr int kMaxMoeGrid = 256;
 constexpr int kMaxRouterTasks = 256;  // E * split <= max(E, grid) <= 256
 constexpr int kWsCounterBytes = 64;

@@ -14,9 +14,10 @@
 // One cooperative grid of one CTA per SM:
 //
 //   A  router: CTA c computes compensated partial dot products x . W_r[e]
-//      over a slice of hidden (E * split tasks) and publishes them (grid
-//      counter 0); every CTA folds each expert's partials in a fixed order
-//      into the fp32 logit and takes the top-k + softmax itself.
+//      over a slice of hidden (E * split tasks) and writes them into every
+//      CTA's replica, where a written value marks itself (never all-zero
+//      bits); every CTA polls its replica, folds each expert's partials in a
+//      fixed order into the fp32 logit and takes the top-k + softmax itself.
 //   B  the selected experts' SwiGLU outputs h (top_k * inter values) are
 //      split into 16-wide slices; CTA c owns slices [hb0, hb1) and streams
 //      exactly the gate/up records that produce them (per-warp bulk-copy
@@ -158,6 +159,36 @@ __device__ bool wait_counter(const uint64_t* p, uint64_t target) {
   }
 }
 
+// Router partials carry their own "written" mark: a stored value never has
+// all-zero bits (+0.0 is stored as -0.0, which is equal in every sum), so a
+// zero word is an empty slot.  The workspace starts zeroed, and each CTA
+// clears its replica after reading it, for the next call.
+__device__ __forceinline__ float nonzero_bits(float v) {
+  return __float_as_uint(v) == 0u ? -0.0f : v;
+}
+__device__ __forceinline__ float2 ld_relaxed_f2(const float2* p) {
+  float2 v;
+  asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p)
+               : "memory");
+  return v;
+}
+// Polls `n` partials until every one has been written (bounded in time).
+__device__ bool poll_partials(const float2* p, int n, float2* v) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    bool all = true;
+#pragma unroll
+    for (int q = 0; q < kMaxRouterSplit; ++q)
+      if (q < n) {
+        v[q] = ld_relaxed_f2(p + q);
+        all = all && __float_as_uint(v[q].x) != 0u && __float_as_uint(v[q].y) != 0u;
+      }
+    if (all) return true;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    __nanosleep(32);
+  }
+}
+
 // Bounded mbarrier wait that suspends the thread (up to hint_ns per try)
 // instead of spinning, so waiting warps leave the issue slots to the warps
 // that compute.
@@ -216,7 +247,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   const int G = gridDim.x;
   const int c = blockIdx.x;
 
-  uint64_t* cnt = reinterpret_cast<uint64_t*>(ws);  // [0] router, [1] partials
+  uint64_t* cnt = reinterpret_cast<uint64_t*>(ws);  // [1]: partial vectors ([0] unused)
   float2* part = reinterpret_cast<float2*>(ws + kWsCounterBytes);  // [G][T] replicas
   float* opart = reinterpret_cast<float*>(ws + kWsHOffset);        // [G][hidden]
 
@@ -274,15 +305,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
   __syncthreads();
   pdl_allow_next_grid();
   pdl_wait_prior_grid();  // x comes from the previous kernel
-  // The counters only grow, by G per call: the call's targets are the next
-  // multiples of G.  Read after the wait, so that the previous call on this
-  // workspace is complete; no CTA of this call adds to counter 1 before every
-  // CTA has read it, and a CTA that reads counter 0 after others added to it
-  // still rounds down to this call's base.
-  uint64_t tgt0 = 0, tgt1 = 0;
+  // Counter 1 only grows, by G per call: the call's target is the next
+  // multiple of G.  Read after the wait, so that the previous call on this
+  // workspace is complete; no CTA of this call adds to it before every CTA
+  // has read it (adds come after the routing decision, which needs every
+  // CTA's router partials).
+  uint64_t tgt1 = 0;
   if (threadIdx.x == 0) {
-    const uint64_t b0 = ld_acquire_u64(&cnt[0]), b1 = ld_acquire_u64(&cnt[1]);
-    tgt0 = b0 - b0 % uint64_t(G) + uint64_t(G);
+    const uint64_t b1 = ld_acquire_u64(&cnt[1]);
     tgt1 = b1 - b1 % uint64_t(G) + uint64_t(G);
   }
 
@@ -321,11 +351,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
     float ts = red_s[0], tc = red_c[0];
     for (int w = 1; w < wused; ++w) comp_merge(ts, tc, red_s[w], red_c[w]);
     // one copy per CTA, so that no L2 line is read by every SM below
-    for (int r = threadIdx.x; r < G; r += kFThreads) part[(size_t)r * T + t] = make_float2(ts, tc);
+    const float2 pv = make_float2(nonzero_bits(ts), nonzero_bits(tc));
+    for (int r = threadIdx.x; r < G; r += kFThreads) part[(size_t)r * T + t] = pv;
     __syncthreads();
   }
-  __syncthreads();
-  if (threadIdx.x == 0) red_release_add(&cnt[0], 1u);  // after the CTA's partial writes
 
   // x -> f16 (one power-of-two prescale) while the other CTAs finish phase A
   uint4 xr[kMaxXChunksPerThread];
@@ -364,21 +393,20 @@ __global__ void __launch_bounds__(kFThreads, 1)
   }
 
   // ---- routing decision (every CTA, same fixed-order fold) ---------------
-  if (threadIdx.x == 0) *sflag = wait_counter(&cnt[0], tgt0) ? 1 : 0;
-  __syncthreads();
-  if (*sflag == 0) {  // nothing of ours is in flight yet
-    if (threadIdx.x == 0) flag_error(err, kErrTimeout);
-    return;
-  }
+  // Warp 0 polls this CTA's replica until every partial has arrived (the
+  // values are their own signal: no separate counter and no second round
+  // trip), folds them, and clears the replica for the next call.
   if (warp == 0) {
-    const float2* mine = part + (size_t)c * T;
+    float2* mine = part + (size_t)c * T;
+    bool got = true;
     for (int e = lane; e < ((E + 31) & ~31); e += 32) {
       float lg = 0.f;
       if (e < E) {
         float2 v[kMaxRouterSplit];
+        got = poll_partials(mine + (size_t)e * split, split, v) && got;
 #pragma unroll
-        for (int p = 0; p < kMaxRouterSplit; ++p)  // independent loads, one L2 round trip
-          v[p] = p < split ? __ldcg(mine + (size_t)e * split + p) : make_float2(0.f, 0.f);
+        for (int p = 0; p < kMaxRouterSplit; ++p)
+          if (p < split) mine[(size_t)e * split + p] = make_float2(0.f, 0.f);
         float s = v[0].x, cc = v[0].y;
 #pragma unroll
         for (int p = 1; p < kMaxRouterSplit; ++p)
@@ -392,8 +420,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
       __syncwarp();
       warp_topk_softmax(slog, E, top_k, lane, sidx, sprob);
     }
+    got = __all_sync(0xffffffffu, got);
+    if (lane == 0) *sflag = got ? 1 : 0;
   }
   __syncthreads();
+  if (*sflag == 0) {  // nothing of ours is in flight yet
+    if (threadIdx.x == 0) flag_error(err, kErrTimeout);
+    return;
+  }
   if (c == 0 && threadIdx.x < top_k) {
     out_idx[threadIdx.x] = sidx[threadIdx.x];
     out_prob[threadIdx.x] = sprob[threadIdx.x];

@@ -199,15 +199,17 @@ tt_status tt_mxfp4_pack_rows(const uint8_t* codes, const uint8_t* scales, int64_
  * >= tt_moe_workspace_bytes(...) bytes, 16-byte aligned, ZERO-FILLED before
  * its first use (e.g. cudaMemsetAsync once after allocating it); the call
  * owns it until the stream reaches the end of the call and leaves it ready
- * for the next call.  Its first 64 bytes hold the kernel's two grid-wide
- * counters (64-bit); each call advances both by the number of CTAs and never
- * resets them.  After a call that reported TT_ERR_TIMEOUT through
- * tt_device_error_read, zero the workspace again before reusing it.
+ * for the next call.  Its first 64 bytes hold the kernel's grid-wide counter
+ * (64-bit), which each call advances by the number of CTAs and never resets;
+ * the router partial replicas that follow are left cleared.  After a call
+ * that reported TT_ERR_TIMEOUT through tt_device_error_read, zero the
+ * workspace again before reusing it.
  * The layer runs as one cooperative kernel of one CTA per SM: router
  * partial sums, expert choice in every CTA, each CTA computing a 16-wide
  * slice range of the selected experts' h and multiplying it into the
  * matching down columns, then a fixed-order sum of the per-CTA partial
- * outputs (two grid-wide counters in the workspace).  A shape whose
+ * outputs (a grid-wide counter and self-marking partial slots in the
+ * workspace).  A shape whose
  * shared-memory plan does not fit one CTA per SM returns TT_ERR_UNSUPPORTED
  * before any launch.
  * Requires hidden, inter multiples of 32, hidden <= 8192, inter <= 8192,
