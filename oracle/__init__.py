@@ -82,6 +82,12 @@ def _declare(lib):
         "orc_softmax_selected": (None, [_P, _P, _I32, _P]),
         "orc_moe_mlp": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _I32, _P, _P,
                                        _P, _P, _P, _P, _P, _P]),
+        "orc_e4m3_value": (ctypes.c_double, [ctypes.c_uint]),
+        "orc_e4m3_encode": (ctypes.c_uint, [ctypes.c_double]),
+        "orc_fp8_quantize": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
+        "orc_fp8_dequantize": (None, [_P, _P, _I64, _I64, _P]),
+        "orc_fp8_matvec": (None, [_P, _P, _I64, _I64, _P, _I64, _P]),
+        "orc_fp8_swiglu_matvec": (None, [_P, _P, _P, _P, _I64, _I64, _P, _I64, _P]),
         "orc_int4_quantize": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P, _P]),
         "orc_int4_dequantize": (None, [_P, _P, _P, _I64, _I64, _I32, _P]),
         "orc_int4_matvec": (None, [_P, _P, _P, _I64, _I64, _I32, _P, _I64, _P]),
@@ -310,3 +316,55 @@ def int4_matvec(codes, scales_f16, zp, group, x_bf16):
     _load().orc_int4_matvec(_ptr(codes), _ptr(sc), _ptr(zp), n, k, group,
                             _ptr(x), m, _ptr(y))
     return y
+
+
+# ---- FP8 (E4M3) with one fp32 scale per row [DL3] -------------------------
+def e4m3_value(code: int) -> float:
+    return _load().orc_e4m3_value(code)
+
+
+def e4m3_encode(t: float) -> int:
+    return _load().orc_e4m3_encode(float(t))
+
+
+def fp8_quantize(w):
+    """fp32 [n, k] -> (codes uint8 [n, k], scales fp32 [n], status)."""
+    w = _c(w, np.float32)
+    n, k = w.shape
+    codes = np.zeros((n, k), np.uint8)
+    scales = np.zeros(n, np.float32)
+    st = _load().orc_fp8_quantize(_ptr(w), n, k, _ptr(codes), _ptr(scales))
+    return codes, scales, st
+
+
+def fp8_dequantize(codes, scales):
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    n, k = codes.shape
+    out = np.zeros((n, k), np.float64)
+    _load().orc_fp8_dequantize(_ptr(codes), _ptr(scales), n, k, _ptr(out))
+    return out
+
+
+def fp8_matvec(codes, scales, x_bf16):
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    x = _c(np.atleast_2d(x_bf16), np.uint16)
+    n, k = codes.shape
+    m = x.shape[0]
+    y = np.zeros((m, n), np.float64)
+    _load().orc_fp8_matvec(_ptr(codes), _ptr(scales), n, k, _ptr(x), m, _ptr(y))
+    return y
+
+
+def fp8_swiglu_matvec(gate, up, x_bf16):
+    """gate/up: (codes, scales).  Returns fp64 [m, n]."""
+    gc, gs = _c(gate[0], np.uint8), _c(gate[1], np.float32)
+    uc, us = _c(up[0], np.uint8), _c(up[1], np.float32)
+    x = _c(np.atleast_2d(x_bf16), np.uint16)
+    n, k = gc.shape
+    m = x.shape[0]
+    h = np.zeros((m, n), np.float64)
+    _load().orc_fp8_swiglu_matvec(_ptr(gc), _ptr(gs), _ptr(uc), _ptr(us), n, k,
+                                  _ptr(x), m, _ptr(h))
+    return h

@@ -491,3 +491,119 @@ void orc_int4_matvec(const uint8_t* codes, const uint16_t* scales_f16,
         }
     }
 }
+
+/* ===================================================================== */
+/* FP8 (E4M3) with one fp32 scale per row                                 */
+/* ===================================================================== */
+
+/* E4M3 without infinities: bit 7 sign, bits 6..3 exponent (bias 7), bits
+   2..0 mantissa.  Exponent 0 is subnormal: (m/8) * 2^-6; exponent 15 with
+   mantissa 7 is NaN; otherwise 2^(e-7) * (1 + m/8).  The largest finite
+   magnitude is 448 (e = 15, m = 6). */
+double orc_e4m3_value(unsigned code)
+{
+    unsigned s = (code >> 7) & 1u;
+    unsigned e = (code >> 3) & 15u;
+    unsigned m = code & 7u;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+    return s ? -v : v;
+}
+
+/* Nearest finite E4M3 magnitude to |t|; at an exact midpoint the code
+   whose mantissa bit 0 is clear wins (ties to even); magnitudes above 448
+   saturate to 448.  The sign is copied from t, so a negative value that
+   rounds to zero gives 0x80; NaN gives 0x7F. */
+unsigned orc_e4m3_encode(double t)
+{
+    if (isnan(t)) return 0x7Fu;
+    unsigned sign = signbit(t) ? 0x80u : 0u;
+    double a = fabs(t);
+    if (a > 448.0) a = 448.0;
+    unsigned best = 0;
+    double best_d = INFINITY;
+    for (unsigned c = 0; c < 0x7Fu; ++c) { /* the 127 finite magnitudes */
+        double d = fabs(a - orc_e4m3_value(c));
+        if (d < best_d || (d == best_d && (c & 1u) == 0u)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return sign | best;
+}
+
+/* Per row: amax = max |w|; scale = fp32(amax / 448); code = E4M3 of
+   w / scale (the division in fp64 with the stored fp32 scale). */
+int orc_fp8_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes,
+                     float* scales)
+{
+    if (n < 0 || k < 0) return ORC_ERR_SHAPE;
+    int status = ORC_OK;
+    for (int64_t r = 0; r < n; ++r) {
+        const float* wr = w + r * k;
+        uint8_t* cr = codes + r * k;
+        int finite = 1;
+        double amax = 0.0;
+        for (int64_t i = 0; i < k; ++i) {
+            double v = (double)wr[i];
+            if (!isfinite(v)) finite = 0;
+            else if (fabs(v) > amax) amax = fabs(v);
+        }
+        if (!finite) {
+            scales[r] = NAN;
+            for (int64_t i = 0; i < k; ++i) cr[i] = 0;
+            status = ORC_ERR_NONFINITE;
+            continue;
+        }
+        float s = (float)(amax / 448.0);
+        scales[r] = s;
+        if (s == 0.0f) { /* amax = 0, or below what an fp32 scale can hold */
+            for (int64_t i = 0; i < k; ++i) cr[i] = 0;
+            continue;
+        }
+        for (int64_t i = 0; i < k; ++i)
+            cr[i] = (uint8_t)orc_e4m3_encode((double)wr[i] / (double)s);
+    }
+    return status;
+}
+
+void orc_fp8_dequantize(const uint8_t* codes, const float* scales, int64_t n,
+                        int64_t k, double* out)
+{
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t i = 0; i < k; ++i)
+            out[r * k + i] = orc_e4m3_value(codes[r * k + i]) * (double)scales[r];
+}
+
+/* The row sum of code values times x, then times the row's scale. */
+void orc_fp8_matvec(const uint8_t* codes, const float* scales, int64_t n,
+                    int64_t k, const uint16_t* x_bf16, int64_t m, double* y)
+{
+    for (int64_t i = 0; i < m; ++i) {
+        for (int64_t r = 0; r < n; ++r) {
+            double acc = 0.0;
+            for (int64_t kk = 0; kk < k; ++kk)
+                acc += orc_e4m3_value(codes[r * k + kk]) *
+                       orc_bf16_value(x_bf16[i * k + kk]);
+            y[i * n + r] = acc * (double)scales[r];
+        }
+    }
+}
+
+void orc_fp8_swiglu_matvec(const uint8_t* g_codes, const float* g_scales,
+                           const uint8_t* u_codes, const float* u_scales,
+                           int64_t n, int64_t k, const uint16_t* x_bf16,
+                           int64_t m, double* h)
+{
+    double* g = (double*)malloc(sizeof(double) * (size_t)(m * n));
+    double* u = (double*)malloc(sizeof(double) * (size_t)(m * n));
+    orc_fp8_matvec(g_codes, g_scales, n, k, x_bf16, m, g);
+    orc_fp8_matvec(u_codes, u_scales, n, k, x_bf16, m, u);
+    orc_swiglu(g, u, m * n, h);
+    free(g);
+    free(u);
+}

@@ -22,6 +22,11 @@
  *          over the selected experts), the 97.87 tok/s notes
  *          (dense_int4_layers) and the fixes list ("correct affine INT4
  *          partial-group quantization").
+ *   [DL3]  same feed, "Dev Log #3 — SmolLM3-3B Results": the "quality
+ *          FP8" profile (gate/up and down projections in FP8, the rest in
+ *          BF16) and its FP8 MLP kernel, a scaled matvec whose row sum of
+ *          w * x is multiplied by the row's scale.  The element format
+ *          (E4M3) and the scale rule (row amax / 448) are not printed.
  * The pages never spell out the bit formats; E2M1 (1 sign, 2 exponent bits
  * with bias 1, 1 mantissa bit) and E8M0 (8 exponent bits, bias 127, 0xFF =
  * NaN) are the MXFP4 element and scale formats, and the scale rule
@@ -95,6 +100,27 @@ int  orc_moe_mlp(const uint16_t* x_bf16, int64_t hidden, int64_t inter,
                  const uint8_t* dn_codes, const uint8_t* dn_scales,
                  double* out, int32_t* idx, double* p,
                  float* logits32 /* [E], out */);
+
+/* ---- FP8 (E4M3) with one fp32 scale per row ----------------------------- */
+/* E4M3 without infinities: bit 7 sign, bits 6..3 exponent (bias 7), bits
+   2..0 mantissa; 0x7F / 0xFF are NaN, the largest magnitude is 448.
+   Quantise per row: scale = fp32(amax / 448), code = E4M3 round-to-nearest-
+   even of w / scale, saturating at 448 (amax = 0: scale 0, zero codes; a
+   row holding a NaN/Inf: NaN scale, zero codes, ORC_ERR_NONFINITE).
+   codes: [n][k] one byte per weight; scales: fp32 [n]. */
+double   orc_e4m3_value(unsigned code);
+unsigned orc_e4m3_encode(double t);
+int  orc_fp8_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes,
+                      float* scales);
+void orc_fp8_dequantize(const uint8_t* codes, const float* scales, int64_t n,
+                        int64_t k, double* out /* [n][k] */);
+/* y[m][n] = scale[n] * sum_k E4M3(code[n][k]) * x[m][k] */
+void orc_fp8_matvec(const uint8_t* codes, const float* scales, int64_t n,
+                    int64_t k, const uint16_t* x_bf16, int64_t m, double* y);
+void orc_fp8_swiglu_matvec(const uint8_t* g_codes, const float* g_scales,
+                           const uint8_t* u_codes, const float* u_scales,
+                           int64_t n, int64_t k, const uint16_t* x_bf16,
+                           int64_t m, double* h);
 
 /* ---- grouped affine INT4 ----------------------------------------------- */
 /* groups [g*G, min((g+1)*G, k)); codes [n][k/2] low nibble = even k

@@ -405,3 +405,156 @@ def test_int4_matvec_equals_dense_dot():
     want = xf @ oracle.int4_dequantize(codes, scales, zp, G).T
     np.testing.assert_allclose(oracle.int4_matvec(codes, scales, zp, G, x), want,
                                rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------- FP8 (E4M3)
+# The next row of the hot path (a per-row-scaled FP8 matvec and SwiGLU).  The
+# element format is pinned against torch's float8_e4m3fn (a library routine),
+# the ties against hand-derived values, the quantiser by its invariants.
+
+def _torch_e4m3():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    return torch
+
+
+def test_e4m3_table_vs_torch_float8():
+    torch = _torch_e4m3()
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn)
+    ref = ref.to(torch.float64).numpy()
+    for c in range(256):
+        v = oracle.e4m3_value(c)
+        if c in (0x7F, 0xFF):
+            assert math.isnan(v) and math.isnan(ref[c])
+            continue
+        assert v == ref[c] and math.copysign(1.0, v) == math.copysign(1.0, ref[c]), hex(c)
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(0x01) == 2.0 ** -9
+
+
+def test_e4m3_encode_roundtrip_all_codes():
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            continue
+        assert oracle.e4m3_encode(oracle.e4m3_value(c)) == c, hex(c)
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+
+
+def test_e4m3_rne_ties_and_saturation():
+    for t, code in _rows("e4m3_rne_ties.txt"):
+        assert oracle.e4m3_encode(float(t)) == int(code, 16), t
+    # just off every midpoint between neighbouring finite codes, the nearest wins
+    vals = [oracle.e4m3_value(c) for c in range(0x7F)]
+    for c in range(0x7E):
+        mid = (vals[c] + vals[c + 1]) / 2
+        assert oracle.e4m3_encode(np.nextafter(mid, 0.0)) == c
+        assert oracle.e4m3_encode(np.nextafter(mid, 1e9)) == c + 1
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode(mid) == even
+
+
+def test_e4m3_encode_vs_torch_float8():
+    torch = _torch_e4m3()
+    g = np.random.default_rng(7)
+    mag = np.exp2(g.uniform(-12.0, math.log2(448.0), 20000))
+    v = (mag * g.choice([-1.0, 1.0], mag.size)).astype(np.float32)
+    vals = [oracle.e4m3_value(c) for c in range(0x7F)]
+    mids = np.array([(vals[c] + vals[c + 1]) / 2 for c in range(0x7E)], np.float32)
+    v = np.concatenate([v, mids, -mids])
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(t)) for t in v], np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def _fp8_rows(seed, n, k):
+    return synth.normal_f32(synth.rng(seed), (n, k), 0.02)
+
+
+def test_fp8_quantize_power_of_two_invariance():
+    w = _fp8_rows(110, 24, 160)
+    c0, s0, st = oracle.fp8_quantize(w)
+    assert st == oracle.OK
+    for j in (-20, -3, 5, 20):
+        c1, s1, _ = oracle.fp8_quantize(w * np.float32(2.0 ** j))
+        assert np.array_equal(c1, c0)
+        assert np.array_equal(s1, s0 * np.float32(2.0 ** j))
+
+
+def test_fp8_quantize_is_idempotent_on_its_grid():
+    # rows of E4M3 values times 2^j, each holding a +-448: the scale is 2^j,
+    # every weight is exact in fp32, and quantising gives the codes back
+    g = np.random.default_rng(11)
+    n, k = 16, 96
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    codes = g.choice(finite, (n, k)).astype(np.uint8)
+    codes[np.arange(n), g.integers(0, k, n)] = g.choice([0x7E, 0xFE], n)
+    j = g.integers(-30, 30, n)
+    vals = np.vectorize(oracle.e4m3_value)(codes)
+    w = (vals * np.exp2(j)[:, None]).astype(np.float32)
+    assert np.array_equal(w.astype(np.float64), vals * np.exp2(j)[:, None])
+    c1, s1, st = oracle.fp8_quantize(w)
+    assert st == oracle.OK
+    assert np.array_equal(s1, np.exp2(j).astype(np.float32))
+    assert np.array_equal(c1, codes)
+
+
+def test_fp8_quantize_error_bound():
+    w = _fp8_rows(111, 32, 200)
+    w[3, :100] *= np.float32(1e-4)  # small values in a row with a normal max
+    codes, scales, _ = oracle.fp8_quantize(w)
+    deq = oracle.fp8_dequantize(codes, scales)
+    s = scales.astype(np.float64)[:, None]
+    t = np.abs(w.astype(np.float64)) / s
+    # half the E4M3 spacing at |t|: 2^(floor(log2 t) - 3) / 2 in the normal
+    # range, 2^-9 / 2 below 2^-6
+    e = np.floor(np.log2(np.maximum(t, 2.0 ** -6)))
+    half = np.exp2(e - 3) / 2
+    assert np.all(np.abs(w - deq) <= half * s * (1 + 1e-12))
+    # the row maximum maps to 448 exactly
+    amax = np.abs(w).max(axis=1)
+    assert np.allclose(np.abs(deq).max(axis=1), amax, rtol=2.0 ** -4)
+    assert np.all(np.isin(codes[np.arange(32), np.abs(w).argmax(axis=1)], [0x7E, 0xFE]))
+
+
+def test_fp8_zero_and_nonfinite_rows():
+    w = _fp8_rows(112, 4, 64)
+    w[1] = 0.0
+    w[2, 5] = np.nan
+    codes, scales, st = oracle.fp8_quantize(w)
+    assert st == oracle.ERR_NONFINITE
+    assert scales[1] == 0.0 and not codes[1].any()
+    assert np.isnan(scales[2]) and not codes[2].any()
+    ref, rs, _ = oracle.fp8_quantize(w[[0, 3]])
+    assert np.array_equal(codes[[0, 3]], ref) and np.array_equal(scales[[0, 3]], rs)
+
+
+def test_fp8_matvec_brute_force():
+    # integer weights (E4M3 holds 0..16 exactly) and integer x: the sums
+    # are exact, here checked with Python integers
+    g = np.random.default_rng(13)
+    n, k, m = 7, 40, 3
+    iw = g.integers(-16, 17, (n, k))
+    codes = np.array([[oracle.e4m3_encode(float(v)) for v in row] for row in iw], np.uint8)
+    scales = np.exp2(g.integers(-4, 5, n)).astype(np.float32)
+    ix = g.integers(-50, 51, (m, k))
+    x = synth.f32_to_bf16_bits(ix.astype(np.float32))
+    y = oracle.fp8_matvec(codes, scales, x)
+    for i in range(m):
+        for r in range(n):
+            exact = Fraction(int(np.dot(iw[r], ix[i]))) * Fraction(float(scales[r]))
+            assert y[i, r] == float(exact)
+
+
+def test_fp8_swiglu_against_expit_and_gate_up_order():
+    wg = _fp8_rows(114, 20, 96)
+    wu = _fp8_rows(115, 20, 96) * np.float32(3.0)
+    gc, gs, _ = oracle.fp8_quantize(wg)
+    uc, us, _ = oracle.fp8_quantize(wu)
+    x = synth.normal_bf16(synth.rng(116), (2, 96))
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    g = xf @ oracle.fp8_dequantize(gc, gs).T
+    u = xf @ oracle.fp8_dequantize(uc, us).T
+    h = oracle.fp8_swiglu_matvec((gc, gs), (uc, us), x)
+    np.testing.assert_allclose(h, g * expit(g) * u, rtol=1e-12, atol=1e-300)
+    swapped = oracle.fp8_swiglu_matvec((uc, us), (gc, gs), x)
+    assert not np.allclose(h, swapped)
