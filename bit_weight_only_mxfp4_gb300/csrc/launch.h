@@ -41,11 +41,12 @@ cudaError_t launch_quantize_int4(const float* w, int64_t n, int64_t k, int group
                                  uint8_t* codes, uint16_t* scales, uint8_t* zp, int32_t* status,
                                  cudaStream_t s);
 
-// gemv_mxfp4.cu — CUDA-core gate/up SwiGLU matvec, m in [1, 16]
+// gemv_mxfp4.cu — CUDA-core gate/up SwiGLU matvec, m in [1, 8]
 cudaError_t launch_swiglu_mxfp4_cc(const uint8_t* packed, int n, int k, const uint16_t* x,
                                    int m, uint16_t* h, cudaStream_t s, bool pdl);
 
-// tc_swiglu.cu — tcgen05 gate/up SwiGLU, m in [9, 64], k % 64 == 0
+// tc_swiglu.cu — tcgen05 gate/up SwiGLU, m in [1, 64] (the library sends
+// m >= 4), k % 64 == 0; a plan that does not fit: cudaErrorInvalidConfiguration
 cudaError_t launch_swiglu_mxfp4_tc(const uint8_t* packed, int n, int k, const uint16_t* x,
                                    int m, uint16_t* h, cudaStream_t s, bool pdl);
 int tc_swiglu_smem_bytes(int m, int k);
