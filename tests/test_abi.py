@@ -37,6 +37,24 @@ def test_every_declared_symbol_is_exported(lib):
         assert name in thinmx.SIGNATURES, f"binding lacks {name}"
 
 
+def declared_arities():
+    """name -> number of parameters, from the prototypes in the header."""
+    text = open(os.path.join(ROOT, "include", "thinmx.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(tt_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text):
+        params = " ".join(params.split())
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    ar = declared_arities()
+    assert set(ar) == set(declared_symbols())
+    for name, n in ar.items():
+        assert len(thinmx.SIGNATURES[name][1]) == n, name
+
+
 def test_status_strings(lib):
     assert thinmx.tt_status_str(0) == "TT_OK"
     assert thinmx.tt_status_str(7) == "TT_ERR_TIMEOUT"
