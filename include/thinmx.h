@@ -233,8 +233,8 @@ tt_status tt_moe_mxfp4_topk_mlp(const uint16_t* x_bf16, int64_t hidden, int64_t 
  * can synchronise the device or fragment the pool), or bindings without a
  * CUDA allocator.  The call allocates nothing; it runs on a fixed array
  * inside the library (static device memory, held by every GPU that loads
- * the library until the process exits, zero at load: 16,448 bytes of
- * counters and router partials + 256 * 4 * TT_MOE_STATIC_MAX_HIDDEN bytes
+ * the library until the process exits, zero at load: 524,352 bytes of
+ * counter and router partials + 256 * 4 * TT_MOE_STATIC_MAX_HIDDEN bytes
  * of partial outputs) sized for hidden <= TT_MOE_STATIC_MAX_HIDDEN; larger
  * requests return TT_ERR_SIZE before any launch.  After a TT_ERR_TIMEOUT
  * from this entry point its counters may be left set: the process must not
