@@ -1,15 +1,18 @@
 """Benchmark of the weight-only MXFP4 decode matvec path on one GB300.
 
-One step = one pass of the SmolLM3-3B-shaped gate/up stack at batch 1:
-24 MXFP4 gate/up SwiGLU layers (K=2048, N=11008, fp32 row postscale) and
-12 bf16 gate/up SwiGLU layers, each layer with its own weights and its own
-bf16 activation vector.  The stack's weights (1.66 GB) exceed L2 many times,
-so every step streams from HBM.
+One step = the 24 MXFP4 gate/up SwiGLU layers (layers 0:24) of the
+SmolLM3-3B-shaped decode stack at batch 1: each layer K=2048, N=11008, fp32
+row postscale, its own weights and its own bf16 activation vector, the 24
+calls chained with programmatic dependent launch in one CUDA graph.  The
+layers' weights (577 MB) exceed L2 several times, so every step streams from
+HBM.
 
-Prints one JSON line.  `value` is the stack's algorithmic weight traffic per
-second (GB/s); per-layer microseconds, the roofline fraction of the dominant
-kernel, the other workloads (single layer, batch sweep, ...) and the CPU
-oracle baseline ride along in the same line.
+Prints one JSON line.  `value` is the MXFP4 layer's algorithmic weight
+traffic per second (GB/s; µs per layer beside it) and `roofline` is that
+kernel's.  The full 36-layer stack (with the 12 bf16 layers), the other
+workloads (single layer over rotating copies, batch sweep, MoE, INT4) and
+the CPU oracle baseline (one thread, and all host cores) ride along in the
+same line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl thinmx|reference]
 
@@ -161,18 +164,24 @@ def capture(torch, fn):
     return g
 
 
-def time_graph(torch, g, reps, warm=3):
+def replay_times(torch, g, reps):
+    """Per-replay CUDA-event times (ms) of `reps` back-to-back replays on the
+    current stream; the events sit between replays and add no sync."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record()
+    for i in range(reps):
+        g.replay()
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
+
+
+def time_graph(torch, g, reps=20, warm=3):
+    """Median of at least 20 timed replays (ms per replay), after `warm`."""
     for _ in range(warm):
         g.replay()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / reps  # ms per replay
+    return statistics.median(replay_times(torch, g, max(20, reps)))
 
 
 def stack_bytes(cfg):
@@ -186,10 +195,17 @@ def gate_up_bytes(n, k, m, postscale=True):
 
 
 # ---------------------------------------------------------------------------
-def cpu_baseline(target_s: float = 10.0, rows=None):
-    """The fp64 CPU oracle, as it stands, on a bounded sample of the stack:
-    one MXFP4 layer and one bf16 layer (rows of each), run alternately until
-    about target_s seconds of oracle time have been spent."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_layer(rows=None):
+    """One MXFP4 gate/up layer of the headline workload (K=2048, N=11008,
+    with postscales), drawn and quantised by the oracle (setup, not timed).
+    `rows` keeps only the first rows (a bounded sample)."""
     import oracle
     from bit_weight_only_mxfp4_gb300 import synth
     cfg = synth.STACK
@@ -197,21 +213,62 @@ def cpu_baseline(target_s: float = 10.0, rows=None):
     d = synth.gate_up_inputs(cfg.wid, 0, rows, cfg.k)
     gc, gs, _ = oracle.mxfp4_quantize(d["wg"])
     uc, us, _ = oracle.mxfp4_quantize(d["wu"])
-    db = synth.bf16_gate_up_inputs(cfg.wid, cfg.mxfp4_layers, rows, cfg.k)
-    mx_bytes = gate_up_bytes(rows, cfg.k, 1)
-    bf_bytes = 2 * rows * cfg.k * 2 + 2 * cfg.k + 2 * rows
-    t_total, bytes_total, calls = 0.0, 0, 0
-    while t_total < target_s or calls < 2:
-        t0 = time.perf_counter()
-        oracle.mxfp4_swiglu_matvec((gc, gs, d["pg"]), (uc, us, d["pu"]), d["x"])
-        oracle.bf16_swiglu_matvec(db["wg"], db["wu"], db["x"])
-        t_total += time.perf_counter() - t0
-        bytes_total += mx_bytes + bf_bytes
-        calls += 2
-    return {"value": bytes_total / t_total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"MXFP4 gate/up layer 0 and bf16 layer 24 of the stack ({rows} of {cfg.n} "
-                      f"rows each), {calls} calls, {t_total:.1f} s, fp64 single thread",
+    return {"gate": (gc, gs, d["pg"]), "up": (uc, us, d["pu"]), "x": d["x"], "rows": rows,
+            "n": cfg.n, "k": cfg.k, "bytes": gate_up_bytes(rows, cfg.k, 1)}
+
+
+def oracle_layer_call(L, threads, pool=None):
+    """The oracle's SwiGLU matvec over the layer's rows: one call, or (threads
+    > 1) contiguous row ranges on `threads` host threads, the oracle's own
+    parallelisation over output rows (the C calls release the GIL)."""
+    import oracle
+    if threads <= 1:
+        return oracle.mxfp4_swiglu_matvec(L["gate"], L["up"], L["x"])
+    rows = L["rows"]
+    cuts = [rows * i // threads for i in range(threads + 1)]
+
+    def part(i):
+        a, b = cuts[i], cuts[i + 1]
+        return oracle.mxfp4_swiglu_matvec(tuple(v[a:b] for v in L["gate"]),
+                                          tuple(v[a:b] for v in L["up"]), L["x"])
+    return list(pool.map(part, range(threads)))
+
+
+def oracle_leg(L, threads, target_s):
+    """Times the oracle on layer L until about target_s seconds have passed."""
+    import concurrent.futures as cf
+    pool = cf.ThreadPoolExecutor(max_workers=threads) if threads > 1 else None
+    try:
+        oracle_layer_call(L, threads, pool)  # first touch of the pages
+        t_total, calls = 0.0, 0
+        while t_total < target_s or calls < 2:
+            t0 = time.perf_counter()
+            oracle_layer_call(L, threads, pool)
+            t_total += time.perf_counter() - t0
+            calls += 1
+    finally:
+        if pool is not None:
+            pool.shutdown()
+    return {"value": L["bytes"] * calls / t_total / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "us_per_layer": round(t_total / calls * 1e6, 1),
+            "sample": f"MXFP4 gate/up layer 0 of the stack ({L['rows']} of {L['n']} rows, "
+                      f"K={L['k']}), {calls} calls, {t_total:.1f} s, fp64, "
+                      + ("1 thread" if threads == 1 else
+                         f"{threads} threads over output rows"),
             "seconds": round(t_total, 2)}
+
+
+def cpu_baseline(target_s: float = 8.0):
+    """The fp64 CPU oracle, as it stands, on the headline workload's unit (one
+    MXFP4 gate/up layer), timed (i) on one thread and (ii) over output rows on
+    every host core.  The all-cores leg is the reported value."""
+    L = oracle_layer()
+    single = oracle_leg(L, 1, target_s)
+    cores = host_cores()
+    allc = oracle_leg(L, cores, target_s) if cores > 1 else dict(single)
+    out = dict(allc)
+    out["legs"] = [single, allc]
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -222,6 +279,9 @@ DRAM_TRAFFIC = {
     "swiglu_mxfp4_m1x_kernel": 24156160,
     "swiglu_bf16_kernel": 92261376,
 }
+# The kernel that serves the batch-1 MXFP4 gate/up layer at K = 2048.
+MXFP4_M1_KERNEL = "swiglu_mxfp4_m1x_kernel"
+NOMINAL_HBM_GBS = 8000.0
 
 
 def max_over_ranks(dist, vals, device=None):
@@ -304,62 +364,49 @@ def main():
     cfg = synth.STACK
     layers = build_stack(torch, synth, loader, cfg, device)
     mx_b, bf_b = stack_bytes(cfg)
-    step_bytes = cfg.mxfp4_layers * mx_b + (cfg.layers - cfg.mxfp4_layers) * bf_b
-
-    g_step = capture(torch, lambda: [run_layer(thinmx, cfg, L) for L in layers])
     mx_layers = [L for L in layers if L[0] == "mxfp4"]
     bf_layers = [L for L in layers if L[0] == "bf16"]
+    n_mx = len(mx_layers)
+    step_bytes = n_mx * mx_b  # the step: the stack's 24 MXFP4 layers
+
     g_mx = capture(torch, lambda: [run_layer(thinmx, cfg, L) for L in mx_layers])
     g_bf = capture(torch, lambda: [run_layer(thinmx, cfg, L) for L in bf_layers])
+    g_stack = capture(torch, lambda: [run_layer(thinmx, cfg, L) for L in layers])
 
-    # ---- timed region: K steps of the stack -------------------------------
+    # ---- timed region: K steps (24 PDL-chained MXFP4 layers each) ----------
     for _ in range(args.warmup):
-        g_step.replay()
+        g_mx.replay()
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
     with Clocks(local) as clk:
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            g_step.replay()
-        e1.record()
-        torch.cuda.synchronize()
+        step_ms = replay_times(torch, g_mx, args.steps)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms_med = statistics.median(step_ms)
+    ms_mean = sum(step_ms) / len(step_ms)
 
-    # per-kernel average launch duration (same stream, CUDA events)
-    reps = max(10, args.steps)
-    ms_mx = time_graph(torch, g_mx, reps) / len(mx_layers)
-    ms_bf = time_graph(torch, g_bf, reps) / len(bf_layers)
+    # the bf16 layers and the whole 36-layer stack, medians of >= 20 replays
+    ms_bf = time_graph(torch, g_bf) / len(bf_layers)
+    ms_stack = time_graph(torch, g_stack)
 
     # ---- end to end through the public API with host buffers --------------
-    L = len(layers)
-    x_host = torch.empty((L, cfg.k), dtype=torch.bfloat16).pin_memory()
-    h_host = torch.empty((L, cfg.n), dtype=torch.bfloat16).pin_memory()
-    for i, lay in enumerate(layers):
+    x_host = torch.empty((n_mx, cfg.k), dtype=torch.bfloat16).pin_memory()
+    h_host = torch.empty((n_mx, cfg.n), dtype=torch.bfloat16).pin_memory()
+    for i, lay in enumerate(mx_layers):
         x_host[i].copy_(lay[2][0].cpu())
-    x_dev = torch.empty((L, cfg.k), dtype=torch.bfloat16, device=device)
-    h_dev = torch.empty((L, cfg.n), dtype=torch.bfloat16, device=device)
+    x_dev = torch.empty((n_mx, cfg.k), dtype=torch.bfloat16, device=device)
+    h_dev = torch.empty((n_mx, cfg.n), dtype=torch.bfloat16, device=device)
 
     # each layer's call with its device addresses, resolved once (the binding
     # takes raw addresses as well as tensors)
-    xs_ptr = [x_dev[i:i + 1].data_ptr() for i in range(L)]
-    hs_ptr = [h_dev[i:i + 1].data_ptr() for i in range(L)]
     stream = torch.cuda.current_stream().cuda_stream
-    calls = []
-    for i, (kind, w, _, _) in enumerate(layers):
-        if kind == "mxfp4":
-            calls.append((thinmx.tt_mxfp4_swiglu_matvec,
-                          (w.data_ptr(), cfg.n, cfg.k, xs_ptr[i], 1, hs_ptr[i], stream)))
-        else:
-            calls.append((thinmx.tt_bf16_swiglu_matvec,
-                          (w[0].data_ptr(), w[1].data_ptr(), cfg.n, cfg.k, xs_ptr[i], 1,
-                           hs_ptr[i], stream)))
+    calls = [(thinmx.tt_mxfp4_swiglu_matvec,
+              (w.data_ptr(), cfg.n, cfg.k, x_dev[i:i + 1].data_ptr(), 1,
+               h_dev[i:i + 1].data_ptr(), stream))
+             for i, (_, w, _, _) in enumerate(mx_layers)]
 
     def e2e_step():
         x_dev.copy_(x_host, non_blocking=True)
@@ -371,18 +418,26 @@ def main():
     for _ in range(args.warmup):
         e2e_step()
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
+    e2e_ms = []
     for _ in range(args.steps):
+        t0 = time.perf_counter()
         e2e_step()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_med = statistics.median(e2e_ms)
     # the slowest replica sets both step times
-    ms, e2e_ms = max_over_ranks(pg, [ms, e2e_ms], device)
+    ms_med, ms_mean, e2e_med = max_over_ranks(pg, [ms_med, ms_mean, e2e_med], device)
 
     # ---- secondary workloads (rank 0 only) -----------------------------------
     others = {}
     hbm, peak_kind, _ = peaks()
     if rank == 0 and not args.quick:
         others = secondary(torch, synth, loader, thinmx, device, hbm, peak_kind)
+    others["smollm3_3b_gate_up_stack_36l_mxfp4_0_24"] = {
+        "us": round(ms_stack * 1e3, 2),
+        "GBps": round(job_throughput(n_mx * mx_b + len(bf_layers) * bf_b, 1, ms_stack), 1),
+        "bytes": n_mx * mx_b + len(bf_layers) * bf_b,
+        "us_per_layer": {"mxfp4": round(ms_med * 1e3 / n_mx, 3), "bf16": round(ms_bf * 1e3, 3)},
+        "timing": "one CUDA graph of the 36 PDL-chained calls; median of 20 replays"}
 
     # ---- cpu baseline ---------------------------------------------------------
     cpu = None
@@ -395,26 +450,30 @@ def main():
             pg.destroy_process_group()
         return 0
 
-    gbs = job_throughput(step_bytes, world, ms)
-    mx_ach = mx_b / (ms_mx * 1e-3) / 1e9
+    gbs = job_throughput(step_bytes, world, ms_med)
+    us_mx = ms_med * 1e3 / n_mx
+    mx_ach = mx_b / (us_mx * 1e-6) / 1e9
     bf_ach = bf_b / (ms_bf * 1e-3) / 1e9
-    t_mx_total = ms_mx * len(mx_layers)
-    t_bf_total = ms_bf * len(bf_layers)
+    mx_kernel = MXFP4_M1_KERNEL
     kernels = [
-        {"kernel": "swiglu_mxfp4_m1x_kernel", "bound": "hbm", "achieved": round(mx_ach, 1),
+        {"kernel": mx_kernel, "bound": "hbm", "achieved": round(mx_ach, 1),
          "peak": hbm, "unit": "GB/s", "frac": round(mx_ach / hbm, 4),
-         "bytes_per_launch": mx_b, "us_per_launch": round(ms_mx * 1e3, 3),
-         "time_share": round(t_mx_total / (t_mx_total + t_bf_total), 3)},
+         "frac_of_nominal_8tbs": round(mx_ach / NOMINAL_HBM_GBS, 4),
+         "bytes_per_launch": mx_b, "us_per_launch": round(us_mx, 3),
+         "traffic": DRAM_TRAFFIC.get(mx_kernel)},
         {"kernel": "swiglu_bf16_kernel", "bound": "hbm", "achieved": round(bf_ach, 1),
          "peak": hbm, "unit": "GB/s", "frac": round(bf_ach / hbm, 4),
+         "frac_of_nominal_8tbs": round(bf_ach / NOMINAL_HBM_GBS, 4),
          "bytes_per_launch": bf_b, "us_per_launch": round(ms_bf * 1e3, 3),
-         "time_share": round(t_bf_total / (t_mx_total + t_bf_total), 3)},
+         "traffic": DRAM_TRAFFIC.get("swiglu_bf16_kernel")},
     ]
-    dominant = max(kernels, key=lambda d: d["time_share"])
-    roofline = {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac")}
-    roofline["traffic"] = DRAM_TRAFFIC.get(dominant["kernel"])
-    roofline["kernel"] = dominant["kernel"]
-    roofline["peak_source"] = f"{peak_kind} HBM copy bandwidth"
+    roofline = {k: kernels[0][k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                           "traffic")}
+    roofline["kernel"] = mx_kernel
+    roofline["frac_of_nominal_8tbs"] = kernels[0]["frac_of_nominal_8tbs"]
+    roofline["peak_source"] = f"{peak_kind} HBM copy bandwidth (of {peak_kind})"
+    roofline["target_frac"] = 0.75
+    roofline["target_met"] = bool(mx_ach / hbm >= 0.75)
     line = {
         "metric": "batch-1 MXFP4 SwiGLU matvec µs/layer, weight GB/s and % of GB300 HBM roofline",
         "value": round(gbs, 1),
@@ -422,26 +481,29 @@ def main():
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms, 5),
+        "ms_per_step": round(ms_med, 5),
+        "ms_per_step_mean": round(ms_mean, 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "mxfp4(e2m1+e8m0) x bf16 -> fp32 acc -> bf16",
         "data": "synthetic: W ~ N(0,0.02^2) quantised to MXFP4 on the GPU, x ~ N(0,1) bf16, "
                 "postscale ~ U[0.9,1.1]; seeded",
-        "config": {"workload": cfg.name, "layers": cfg.layers, "mxfp4_layers": "0:24",
-                   "k": cfg.k, "n": cfg.n, "m": 1, "bytes_per_step": step_bytes,
-                   "l2_policy": "inputs larger than L2 (1.66 GB of weights per step)",
-                   "timing": "CUDA graph of the 36 calls, CUDA events on the replay stream"},
-        "us_per_layer": {"mxfp4": round(ms_mx * 1e3, 3), "bf16": round(ms_bf * 1e3, 3),
-                         "stack_total": round(ms * 1e3, 2)},
+        "config": {"workload": "smollm3_3b_mxfp4_gate_up_layers_0_24_k2048_n11008_m1",
+                   "layers_per_step": n_mx, "k": cfg.k, "n": cfg.n, "m": 1,
+                   "bytes_per_step": step_bytes, "bytes_per_layer": mx_b,
+                   "l2_policy": "inputs larger than L2 (577 MB of MXFP4 weights per step)",
+                   "timing": "CUDA graph of the 24 PDL-chained calls; CUDA events on the replay "
+                             "stream around every step; median of the K steps"},
+        "us_per_layer": {"mxfp4": round(us_mx, 3), "bf16": round(ms_bf * 1e3, 3)},
         "roofline": roofline,
         "roofline_by_kernel": kernels,
-        "e2e": {"value": round(job_throughput(step_bytes, world, e2e_ms), 1), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": L * cfg.k * 2, "d2h_bytes_per_step": L * cfg.n * 2,
-                "path": "pinned host x -> device, 36 C-ABI calls (no graph), h -> pinned host"},
-        "gpu_launches": len(layers) * args.steps,
+        "e2e": {"value": round(job_throughput(step_bytes, world, e2e_med), 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_med, 4),
+                "h2d_bytes_per_step": n_mx * cfg.k * 2, "d2h_bytes_per_step": n_mx * cfg.n * 2,
+                "path": "pinned host x -> device, 24 C-ABI calls (no graph), h -> pinned host; "
+                        "median of the K steps"},
+        "gpu_launches": n_mx * args.steps,
         "clocks": clk.summary(),
         "others": others,
         "cpu_baseline": cpu,
@@ -633,28 +695,42 @@ def moe_workload(torch, synth, loader, thinmx, device, hbm, reps=20, layers=None
 
 def reference_arm(args, world, rank):
     """The CPU oracle timed as the reference arm (the pages ship no runnable
-    implementation): each step is a bounded sample of the stack."""
+    implementation).  Each step is a bounded sample of the headline workload:
+    one full MXFP4 gate/up layer (K=2048, N=11008), the oracle's matvec over
+    output rows on every host core."""
     if rank != 0:
         return 0
-    from bit_weight_only_mxfp4_gb300 import synth
-    cfg = synth.STACK
-    rows = 512
-    for _ in range(args.warmup):
-        cpu_baseline(0.0, rows)
-    t0 = time.perf_counter()
-    vals = [cpu_baseline(0.0, rows) for _ in range(args.steps)]
-    dt = time.perf_counter() - t0
-    v = statistics.median(x["value"] for x in vals)
+    import concurrent.futures as cf
+    L = oracle_layer()
+    cores = host_cores()
+    pool = cf.ThreadPoolExecutor(max_workers=cores) if cores > 1 else None
+    try:
+        for _ in range(args.warmup):
+            oracle_layer_call(L, cores, pool)
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            oracle_layer_call(L, cores, pool)
+            times.append(time.perf_counter() - t0)
+    finally:
+        if pool is not None:
+            pool.shutdown()
+    med = statistics.median(times)
+    v = L["bytes"] / med / 1e9
+    sample = (f"MXFP4 gate/up layer 0 of the stack (all {L['rows']} rows, K={L['k']}) per step, "
+              f"fp64 oracle over output rows on {cores} host threads; median of {args.steps}")
     line = {
         "impl": "reference",
         "metric": "batch-1 MXFP4 SwiGLU matvec µs/layer, weight GB/s and % of GB300 HBM roofline",
         "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "warmup": args.warmup, "ms_per_step": round(med * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic, seeded (same draws as the GPU arm)",
-        "config": {"workload": cfg.name, "sample_rows": rows},
-        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": vals[0]["sample"]},
+        "data": "synthetic, seeded (the same distributions as the GPU arm)",
+        "config": {"workload": "smollm3_3b_mxfp4_gate_up_layers_0_24_k2048_n11008_m1",
+                   "sample": "one layer per step"},
+        "us_per_layer": {"mxfp4": round(med * 1e6, 1)},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
