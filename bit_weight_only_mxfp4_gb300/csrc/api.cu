@@ -163,16 +163,20 @@ tt_status tt_mxfp4_swiglu_matvec(const void* packed, int64_t n, int64_t k,
   if (m < 1 || m > 64) return TT_ERR_SHAPE;
   if (!packed || !x_bf16 || !h_bf16) return TT_ERR_NULL;
   if (!aligned(packed, 16) || !aligned(x_bf16, 16) || !aligned(h_bf16, 2)) return TT_ERR_ALIGN;
-  // m >= 4 goes to the tensor cores where k allows (k % 64 == 0 and the
-  // shared-memory plan fits); m <= 8 falls back to the CUDA-core kernels.
-  // Measured at K = 5120: the tensor path is flat at ~54 us for m = 3..16,
-  // the CUDA cores take 53 / 55 / 90 / 99 us at m = 3 / 4 / 5 / 8.
+  // m = 2..8: the tile kernel with its multiply-adds on mma.sync, where its
+  // x registers hold K (k <= 5120).  m = 1 streams records on the CUDA-core
+  // kernels.  Otherwise m >= 4 goes to the tcgen05 kernel where k allows
+  // (k % 64 == 0 and the shared-memory plan fits), and m <= 8 falls back to
+  // the CUDA-core kernels.
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
-  cudaError_t e = cudaErrorInvalidConfiguration;
-  if (m > 8 || (m >= kTcMinBatch && k % 64 == 0))
+  cudaError_t e = cudaErrorInvalidConfiguration;  // "nothing launched"
+  if (m >= 2 && m <= 8)
+    e = tt::launch_swiglu_mxfp4_mma(pk, int(n), int(k), x_bf16, int(m), h_bf16, as_stream(stream),
+                                    kPdl);
+  if (e == cudaErrorInvalidConfiguration && (m > 8 || (m >= kTcMinBatch && k % 64 == 0)))
     e = tt::launch_swiglu_mxfp4_tc(pk, int(n), int(k), x_bf16, int(m), h_bf16, as_stream(stream),
                                    kPdl);
-  if (m <= 8 && e == cudaErrorInvalidConfiguration)  // nothing was launched
+  if (m <= 8 && e == cudaErrorInvalidConfiguration)
     e = tt::launch_swiglu_mxfp4_cc(pk, int(n), int(k), x_bf16, int(m), h_bf16, as_stream(stream),
                                    kPdl);
   if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;

@@ -45,6 +45,11 @@ cudaError_t launch_quantize_int4(const float* w, int64_t n, int64_t k, int group
 cudaError_t launch_swiglu_mxfp4_cc(const uint8_t* packed, int n, int k, const uint16_t* x,
                                    int m, uint16_t* h, cudaStream_t s, bool pdl);
 
+// gemv_mxfp4_mma.cu — gate/up SwiGLU with the multiply-adds on mma.sync, m in
+// [2, 8], k <= 5120; otherwise cudaErrorInvalidConfiguration (nothing launched)
+cudaError_t launch_swiglu_mxfp4_mma(const uint8_t* packed, int n, int k, const uint16_t* x,
+                                    int m, uint16_t* h, cudaStream_t s, bool pdl);
+
 // tc_swiglu.cu — tcgen05 gate/up SwiGLU, m in [1, 64] (the library sends
 // m >= 4), k % 64 == 0; a plan that does not fit: cudaErrorInvalidConfiguration
 cudaError_t launch_swiglu_mxfp4_tc(const uint8_t* packed, int n, int k, const uint16_t* x,

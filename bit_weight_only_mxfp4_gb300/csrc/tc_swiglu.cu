@@ -21,9 +21,8 @@
 // 2^(X_block - X_row) where X_row is the row's largest block exponent (so the
 // f16 values stay in range and exact), stored in the swizzled layout; and
 // converts its share of the x tile to f16 after an exact power-of-two
-// prescale per x row that lifts a row whose first k-tile stays below 1 to
-// [1, 2) (a scaled value beyond 65504 raises TT_ERR_UNSUPPORTED in the
-// device error word).
+// prescale per x row that puts the row's largest |x| (over all of K, read
+// once per CTA) in [2^14, 2^15), so no finite input leaves f16's range.
 // Warp 17 brings each k-tile in with three TMA loads (gate codes 128 x 32 B,
 // up codes 128 x 32 B, both strided by the packed record size, and the x
 // tile, whose padding rows TMA fills with zeros) into a ring of raw slots.
@@ -67,7 +66,6 @@ constexpr int kTileK = 64;                      // f16: 128 bytes = one swizzle 
 #endif
 constexpr int kStages = TT_TC_STAGES;  // decoded A/B stages
 constexpr int kScaleBatch = 20;        // scale words per thread per load batch
-constexpr int kErrUnsupported = 5;              // TT_ERR_UNSUPPORTED
 
 // ---- tcgen05 / descriptor helpers ------------------------------------------
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
@@ -206,7 +204,8 @@ struct TcPlan {
 __global__ void __launch_bounds__(kThreads, 1)
     tc_swiglu_kernel(const __grid_constant__ CUtensorMap map_w,
                      const __grid_constant__ CUtensorMap map_x, const uint8_t* __restrict__ packed,
-                     int n, int k, int m, int nraw, uint16_t* __restrict__ h, int32_t* err) {
+                     const uint16_t* __restrict__ x, int n, int k, int m, int nraw,
+                     uint16_t* __restrict__ h, int32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   const SwigluRecord L(k);
   const TcPlan P(m, k, nraw);
@@ -370,31 +369,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = warp / kGroupWarps;
     const int t = threadIdx.x - g * kGroupWarps * 32, r = t & 127, part = t >> 7;
     const int xg = sxr[r], xu = sxr[kTileRows + r];
-    // An x row whose first k-tile stays below 1 in magnitude is scaled up by
-    // an exact power of two 2^sxs[i] that brings that tile's max to [1, 2),
-    // so that small activations keep their bits in f16; rows at or above 1
-    // are not scaled, and the epilogue divides the factor back out.
-    bool ok = mbar_wait_bounded(smem_u32(&raw_full[0]), 0u);
-    if (ok) {
-      const uint8_t* rw0 = base + P.off_raw;
-      for (int c = threadIdx.x; c < P.np * 8; c += kProdWarps * 32) {
-        const int row = c >> 3, piece = c & 7;
-        const uint4 v = *reinterpret_cast<const uint4*>(rw0 + 8192 + row * 128 + piece * 16);
-        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+    // Each x row gets the exact power-of-two prescale 2^sxs[i] that puts its
+    // largest |x| over the whole row in [2^14, 2^15): every finite value then
+    // fits f16 and keeps its bits down to 2^-28 of the row's max.  The
+    // producer warps scan x once (a warp per row, all of K) after the
+    // dependency wait; the epilogue divides the factor back out.
+    pdl_wait_prior_grid();  // x is produced by the previous kernel
+    {
+      const int nch = k >> 3;  // 16-byte chunks per row
+      for (int row = warp; row < P.np; row += kProdWarps) {
         float mx = 0.f;
+        if (row < m) {
+          const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * k);
+#pragma unroll 4
+          for (int c = lane; c < nch; c += 32) {
+            const uint4 v = xr[c];
+            const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(vw[e] & 0xFFFFu)),
-                               fabsf(bf16_bits_to_f32(vw[e] >> 16))));
-        atomicMax(&xmax[row], __float_as_uint(mx));  // non-negative: bits order as values
+            for (int e = 0; e < 4; ++e)
+              mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(vw[e] & 0xFFFFu)),
+                                   fabsf(bf16_bits_to_f32(vw[e] >> 16))));
+          }
+          mx = warp_max(mx);
+        }
+        if (lane == 0) xmax[row] = __float_as_uint(mx);
       }
     }
     producer_bar_sync();
     if (threadIdx.x < P.np) {
       const float mx = __uint_as_float(xmax[threadIdx.x]);
-      sxs[threadIdx.x] = mx > 0.f ? min(max(f16_prescale_exponent(mx) - 14, 0), 127) : 0;
+      sxs[threadIdx.x] = mx > 0.f ? min(f16_prescale_exponent(mx), 127) : 0;
     }
     producer_bar_sync();
+    bool ok = true;
     for (int kt = g; kt < nkt; kt += kGroups) {
       const int s = kt % kStages, d = kt % P.nraw;
       ok = mbar_wait_bounded(smem_u32(&raw_full[d]), uint32_t((kt / P.nraw) & 1));
@@ -453,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(hmul2(h0, f), hmul2(h1, f), hmul2(h2, f), hmul2(h3, f));
         }
       }
-      // x: bf16 * 2^sxs[row] -> f16 (scaled values beyond 65504 are flagged)
+      // x: bf16 * 2^sxs[row] -> f16, within range by the choice of sxs
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int c = t + j * kGroupWarps * 32;
@@ -462,15 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t vw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
           const float two_s = scalbnf(1.0f, xe[j]);
           uint32_t o[4];
-          bool big = false;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = bf16_bits_to_f32(vw[e] & 0xFFFFu) * two_s;  // exact
-            const float hi = bf16_bits_to_f32(vw[e] >> 16) * two_s;
-            big = big || fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
-            o[e] = pack_f16x2_scaled(lo, hi, 1.0f);
-          }
-          if (big) flag_error(err, kErrUnsupported);
+          for (int e = 0; e < 4; ++e)
+            o[e] = pack_f16x2_scaled(bf16_bits_to_f32(vw[e] & 0xFFFFu),
+                                     bf16_bits_to_f32(vw[e] >> 16), two_s);  // exact
           *reinterpret_cast<uint4*>(stage + 2 * P.a_bytes + sw128(row, piece)) =
               make_uint4(o[0], o[1], o[2], o[3]);
         }
@@ -601,7 +603,7 @@ cudaError_t launch_swiglu_mxfp4_tc(const uint8_t* packed, int n, int k, const ui
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, tc_swiglu_kernel, map_w, map_x, packed, n, k, m, nraw, h,
+  return cudaLaunchKernelEx(&cfg, tc_swiglu_kernel, map_w, map_x, packed, x, n, k, m, nraw, h,
                             di->error_word);
 }
 

@@ -122,10 +122,14 @@ def _swiglu_case(n, k, m, postscale=True, wid=92, layer=0):
     (37, 96, 1, True), (64, 32, 1, False), (129, 1024, 1, True), (300, 2880, 1, True),
     (50, 5120, 1, False), (33, 8192, 1, True), (21, 16384, 1, True),
     (77, 2048, 2, True), (77, 2048, 3, False),
-    # m = 4..8 with k % 64 != 0: CUDA cores
+    # m <= 8, k <= 5120: the mma.sync streaming kernel; 8-row tiles with
+    # ragged ends, n below one tile, fewer 32-blocks than consumer warps
     (31, 1056, 5, True), (37, 2080, 4, True), (29, 1120, 8, False),
-    # tcgen05 tensor-core path (m >= 4, k % 64 == 0); ragged row tiles
-    (45, 5120, 4, True), (40, 2880, 8, True), (19, 6144, 6, False),
+    (1, 2048, 1, True), (7, 64, 3, True), (9, 4096, 7, False), (17, 160, 1, True),
+    (45, 5120, 4, True), (40, 2880, 8, True), (8, 5120, 6, True),
+    # m = 4..8 with k > 5120: tcgen05 (k % 64 == 0) or CUDA-core FMA kernels
+    (19, 6144, 6, False), (23, 5152, 5, True), (13, 6176, 2, True),
+    # tcgen05 tensor-core path (m >= 9, k % 64 == 0); ragged row tiles
     (128, 128, 16, True), (130, 2048, 16, True), (300, 2880, 32, False), (256, 5120, 64, True),
     (77, 1024, 9, True), (129, 4096, 40, True), (1000, 768, 63, True),
 ])
@@ -211,28 +215,56 @@ def test_tensor_path_rejects_k_not_multiple_of_64():
     assert e.value.status == 5  # TT_ERR_UNSUPPORTED, nothing launched
 
 
-@pytest.mark.parametrize("m", [5, 16])
-def test_tensor_path_flags_activations_beyond_f16_range(m):
-    """The tensor path (m >= 4 with k % 64 == 0) converts x to f16 for the
-    MMA: an activation beyond f16's range is reported through the device
-    error word (no fault), and the next call is unaffected."""
-    n, k = 128, 256
-    h, ref, packed, d = _swiglu_case(n, k, m, True)
-    assert_float_parity(h, ref, "before")
-    assert gu.device_error() == 0
+@pytest.mark.parametrize("m", [9, 16, 64])
+def test_tensor_path_serves_activations_beyond_f16_range(m):
+    """The tensor path (m >= 9 with k % 64 == 0) converts x to f16 for the MMA
+    after an exact power-of-two prescale taken from each x row's largest
+    value over all of K: an activation beyond f16's range, in a late k-tile,
+    is served exactly (no flag), row by row."""
+    n, k = 128, 1024
+    d = synth.gate_up_inputs(98, 0, n, k, m=m)
     x = d["x"].copy()
-    x[3, 17] = synth.f32_to_bf16_bits(np.array([1.0e5], np.float32))[0]
-    gu.swiglu(packed, n, k, x)
-    assert gu.device_error() == 5   # TT_ERR_UNSUPPORTED; reading clears the word
+    x[min(3, m - 1), 900] = synth.f32_to_bf16_bits(np.array([1.0e5], np.float32))[0]
+    x[0, 17] = synth.f32_to_bf16_bits(np.array([-3.0e9], np.float32))[0]
+    gc, gs, _ = gu.quantize(d["wg"])
+    uc, us, _ = gu.quantize(d["wu"])
+    packed = gu.pack_swiglu(gc, gs, gu.dev(d["pg"]), uc, us, gu.dev(d["pu"]), n, k)
+    h = gu.swiglu(packed, n, k, x)
     assert gu.device_error() == 0
-    h2 = gu.swiglu(packed, n, k, d["x"])
-    assert np.array_equal(h2, h)
+    ref = oracle.mxfp4_swiglu_matvec((gu.host(gc), gu.host(gs), d["pg"]),
+                                     (gu.host(uc), gu.host(us), d["pu"]), x)
+    for i in range(m):
+        assert_float_parity(h[i], ref[i], f"row {i}")
+
+
+@pytest.mark.parametrize("m", [4, 16])
+def test_outlier_activation_row(m):
+    """A realistic hidden-state outlier: one activation 10^4 times its row's
+    median magnitude, in the last k-tile of an otherwise quiet row, on the
+    path m takes at the Phi-4 K (m = 4: mma.sync streaming kernel; m = 16:
+    tcgen05)."""
+    n, k = 96, 5120
+    d = synth.gate_up_inputs(99, 0, n, k, m=m)
+    xf = synth.bf16_bits_to_f32(d["x"]).copy()
+    med = np.median(np.abs(xf[1]))
+    xf[1, k - 5] = np.float32(1.0e4 * med)
+    x = synth.f32_to_bf16_bits(xf)
+    gc, gs, _ = gu.quantize(d["wg"])
+    uc, us, _ = gu.quantize(d["wu"])
+    packed = gu.pack_swiglu(gc, gs, gu.dev(d["pg"]), uc, us, gu.dev(d["pu"]), n, k)
+    h = gu.swiglu(packed, n, k, x)
+    assert gu.device_error() == 0
+    ref = oracle.mxfp4_swiglu_matvec((gu.host(gc), gu.host(gs), d["pg"]),
+                                     (gu.host(uc), gu.host(us), d["pu"]), x)
+    for i in range(m):
+        assert_float_parity(h[i], ref[i], f"row {i}")
 
 
 def test_tensor_path_small_activations_keep_precision():
-    """The tensor path lifts an x row whose first k-tile stays below 1 by an
-    exact power of two before the f16 conversion, so rows of tiny activations
-    (which f16 alone would flush) match the oracle row by row."""
+    """The tensor path scales each x row by an exact power of two before the
+    f16 conversion, so rows of tiny activations (which f16 alone would flush)
+    match the oracle row by row, also where the first k-tile is far below
+    the rest of the row."""
     n, k, m = 160, 1024, 16
     d = synth.gate_up_inputs(95, 0, n, k, m=m)
     xf = synth.bf16_bits_to_f32(d["x"]).copy()
@@ -282,11 +314,12 @@ def test_swiglu_m1_blocks_of_very_different_magnitude(k):
     assert_float_parity(h, ref, f"block magnitudes 2^-60..2^60, k={k}")
 
 
-def test_cuda_cores_serve_large_activations_where_k_is_not_a_multiple_of_64():
-    """m = 5 with k % 64 != 0 stays on the CUDA cores, whose prescale is taken
-    from the data itself: an activation of 1e5 is served exactly, with no
-    flag (the tensor path would flag it)."""
-    n, k, m = 96, 1056, 5
+@pytest.mark.parametrize("k", [1056, 2048])
+def test_small_batches_serve_large_activations(k):
+    """m = 5 runs on the streaming kernels, whose prescale is taken from the
+    data itself per 32-block: an activation of 1e5 is served exactly, with no
+    flag."""
+    n, m = 96, 5
     d = synth.gate_up_inputs(97, 0, n, k, m=m)
     x = d["x"].copy()
     x[3, 17] = synth.f32_to_bf16_bits(np.array([1.0e5], np.float32))[0]
