@@ -276,11 +276,11 @@ def cpu_baseline(target_s: float = 8.0):
 # capture of the current kernel on the same shape (K = 2048, N = 11008, m = 1);
 # set an entry back to None whenever its kernel changes.
 DRAM_TRAFFIC = {
-    "swiglu_mxfp4_mma_kernel": None,
+    "swiglu_mxfp4_m1x_kernel": 24156160,
     "swiglu_bf16_kernel": 92261376,
 }
 # The kernel that serves the batch-1 MXFP4 gate/up layer at K = 2048.
-MXFP4_M1_KERNEL = "swiglu_mxfp4_mma_kernel"
+MXFP4_M1_KERNEL = "swiglu_mxfp4_m1x_kernel"
 NOMINAL_HBM_GBS = 8000.0
 
 
@@ -583,9 +583,10 @@ def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
 
 
 def secondary_sweep(torch, synth, loader, thinmx, device, hbm, reps=20, ms=None):
-    """Phi-4 gate/up (K=5120, N=17920) over the batch sizes: the streaming
-    kernel with mma.sync multiply-adds for m <= 8, the tcgen05 tensor-core
-    kernel above; weight copies > 2x L2."""
+    """Phi-4 gate/up (K=5120, N=17920) over the batch sizes: the CUDA-core
+    streaming kernel at m = 1, the tile kernel with mma.sync multiply-adds
+    for m = 2..8, the tcgen05 tensor-core kernel above; weight copies > 2x
+    L2."""
     tensor_peak = tensor_peak_tflops()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     s = synth.SWEEP
@@ -608,12 +609,14 @@ def secondary_sweep(torch, synth, loader, thinmx, device, hbm, reps=20, ms=None)
         ms = time_graph(torch, g, reps) / copies
         b = gate_up_bytes(s.n, s.k, m)
         tflops = 4 * m * s.n * s.k / (ms * 1e-3) / 1e12
-        tc = m > 8  # the library's dispatch at this size (k = 5120)
+        # the library's dispatch at this size (k = 5120)
+        path = ("tcgen05 kind::f16" if m > 8 else
+                "mma.sync tile kernel" if m >= 2 else "cuda-core streaming (FMA)")
         sweep[str(m)] = {"us": round(ms * 1e3, 3), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
                          "frac": round(b / (ms * 1e-3) / 1e9 / hbm, 4),
                          "TFLOPs": round(tflops, 2),
-                         "path": "tcgen05 kind::f16" if tc else "streaming + mma.sync"}
-        if tc:  # against the dense f16/bf16 tensor peak as well
+                         "path": path}
+        if m > 8:  # against the dense f16/bf16 tensor peak as well
             sweep[str(m)]["tensor_frac"] = round(tflops / tensor_peak, 4)
         del g
     del packs, base
