@@ -656,25 +656,21 @@ def moe_workload(torch, synth, loader, thinmx, device, hbm, reps=20, layers=None
     (~10 GB, far beyond L2)."""
     c = synth.MOE
     H, I, E, K = c.hidden, c.inter, c.experts, c.top_k
-    sw = thinmx.tt_mxfp4_swiglu_packed_bytes(I, H)
-    rw = thinmx.tt_mxfp4_rows_packed_bytes(H, I)
     n_layers = layers or c.layers
     layers = []
     for l in range(n_layers):
-        gu = torch.empty(E * sw, dtype=torch.uint8, device=device)
-        dn = torch.empty(E * rw, dtype=torch.uint8, device=device)
-        for e in range(E):
-            w = synth.torch_normal((2 * I, H), synth.WEIGHT_STD, c.wid, l, 100 + 2 * e, device)
-            gc, gs = loader.quantize_mxfp4(w)
-            thinmx.tt_mxfp4_pack_swiglu(gc[:I], gs[:I], None, gc[I:], gs[I:], None, I, H,
-                                        gu[e * sw:], sw)
-            w = synth.torch_normal((H, I), synth.WEIGHT_STD, c.wid, l, 101 + 2 * e, device)
-            dc, ds = loader.quantize_mxfp4(w)
-            thinmx.tt_mxfp4_pack_rows(dc, ds, H, I, dn[e * rw:], rw)
-            del w, gc, gs, dc, ds
+        gbufs, dbufs = [], []
+        for e in range(E):  # every expert in buffers of its own
+            wgu = synth.torch_normal((2 * I, H), synth.WEIGHT_STD, c.wid, l, 100 + 2 * e, device)
+            wdn = synth.torch_normal((H, I), synth.WEIGHT_STD, c.wid, l, 101 + 2 * e, device)
+            g, d = loader.moe_expert_from_f32(wgu, wdn)
+            gbufs.append(g)
+            dbufs.append(d)
+            del wgu, wdn
         wr = synth.torch_normal((E, H), synth.WEIGHT_STD, c.wid, l, 1, device).to(torch.bfloat16)
         x = synth.torch_normal((H,), 1.0, c.wid, l, 0, device).to(torch.bfloat16)
-        layers.append((gu, dn, wr, x))
+        layers.append((loader.expert_table(gbufs), loader.expert_table(dbufs), wr, x,
+                       (gbufs, dbufs)))
     out = torch.empty(H, dtype=torch.bfloat16, device=device)
     idx = torch.empty(K, dtype=torch.int32, device=device)
     prob = torch.empty(K, dtype=torch.float32, device=device)
@@ -683,8 +679,8 @@ def moe_workload(torch, synth, loader, thinmx, device, hbm, reps=20, layers=None
     torch.cuda.synchronize()
 
     def step():
-        for gu, dn, wr, x in layers:
-            thinmx.tt_moe_mxfp4_topk_mlp(x, H, I, wr, E, K, gu, dn, out, idx, prob, ws, wsb)
+        for gt, dt, wr, x, _ in layers:
+            thinmx.tt_moe_mxfp4_topk_mlp(x, H, I, wr, E, K, gt, dt, out, idx, prob, ws, wsb)
 
     g = capture(torch, step)
     ms = time_graph(torch, g, reps) / n_layers

@@ -219,7 +219,7 @@ size_t tt_moe_workspace_bytes(int64_t hidden, int64_t inter, int32_t n_experts, 
 
 tt_status tt_moe_mxfp4_topk_mlp(const uint16_t* x_bf16, int64_t hidden, int64_t inter,
                                 const uint16_t* router_w_bf16, int32_t n_experts, int32_t top_k,
-                                const void* gate_up_packed, const void* down_packed,
+                                const void* const* gate_up_packed, const void* const* down_packed,
                                 uint16_t* out_bf16, int32_t* out_idx, float* out_prob,
                                 void* workspace, size_t workspace_bytes, void* stream) {
   if (hidden < 32 || hidden % 32 != 0 || hidden > kMoeMaxHidden) return TT_ERR_SHAPE;
@@ -231,22 +231,23 @@ tt_status tt_moe_mxfp4_topk_mlp(const uint16_t* x_bf16, int64_t hidden, int64_t 
     return TT_ERR_NULL;
   if (workspace_bytes < tt_moe_workspace_bytes(hidden, inter, n_experts, top_k))
     return TT_ERR_SIZE;
-  if (!aligned(x_bf16, 16) || !aligned(router_w_bf16, 16) || !aligned(gate_up_packed, 16) ||
-      !aligned(down_packed, 16) || !aligned(out_bf16, 2) || !aligned(out_idx, 4) ||
+  if (!aligned(x_bf16, 16) || !aligned(router_w_bf16, 16) || !aligned(gate_up_packed, 8) ||
+      !aligned(down_packed, 8) || !aligned(out_bf16, 2) || !aligned(out_idx, 4) ||
       !aligned(out_prob, 4) || !aligned(workspace, 16))
     return TT_ERR_ALIGN;
   const cudaError_t e = tt::launch_moe(
       x_bf16, int(hidden), int(inter), router_w_bf16, int(n_experts), int(top_k),
-      static_cast<const uint8_t*>(gate_up_packed), static_cast<const uint8_t*>(down_packed),
-      out_bf16, out_idx, out_prob, workspace, as_stream(stream), kPdl);
+      reinterpret_cast<const uint8_t* const*>(gate_up_packed),
+      reinterpret_cast<const uint8_t* const*>(down_packed), out_bf16, out_idx, out_prob,
+      workspace, as_stream(stream), kPdl);
   if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
   return from_cuda(e);
 }
 
 tt_status tt_moe_mxfp4_topk_mlp_static(const uint16_t* x_bf16, int64_t hidden, int64_t inter,
                                        const uint16_t* router_w_bf16, int32_t n_experts,
-                                       int32_t top_k, const void* gate_up_packed,
-                                       const void* down_packed, uint16_t* out_bf16,
+                                       int32_t top_k, const void* const* gate_up_packed,
+                                       const void* const* down_packed, uint16_t* out_bf16,
                                        int32_t* out_idx, float* out_prob, void* stream) {
   if (hidden < 32 || hidden % 32 != 0 || hidden > kMoeMaxHidden) return TT_ERR_SHAPE;
   if (inter < 32 || inter % 32 != 0 || inter > 8192) return TT_ERR_SHAPE;
@@ -256,8 +257,8 @@ tt_status tt_moe_mxfp4_topk_mlp_static(const uint16_t* x_bf16, int64_t hidden, i
   if (!x_bf16 || !router_w_bf16 || !gate_up_packed || !down_packed || !out_bf16 || !out_idx ||
       !out_prob)
     return TT_ERR_NULL;
-  if (!aligned(x_bf16, 16) || !aligned(router_w_bf16, 16) || !aligned(gate_up_packed, 16) ||
-      !aligned(down_packed, 16) || !aligned(out_bf16, 2) || !aligned(out_idx, 4) ||
+  if (!aligned(x_bf16, 16) || !aligned(router_w_bf16, 16) || !aligned(gate_up_packed, 8) ||
+      !aligned(down_packed, 8) || !aligned(out_bf16, 2) || !aligned(out_idx, 4) ||
       !aligned(out_prob, 4))
     return TT_ERR_ALIGN;
   void* scratch = nullptr;
@@ -266,9 +267,9 @@ tt_status tt_moe_mxfp4_topk_mlp_static(const uint16_t* x_bf16, int64_t hidden, i
   if (e != cudaSuccess) return from_cuda(e);
   if (scratch_bytes < tt_moe_workspace_bytes(hidden, inter, n_experts, top_k)) return TT_ERR_SIZE;
   e = tt::launch_moe(x_bf16, int(hidden), int(inter), router_w_bf16, int(n_experts), int(top_k),
-                     static_cast<const uint8_t*>(gate_up_packed),
-                     static_cast<const uint8_t*>(down_packed), out_bf16, out_idx, out_prob,
-                     scratch, as_stream(stream), kPdl);
+                     reinterpret_cast<const uint8_t* const*>(gate_up_packed),
+                     reinterpret_cast<const uint8_t* const*>(down_packed), out_bf16, out_idx,
+                     out_prob, scratch, as_stream(stream), kPdl);
   if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
   return from_cuda(e);
 }

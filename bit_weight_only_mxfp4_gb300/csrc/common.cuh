@@ -16,6 +16,8 @@ namespace tt {
 // Error reporting from device code.  Kernels get a pointer to the library's
 // device error word; the first error code written wins.
 // ---------------------------------------------------------------------------
+constexpr int kErrNull = 1;     // TT_ERR_NULL
+constexpr int kErrAlign = 3;    // TT_ERR_ALIGN
 constexpr int kErrTimeout = 7;  // TT_ERR_TIMEOUT
 
 __device__ __forceinline__ void flag_error(int32_t* word, int code) {

@@ -66,13 +66,15 @@ cudaError_t launch_int4_matvec(const uint8_t* codes, const uint16_t* scales, con
 // shared memory: cudaErrorInvalidConfiguration
 size_t moe_workspace_bytes(int64_t hidden, int64_t inter, int n_experts, int top_k);
 size_t moe_fused_workspace_bytes(int64_t hidden);
+// gu, dn: device arrays of E device pointers (one packed buffer per expert)
 cudaError_t launch_moe(const uint16_t* x, int hidden, int inter, const uint16_t* wr, int E,
-                       int top_k, const uint8_t* gu, const uint8_t* dn, uint16_t* out,
-                       int32_t* out_idx, float* out_prob, void* ws, cudaStream_t s, bool pdl);
+                       int top_k, const uint8_t* const* gu, const uint8_t* const* dn,
+                       uint16_t* out, int32_t* out_idx, float* out_prob, void* ws,
+                       cudaStream_t s, bool pdl);
 cudaError_t launch_moe_fused(const uint16_t* x, int hidden, int inter, const uint16_t* wr, int E,
-                             int top_k, const uint8_t* gu, const uint8_t* dn, uint16_t* out,
-                             int32_t* out_idx, float* out_prob, void* ws, cudaStream_t s,
-                             bool pdl);
+                             int top_k, const uint8_t* const* gu, const uint8_t* const* dn,
+                             uint16_t* out, int32_t* out_idx, float* out_prob, void* ws,
+                             cudaStream_t s, bool pdl);
 // The library-owned MoE scratch (a static device array) of the current
 // device: its address (looked up on the first call on each device) and size.
 constexpr int kMoeStaticMaxHidden = 4096;  // hidden limit of the static scratch

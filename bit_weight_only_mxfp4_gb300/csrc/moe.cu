@@ -23,8 +23,9 @@ size_t moe_workspace_bytes(int64_t hidden, int64_t inter, int n_experts, int top
 }
 
 cudaError_t launch_moe(const uint16_t* x, int hidden, int inter, const uint16_t* wr, int E,
-                       int top_k, const uint8_t* gu, const uint8_t* dn, uint16_t* out,
-                       int32_t* out_idx, float* out_prob, void* ws, cudaStream_t s, bool pdl) {
+                       int top_k, const uint8_t* const* gu, const uint8_t* const* dn,
+                       uint16_t* out, int32_t* out_idx, float* out_prob, void* ws,
+                       cudaStream_t s, bool pdl) {
   return launch_moe_fused(x, hidden, inter, wr, E, top_k, gu, dn, out, out_idx, out_prob, ws, s,
                           pdl);
 }

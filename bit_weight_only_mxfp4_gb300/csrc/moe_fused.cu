@@ -69,7 +69,7 @@ struct MoePlan {
   int item;     // bytes of a down item slot: rc * 8 codes + rc scales
   int dslots;   // down item slots
   // shared-memory offsets
-  int bars, misc, hs, xs, dring, gring, total;
+  int bars, misc, tab, hs, xs, dring, gring, total;
 };
 
 __host__ __device__ inline int align128(int o) { return (o + 127) & ~127; }
@@ -80,6 +80,9 @@ __host__ __device__ inline void plan_offsets(MoePlan& p, int hidden, int gu_rec_
   o += (kFWarps * kMaxGuSlots + kMaxDSlots + kMaxSlices) * 8;
   p.misc = o;  // reductions, top-k, flags, per-slot consumer counts
   o += (2 * kFWarps + 2 * kMaxTopK + kMaxExperts + 4 + kMaxDSlots) * 4;
+  o = (o + 7) & ~7;
+  p.tab = o;  // the experts' gate/up and down pointers
+  o += 2 * kMaxExperts * 8;
   p.hs = o;
   o += p.nhb_max * 16 * 4;
   o = align128(o);
@@ -172,6 +175,10 @@ __device__ __forceinline__ float2 ld_relaxed_f2(const float2* p) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ void st_relaxed_f2(float2* p, float2 v) {
+  asm volatile("st.relaxed.gpu.global.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(v.x), "f"(v.y)
+               : "memory");
+}
 // Polls `n` partials until every one has been written (bounded in time).
 __device__ bool poll_partials(const float2* p, int n, float2* v) {
   const uint64_t t0 = globaltimer_ns();
@@ -236,8 +243,9 @@ template <int NBG>
 __global__ void __launch_bounds__(kFThreads, 1)
     moe_fused_kernel(const uint16_t* __restrict__ x, int hidden, int inter,
                      const uint16_t* __restrict__ wr, int E, int top_k,
-                     const uint8_t* __restrict__ gate_up, const uint8_t* __restrict__ down,
-                     uint16_t* __restrict__ out, int32_t* __restrict__ out_idx,
+                     const uint8_t* const* __restrict__ gu_tab,
+                     const uint8_t* const* __restrict__ dn_tab, uint16_t* __restrict__ out,
+                     int32_t* __restrict__ out_idx,
                      float* __restrict__ out_prob, uint8_t* __restrict__ ws, int split,
                      MoePlan P, int32_t* err) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -267,6 +275,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
   uint4* xs = reinterpret_cast<uint4*>(smem + P.xs);
   uint8_t* dring = smem + P.dring;
   uint8_t* gring = smem + P.gring;
+  const uint8_t** tab_g = reinterpret_cast<const uint8_t**>(smem + P.tab);  // [E]
+  const uint8_t** tab_d = tab_g + kMaxExperts;                             // [E]
 
   const int nch = hidden >> 3;
   const int HB = top_k * inter / 16;
@@ -275,8 +285,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
   const int hb0 = hb_lo(c), hb1 = hb_lo(c + 1);
   const int nhb = hb1 - hb0;  // rounds: every warp computes one record per round
   const int qa = hb0 * 16;
-  const int64_t gu_stride = (int64_t)inter * Lg.bytes;
-  const int64_t dn_stride = Ld.bytes;
   const int T = E * split;
   const int cs = (nch + split - 1) / split;
   const uint64_t policy = l2_evict_first_policy();
@@ -293,6 +301,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
       *d_issued = 0;
     }
     fence_mbar_init();
+  }
+  // The expert tables, like the weights, are not written by the previous
+  // kernel: copy them in while that kernel finishes.
+  for (int e = threadIdx.x; e < E; e += kFThreads) {
+    tab_g[e] = gu_tab[e];
+    tab_d[e] = dn_tab[e];
   }
   // Router weights do not depend on the previous kernel: warm L2 with this
   // CTA's slices while that kernel finishes.
@@ -352,7 +366,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     for (int w = 1; w < wused; ++w) comp_merge(ts, tc, red_s[w], red_c[w]);
     // one copy per CTA, so that no L2 line is read by every SM below
     const float2 pv = make_float2(nonzero_bits(ts), nonzero_bits(tc));
-    for (int r = threadIdx.x; r < G; r += kFThreads) part[(size_t)r * T + t] = pv;
+    for (int r = threadIdx.x; r < G; r += kFThreads) st_relaxed_f2(part + (size_t)r * T + t, pv);
     __syncthreads();
   }
 
@@ -406,7 +420,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         got = poll_partials(mine + (size_t)e * split, split, v) && got;
 #pragma unroll
         for (int p = 0; p < kMaxRouterSplit; ++p)
-          if (p < split) mine[(size_t)e * split + p] = make_float2(0.f, 0.f);
+          if (p < split) st_relaxed_f2(mine + (size_t)e * split + p, make_float2(0.f, 0.f));
         float s = v[0].x, cc = v[0].y;
 #pragma unroll
         for (int p = 1; p < kMaxRouterSplit; ++p)
@@ -427,6 +441,22 @@ __global__ void __launch_bounds__(kFThreads, 1)
   if (*sflag == 0) {  // nothing of ours is in flight yet
     if (threadIdx.x == 0) flag_error(err, kErrTimeout);
     return;
+  }
+  // The selected experts' buffers must be usable by the bulk copies: a null
+  // or misaligned pointer is reported (every CTA decides alike) and nothing
+  // is copied from it.
+  {
+    int bad = 0;
+    for (int j = 0; j < top_k; ++j) {
+      const uintptr_t a = reinterpret_cast<uintptr_t>(tab_g[sidx[j]]);
+      const uintptr_t b = reinterpret_cast<uintptr_t>(tab_d[sidx[j]]);
+      if (a == 0 || b == 0) bad = bad ? bad : kErrNull;
+      else if ((a | b) & 15u) bad = bad ? bad : kErrAlign;
+    }
+    if (bad) {
+      if (threadIdx.x == 0) flag_error(err, bad);
+      return;
+    }
   }
   if (c == 0 && threadIdx.x < top_k) {
     out_idx[threadIdx.x] = sidx[threadIdx.x];
@@ -452,7 +482,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const uint32_t bar = smem_u32(&wbars[sl]);
     mbar_arrive_expect_tx(bar, uint32_t(Lg.bytes));
     bulk_g2s(smem_u32(wbase + (size_t)sl * Lg.bytes),
-             gate_up + (int64_t)sidx[j] * gu_stride + (int64_t)r * Lg.bytes, uint32_t(Lg.bytes),
+             tab_g[sidx[j]] + (int64_t)r * Lg.bytes, uint32_t(Lg.bytes),
              bar, policy);
   };
   auto issue_dn = [&](int k) {  // one thread: down item k -> slot k % dslots
@@ -462,7 +492,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const int s = k % P.dslots;
     const uint32_t bar = smem_u32(&dbars[s]);
     uint8_t* dst = dring + (size_t)s * P.item;
-    const uint8_t* src = down + (int64_t)sidx[j] * dn_stride;
+    const uint8_t* src = tab_d[sidx[j]];
     mbar_arrive_expect_tx(bar, uint32_t(nr * 9));
     bulk_g2s(smem_u32(dst), src + Ld.code_at(sl, r0), uint32_t(nr * 8), bar, policy);
     bulk_g2s(smem_u32(dst + (size_t)P.rc * 8), src + Ld.scale_at(sl >> 1, r0), uint32_t(nr), bar,
@@ -676,7 +706,8 @@ size_t moe_fused_workspace_bytes(int64_t hidden) {
 }
 
 cudaError_t launch_moe_fused(const uint16_t* x, int hidden, int inter, const uint16_t* wr, int E,
-                             int top_k, const uint8_t* gu, const uint8_t* dn, uint16_t* out,
+                             int top_k, const uint8_t* const* gu, const uint8_t* const* dn,
+                             uint16_t* out,
                              int32_t* out_idx, float* out_prob, void* ws, cudaStream_t s,
                              bool pdl) {
   const DeviceInfo* di = device_info();

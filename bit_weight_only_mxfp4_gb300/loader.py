@@ -37,3 +37,26 @@ def mxfp4_gate_up_from_f32(wg: torch.Tensor, wu: torch.Tensor, pg=None, pu=None)
     packed = pack_swiglu((gc, gs, pg), (uc, us, pu), n, k)
     del gc, gs, uc, us
     return packed
+
+
+def expert_table(buffers) -> torch.Tensor:
+    """The device array of expert buffer addresses the MoE entry points take
+    (one int64 per expert, in expert order).  The buffers must stay alive as
+    long as the table is used."""
+    dev = buffers[0].device
+    return torch.tensor([b.data_ptr() for b in buffers], dtype=torch.int64, device=dev)
+
+
+def moe_expert_from_f32(w_gate_up: torch.Tensor, w_down: torch.Tensor):
+    """One expert's fp32 gate/up [2*inter, hidden] (gate rows first) and down
+    [hidden, inter] matrices -> its own packed gate/up and down buffers."""
+    two_i, hidden = w_gate_up.shape
+    inter = two_i // 2
+    gc, gs = quantize_mxfp4(w_gate_up)
+    gu = pack_swiglu((gc[:inter], gs[:inter], None), (gc[inter:], gs[inter:], None), inter,
+                     hidden)
+    dc, ds = quantize_mxfp4(w_down)
+    nbytes = thinmx.tt_mxfp4_rows_packed_bytes(hidden, inter)
+    dn = torch.empty(nbytes, dtype=torch.uint8, device=w_down.device)
+    thinmx.tt_mxfp4_pack_rows(dc, ds, hidden, inter, dn, nbytes)
+    return gu, dn

@@ -55,6 +55,15 @@
  *   - Alignment: every device pointer 16 bytes, except the per-row vectors
  *     (postscales, scales_f16, zero points, status words) which need their
  *     natural alignment.
+ *   - Weights (and the MoE expert tables) are read before a call waits for
+ *     the preceding kernel on its stream (programmatic dependent launch), so
+ *     that their streaming overlaps that kernel's tail: the kernel launched
+ *     just before a call must not write them.  Activations and outputs are
+ *     touched only after the wait.
+ *   - The library caches per-device state on first use (the device error
+ *     word's address, the fixed MoE scratch's address, kernel attributes).
+ *     A device reset (cudaDeviceReset) invalidates it: do not call the
+ *     library on a device after resetting that device in the same process.
  */
 #ifndef THINMX_H
 #define THINMX_H
@@ -191,10 +200,18 @@ tt_status tt_mxfp4_pack_rows(const uint8_t* codes, const uint8_t* scales, int64_
  *              index; p = softmax of their logits
  *   h_j      = silu(Wg[idx_j] x) * (Wu[idx_j] x)          (fp32, inter)
  *   out      = bf16_rne( sum_j p_j * Wd[idx_j] h_j )      (hidden)
- * Experts are stacked: gate_up_packed holds E buffers of
- * tt_mxfp4_swiglu_packed_bytes(inter, hidden) bytes (gate = the swiglu gate
- * rows, packed without postscales); down_packed holds E buffers of
- * tt_mxfp4_rows_packed_bytes(hidden, inter) bytes.  router_w_bf16 [E][hidden].
+ * Experts live in buffers of their own: gate_up_packed and down_packed are
+ * DEVICE arrays of n_experts DEVICE pointers (8-byte aligned arrays), entry
+ * e pointing to expert e's tt_mxfp4_swiglu_packed_bytes(inter, hidden)-byte
+ * gate/up buffer (gate = the swiglu gate rows, packed without postscales)
+ * and its tt_mxfp4_rows_packed_bytes(hidden, inter)-byte down buffer, each
+ * 16-byte aligned.  Only the selected experts' entries are read; a selected
+ * entry that is NULL or misaligned is reported through the device error
+ * word (TT_ERR_NULL / TT_ERR_ALIGN, tt_device_error_read) and nothing is
+ * read from it or written to out.  The tables, like every weight buffer of
+ * this library, are read before the call waits for the preceding kernel on
+ * the stream (programmatic dependent launch): that kernel must not write
+ * them.  router_w_bf16 [E][hidden].
  * out_idx int32 [top_k], out_prob fp32 [top_k] (device).  workspace: device,
  * >= tt_moe_workspace_bytes(...) bytes, 16-byte aligned, ZERO-FILLED before
  * its first use (e.g. cudaMemsetAsync once after allocating it); the call
@@ -218,7 +235,7 @@ tt_status tt_mxfp4_pack_rows(const uint8_t* codes, const uint8_t* scales, int64_
 size_t tt_moe_workspace_bytes(int64_t hidden, int64_t inter, int32_t n_experts, int32_t top_k);
 tt_status tt_moe_mxfp4_topk_mlp(const uint16_t* x_bf16, int64_t hidden, int64_t inter,
                                 const uint16_t* router_w_bf16, int32_t n_experts, int32_t top_k,
-                                const void* gate_up_packed, const void* down_packed,
+                                const void* const* gate_up_packed, const void* const* down_packed,
                                 uint16_t* out_bf16, int32_t* out_idx, float* out_prob,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
@@ -246,8 +263,8 @@ tt_status tt_moe_mxfp4_topk_mlp(const uint16_t* x_bf16, int64_t hidden, int64_t 
 #define TT_MOE_STATIC_MAX_HIDDEN 4096
 tt_status tt_moe_mxfp4_topk_mlp_static(const uint16_t* x_bf16, int64_t hidden, int64_t inter,
                                        const uint16_t* router_w_bf16, int32_t n_experts,
-                                       int32_t top_k, const void* gate_up_packed,
-                                       const void* down_packed, uint16_t* out_bf16,
+                                       int32_t top_k, const void* const* gate_up_packed,
+                                       const void* const* down_packed, uint16_t* out_bf16,
                                        int32_t* out_idx, float* out_prob, void* stream);
 
 /* ------------------------------------------------------------------------

@@ -56,30 +56,38 @@ def device_error():
 
 
 def build_moe_experts(gu_list, dn_list, hidden, inter):
-    """fp32 expert matrices (numpy) -> stacked packed device buffers for the
-    MoE call, plus the canonical codes/scales (host) for the oracle."""
+    """fp32 expert matrices (numpy) -> one packed gate/up and one packed down
+    buffer per expert (separate allocations) and the two device tables of
+    their addresses the MoE call takes, plus the canonical codes/scales
+    (host) for the oracle.  Returns (gu_table, dn_table, canonical, buffers);
+    the buffers must outlive every call that uses the tables."""
     import torch
+    from bit_weight_only_mxfp4_gb300 import loader
     E = len(gu_list)
     sw = thinmx.tt_mxfp4_swiglu_packed_bytes(inter, hidden)
     rw = thinmx.tt_mxfp4_rows_packed_bytes(hidden, inter)
-    gu_packed = torch.empty(E * sw, dtype=torch.uint8, device="cuda")
-    dn_packed = torch.empty(E * rw, dtype=torch.uint8, device="cuda")
     gc_h = np.zeros((E, 2 * inter, hidden // 2), np.uint8)
     gs_h = np.zeros((E, 2 * inter, hidden // 32), np.uint8)
     dc_h = np.zeros((E, hidden, inter // 2), np.uint8)
     ds_h = np.zeros((E, hidden, inter // 32), np.uint8)
+    gbufs, dbufs = [], []
     for e in range(E):
         gc, gs, _ = quantize(gu_list[e])
+        g = torch.empty(sw, dtype=torch.uint8, device="cuda")
         thinmx.tt_mxfp4_pack_swiglu(gc[:inter], gs[:inter], None, gc[inter:], gs[inter:], None,
-                                    inter, hidden, gu_packed[e * sw:], sw)
+                                    inter, hidden, g, sw)
         dc, ds, _ = quantize(dn_list[e])
-        thinmx.tt_mxfp4_pack_rows(dc, ds, hidden, inter, dn_packed[e * rw:], rw)
+        d = torch.empty(rw, dtype=torch.uint8, device="cuda")
+        thinmx.tt_mxfp4_pack_rows(dc, ds, hidden, inter, d, rw)
+        gbufs.append(g)
+        dbufs.append(d)
         gc_h[e], gs_h[e], dc_h[e], ds_h[e] = host(gc), host(gs), host(dc), host(ds)
     torch.cuda.synchronize()
-    return gu_packed, dn_packed, (gc_h, gs_h, dc_h, ds_h)
+    return (loader.expert_table(gbufs), loader.expert_table(dbufs), (gc_h, gs_h, dc_h, ds_h),
+            (gbufs, dbufs))
 
 
-def run_moe(x, wr, top_k, gu_packed, dn_packed, hidden, inter):
+def run_moe(x, wr, top_k, gu_table, dn_table, hidden, inter):
     import torch
     E = wr.shape[0]
     out = torch.empty(hidden, dtype=torch.int16, device="cuda")
@@ -87,7 +95,7 @@ def run_moe(x, wr, top_k, gu_packed, dn_packed, hidden, inter):
     prob = torch.empty(top_k, dtype=torch.float32, device="cuda")
     wsb = thinmx.tt_moe_workspace_bytes(hidden, inter, E, top_k)
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
-    thinmx.tt_moe_mxfp4_topk_mlp(dev(x), hidden, inter, dev(wr), E, top_k, gu_packed, dn_packed,
+    thinmx.tt_moe_mxfp4_topk_mlp(dev(x), hidden, inter, dev(wr), E, top_k, gu_table, dn_table,
                                  out, idx, prob, ws, wsb)
     torch.cuda.synchronize()
     return host(out, np.uint16), host(idx), host(prob)

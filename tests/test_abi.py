@@ -106,8 +106,8 @@ def test_moe_validation_before_launch(lib):
     assert ws >= 64 + 256 * 2880 * 4  # counters + one partial vector per CTA
     assert _st("tt_moe_workspace_bytes", 8224, 2880, 32, 4) == 0  # hidden beyond 8192
     assert _st("tt_moe_workspace_bytes", 2880, 2880, 4, 8) == 0   # top_k > n_experts
-    call = lambda H, I, E, K, x=A, wsp=A, wsb=ws: _st(
-        "tt_moe_mxfp4_topk_mlp", x, H, I, A, E, K, A, A, A, A, A, wsp, wsb, s)
+    call = lambda H, I, E, K, x=A, wsp=A, wsb=ws, tg=A, td=A: _st(
+        "tt_moe_mxfp4_topk_mlp", x, H, I, A, E, K, tg, td, A, A, A, wsp, wsb, s)
     assert call(2880, 2880, 32, 4, wsb=ws - 1) == 8          # workspace too small
     assert call(8224, 2880, 32, 4, wsb=1 << 30) == 2          # hidden beyond 8192
     assert call(2880, 8224, 32, 4, wsb=1 << 30) == 2          # inter beyond 8192
@@ -118,6 +118,8 @@ def test_moe_validation_before_launch(lib):
     assert call(2880, 2880, 32, 4, wsp=None) == 1
     assert call(2880, 2880, 32, 4, x=A + 8) == 3              # x not 16-byte aligned
     assert call(2880, 2880, 32, 4, wsp=A + 4) == 3            # workspace not 16-byte aligned
+    assert call(2880, 2880, 32, 4, tg=None) == 1              # no gate/up expert table
+    assert call(2880, 2880, 32, 4, td=A + 4) == 3             # expert table not 8-byte aligned
 
 
 def test_int4_validation_before_launch(lib):

@@ -30,7 +30,7 @@ def _case(E, H, I, K, wid, tie_rows=None):
         g, d = synth.moe_expert_weights(wid, 0, e, H, I)
         gus.append(g)
         dns.append(d)
-    gup, dnp, (gc, gs, dc, ds) = gu.build_moe_experts(gus, dns, H, I)
+    gup, dnp, (gc, gs, dc, ds), _bufs = gu.build_moe_experts(gus, dns, H, I)
     out, idx, prob = gu.run_moe(x, wr, K, gup, dnp, H, I)
     ref, ridx, rp, rlg, st = oracle.moe_mlp(x, wr, K, gc, gs, dc, ds)
     assert st == oracle.OK
@@ -91,7 +91,7 @@ def test_moe_workspace_reused_across_calls():
     from bit_weight_only_mxfp4_gb300 import thinmx
     E, H, I, K = 8, 320, 640, 4
     gus, dns = zip(*[synth.moe_expert_weights(41, 0, e, H, I) for e in range(E)])
-    gup, dnp, _ = gu.build_moe_experts(list(gus), list(dns), H, I)
+    gup, dnp, _, _bufs = gu.build_moe_experts(list(gus), list(dns), H, I)
     wsb = thinmx.tt_moe_workspace_bytes(H, I, E, K)
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
     sms = min(torch.cuda.get_device_properties(0).multi_processor_count, 256)
@@ -112,3 +112,69 @@ def test_moe_workspace_reused_across_calls():
         # the rest of the counter bytes and the router replicas (64 + 256 x 256 x 8 B)
         assert not gu.host(ws[16:524352]).any()
     assert gu.device_error() == 0
+
+
+def test_moe_experts_in_scattered_allocations():
+    """Experts are separate buffers at unrelated addresses: allocated in a
+    shuffled order with unused allocations between them, and the tables list
+    them in expert order."""
+    import torch
+    from bit_weight_only_mxfp4_gb300 import loader
+    E, H, I, K = 8, 320, 640, 4
+    r = synth.moe_router_inputs(43, 0, H, E)
+    gus, dns = zip(*[synth.moe_expert_weights(43, 0, e, H, I) for e in range(E)])
+    _, _, (gc, gs, dc, ds), (gb, db) = gu.build_moe_experts(list(gus), list(dns), H, I)
+    order = [5, 2, 7, 0, 3, 6, 1, 4]
+    moved_g, moved_d, gaps = [None] * E, [None] * E, []
+    for e in order:
+        gaps.append(torch.empty(4096 * (e + 1), dtype=torch.uint8, device="cuda"))
+        moved_g[e] = gb[e].clone()
+        gaps.append(torch.empty(256, dtype=torch.uint8, device="cuda"))
+        moved_d[e] = db[e].clone()
+    out, idx, prob = gu.run_moe(r["x"], r["wr"], K, loader.expert_table(moved_g),
+                                loader.expert_table(moved_d), H, I)
+    ref, ridx, rp, rlg, st = oracle.moe_mlp(r["x"], r["wr"], K, gc, gs, dc, ds)
+    assert list(idx) == list(ridx)
+    assert_float_parity(out, ref, "moe scattered experts")
+    assert gu.device_error() == 0
+
+
+def test_moe_bad_expert_pointer_is_reported_not_used():
+    """A NULL or misaligned table entry of a SELECTED expert is reported
+    through the device error word before any copy from it (the output is left
+    alone); a bad entry of an expert that is not selected is never read."""
+    import torch
+    from bit_weight_only_mxfp4_gb300 import loader, thinmx
+    E, H, I, K = 8, 256, 128, 2
+    r = synth.moe_router_inputs(44, 0, H, E)
+    gus, dns = zip(*[synth.moe_expert_weights(44, 0, e, H, I) for e in range(E)])
+    _, _, (gc, gs, dc, ds), (gb, db) = gu.build_moe_experts(list(gus), list(dns), H, I)
+    ref, ridx, rp, rlg, st = oracle.moe_mlp(r["x"], r["wr"], K, gc, gs, dc, ds)
+    unused = [e for e in range(E) if e not in set(int(i) for i in ridx)][0]
+    base_g = [b.data_ptr() for b in gb]
+    base_d = [b.data_ptr() for b in db]
+
+    def call(tg, td):
+        tgt = torch.tensor(tg, dtype=torch.int64, device="cuda")
+        tdt = torch.tensor(td, dtype=torch.int64, device="cuda")
+        out, idx, prob = gu.run_moe(r["x"], r["wr"], K, tgt, tdt, H, I)
+        return out, idx, gu.device_error()
+
+    # an unselected expert's entry is never read
+    tg = list(base_g)
+    tg[unused] = 0
+    out, idx, errw = call(tg, base_d)
+    assert errw == 0 and list(idx) == list(ridx)
+    assert_float_parity(out, ref, "moe with an unused NULL entry")
+    # a selected expert with a misaligned gate/up or a NULL down entry
+    sel = int(ridx[0])
+    tg = list(base_g)
+    tg[sel] += 8
+    assert call(tg, base_d)[2] == 3  # TT_ERR_ALIGN
+    td = list(base_d)
+    td[sel] = 0
+    assert call(base_g, td)[2] == 1  # TT_ERR_NULL
+    # the library is fine afterwards
+    out, idx, errw = call(base_g, base_d)
+    assert errw == 0
+    assert_float_parity(out, ref, "moe after the reported calls")
