@@ -308,7 +308,8 @@ def main():
     ap.add_argument("--impl", default="thinmx", choices=["thinmx", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--only", default=None, choices=["gate_up", "bf16", "moe", "int4", "sweep"],
+    ap.add_argument("--only", default=None,
+                    choices=["gate_up", "bf16", "moe", "int4", "sweep", "fp8"],
                     help="run one small workload only (for profiler captures)")
     ap.add_argument("--layers", type=int, default=None,
                     help="with --only moe: MoE layers to build (default: the full stack)")
@@ -355,6 +356,9 @@ def main():
         elif args.only == "int4":
             l2 = torch.cuda.get_device_properties(device).L2_cache_size
             r = int4_workload(torch, synth, thinmx, device, hbm, l2, reps=args.steps)
+        elif args.only == "fp8":
+            l2 = torch.cuda.get_device_properties(device).L2_cache_size
+            r = fp8_workload(torch, synth, thinmx, device, hbm, l2, reps=args.steps)
         else:
             r = moe_workload(torch, synth, loader, thinmx, device, hbm, reps=args.steps,
                              layers=args.layers)
@@ -575,6 +579,8 @@ def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
     torch.cuda.empty_cache()
     out.update(int4_workload(torch, synth, thinmx, device, hbm, l2))
     torch.cuda.empty_cache()
+    out.update(fp8_workload(torch, synth, thinmx, device, hbm, l2))
+    torch.cuda.empty_cache()
     out.update(moe_workload(torch, synth, loader, thinmx, device, hbm))
     torch.cuda.empty_cache()
     out["peak"] = {"hbm_gbs": hbm, "source": peak_kind,
@@ -621,6 +627,47 @@ def secondary_sweep(torch, synth, loader, thinmx, device, hbm, reps=20, ms=None)
         del g
     del packs, base
     return {s.name: sweep}
+
+
+def fp8_workload(torch, synth, thinmx, device, hbm, l2, reps=50):
+    """The quality-FP8 profile's MLP matvecs at SmolLM3 sizes, M=1: the gate/up
+    SwiGLU (K=2048, N=11008) and the down projection (K=11008, N=2048), each
+    over rotating weight copies whose total exceeds twice the L2 size."""
+    c = synth.GATE_UP
+    out = {}
+    for name, (n, k, swiglu) in {
+            "fp8_gate_up_k2048_n11008_m1": (c.n, c.k, True),
+            "fp8_down_k11008_n2048_m1": (c.k, c.n, False)}.items():
+        mats = 2 if swiglu else 1
+        per = mats * (n * k + 4 * n) + 2 * k + 2 * n
+        copies = max(4, int(2 * l2 // per) + 2)
+        bufs = []
+        for i in range(copies):
+            ws = []
+            for j in range(mats):
+                w = synth.torch_normal((n, k), synth.WEIGHT_STD, 20, i, j, device)
+                codes = torch.empty((n, k), dtype=torch.uint8, device=device)
+                scales = torch.empty(n, dtype=torch.float32, device=device)
+                thinmx.tt_quantize_fp8(w, n, k, codes, scales)
+                del w
+                ws.append((codes, scales))
+            x = synth.torch_normal((1, k), 1.0, 20, i, 9, device).to(torch.bfloat16)
+            y = torch.empty((1, n), dtype=torch.bfloat16, device=device)
+            bufs.append((ws, x, y))
+        if swiglu:
+            fn = lambda: [thinmx.tt_fp8_swiglu_matvec(w[0][0], w[0][1], w[1][0], w[1][1], n, k, x,
+                                                      1, y) for w, x, y in bufs]
+        else:
+            fn = lambda: [thinmx.tt_fp8_matvec(w[0][0], w[0][1], n, k, x, 1, y)
+                          for w, x, y in bufs]
+        g = capture(torch, fn)
+        ms = time_graph(torch, g, reps) / copies
+        del bufs, g
+        torch.cuda.empty_cache()
+        out[name] = {"us": round(ms * 1e3, 3), "GBps": round(per / (ms * 1e-3) / 1e9, 1),
+                     "frac": round(per / (ms * 1e-3) / 1e9 / hbm, 4), "bytes": per,
+                     "rotating_copies": copies}
+    return out
 
 
 def int4_workload(torch, synth, thinmx, device, hbm, l2, reps=50):

@@ -274,6 +274,53 @@ tt_status tt_moe_mxfp4_topk_mlp_static(const uint16_t* x_bf16, int64_t hidden, i
   return from_cuda(e);
 }
 
+tt_status tt_quantize_fp8(const float* w, int64_t n, int64_t k, uint8_t* codes, float* scales,
+                          int32_t* status_dev, void* stream) {
+  if (n < 0 || k < 0 || n > kMaxRows) return TT_ERR_SHAPE;
+  if (n == 0 || k == 0) return TT_OK;
+  if (!w || !codes || !scales) return TT_ERR_NULL;
+  if (!aligned(w, 4) || !aligned(scales, 4) || (status_dev && !aligned(status_dev, 4)))
+    return TT_ERR_ALIGN;
+  return from_cuda(tt::launch_quantize_fp8(w, n, k, codes, scales, status_dev, as_stream(stream)));
+}
+
+namespace {
+inline tt_status fp8_shape(int64_t n, int64_t k, int64_t m) {
+  if (n < 1 || n > kMaxRows || k < 16 || k % 16 != 0 || k > kMaxK) return TT_ERR_SHAPE;
+  if (m < 1 || m > 8) return TT_ERR_SHAPE;
+  return TT_OK;
+}
+}  // namespace
+
+tt_status tt_fp8_matvec(const uint8_t* codes, const float* scales, int64_t n, int64_t k,
+                        const uint16_t* x_bf16, int64_t m, uint16_t* y_bf16, void* stream) {
+  if (tt_status st = fp8_shape(n, k, m)) return st;
+  if (!codes || !scales || !x_bf16 || !y_bf16) return TT_ERR_NULL;
+  if (!aligned(codes, 16) || !aligned(scales, 4) || !aligned(x_bf16, 16) || !aligned(y_bf16, 2))
+    return TT_ERR_ALIGN;
+  const cudaError_t e = tt::launch_fp8_matvec(codes, scales, int(n), int(k), x_bf16, int(m),
+                                              y_bf16, as_stream(stream), kPdl);
+  if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+tt_status tt_fp8_swiglu_matvec(const uint8_t* gate_codes, const float* gate_scales,
+                               const uint8_t* up_codes, const float* up_scales, int64_t n,
+                               int64_t k, const uint16_t* x_bf16, int64_t m, uint16_t* h_bf16,
+                               void* stream) {
+  if (tt_status st = fp8_shape(n, k, m)) return st;
+  if (!gate_codes || !gate_scales || !up_codes || !up_scales || !x_bf16 || !h_bf16)
+    return TT_ERR_NULL;
+  if (!aligned(gate_codes, 16) || !aligned(up_codes, 16) || !aligned(gate_scales, 4) ||
+      !aligned(up_scales, 4) || !aligned(x_bf16, 16) || !aligned(h_bf16, 2))
+    return TT_ERR_ALIGN;
+  const cudaError_t e = tt::launch_fp8_swiglu(gate_codes, gate_scales, up_codes, up_scales,
+                                              int(n), int(k), x_bf16, int(m), h_bf16,
+                                              as_stream(stream), kPdl);
+  if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
 tt_status tt_quantize_int4_grouped(const float* w, int64_t n, int64_t k, int32_t group,
                                    uint8_t* codes, uint16_t* scales_f16, uint8_t* zp_u4,
                                    int32_t* status_dev, void* stream) {

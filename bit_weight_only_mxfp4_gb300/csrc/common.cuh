@@ -18,6 +18,7 @@ namespace tt {
 // ---------------------------------------------------------------------------
 constexpr int kErrNull = 1;     // TT_ERR_NULL
 constexpr int kErrAlign = 3;    // TT_ERR_ALIGN
+constexpr int kErrNonfinite = 4;  // TT_ERR_NONFINITE
 constexpr int kErrTimeout = 7;  // TT_ERR_TIMEOUT
 
 __device__ __forceinline__ void flag_error(int32_t* word, int code) {

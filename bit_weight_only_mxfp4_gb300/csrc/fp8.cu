@@ -1,0 +1,315 @@
+// FP8 (E4M3) weights with one fp32 scale per row: quantiser, matvec and the
+// gate/up SwiGLU matvec.
+//
+// Method: ThinTensor devlog (kerbin.cskartikey.dev/@satvikhardat), Dev Log #3
+// "SmolLM3-3B Results": the quality FP8 profile keeps gate/up and the middle
+// down projections in FP8, and its scaled matvec sums code value times x
+// along the row and multiplies the sum by the row's scale.  The element
+// format and the scale rule are not printed there; this library takes E4M3
+// without infinities (largest magnitude 448) and scale = fp32(amax / 448).
+//
+// Matvec design.  With one scale per row there is no per-block factor, so
+// the whole row can accumulate inside the tensor core (mma.sync m16n8k16,
+// f16 x f16 -> fp32):
+//  * one warp streams a pair of weight rows (gate and up, or rows r and r+1)
+//    with plain 128-bit loads, all of a step's loads in flight;
+//  * a 512-byte group of a row splits into 8 chunks of 64 k (chunk g = the
+//    bytes of lanes 4g..4g+3); in each of 4 MMAs, A row g holds 16 k of
+//    chunk g of the first row and A row 8 + g the same k of the second row,
+//    and B column c holds x of chunk c at chunk c's k and zeros elsewhere.
+//    D[c][c] and D[8 + c][c] then accumulate the two rows' dot products over
+//    chunk c; the other entries of D are never read.  Thread (g, t) reads the
+//    16 bytes 64g + 16t .. +15 of each row with one load, decoded by
+//    cvt.rn.f16x2.e4m3x2 (two codes per instruction);
+//  * x is staged once per CTA in shared memory, in that fragment order, as
+//    f16 after one exact power-of-two prescale per batch row (the row's max
+//    |x| -> [2^14, 2^15), so every finite value fits);
+//  * the diagonal entries meet in one warp reduction; the epilogue applies
+//    2^-s, the row scale and (gate/up) silu(g) * u, and stores bf16.
+// e4m3 x f16 products are exact; the tensor core accumulates in fp32.
+#include <cmath>
+
+#include "common.cuh"
+#include "launch.h"
+#include "mxfp4_core.cuh"
+
+namespace tt {
+namespace {
+
+constexpr int kQThreads = 256;
+
+// E4M3 code of t, round to nearest with ties to the even mantissa,
+// saturating at 448, sign kept on zero; computed from the fp64 value (no
+// intermediate rounding).
+__device__ uint32_t e4m3_from_double(double t) {
+  if (isnan(t)) return 0x7Fu;
+  const uint32_t sign = signbit(t) ? 0x80u : 0u;
+  const double a = fabs(t);
+  if (a >= 448.0) return sign | 0x7Eu;
+  if (a < 0.015625) {                       // below 2^-6: steps of 2^-9
+    return sign | uint32_t(rint(a * 512.0));  // 8 = 2^-6 = code 0x08
+  }
+  int e2;
+  (void)frexp(a, &e2);  // a = f * 2^e2, f in [0.5, 1)
+  int E = e2 - 1;       // a in [2^E, 2^(E+1))
+  double q = rint(ldexp(a, 3 - E));  // in [8, 16]
+  if (q == 16.0) {
+    q = 8.0;
+    ++E;
+  }
+  return sign | (uint32_t(E + 7) << 3) | (uint32_t(q) - 8u);
+}
+
+// One warp per row: amax, the row's fp32 scale, then every code.
+__global__ void __launch_bounds__(kQThreads)
+    quantize_fp8_kernel(const float* __restrict__ w, int64_t n, int64_t k,
+                        uint8_t* __restrict__ codes, float* __restrict__ scales,
+                        int32_t* __restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * (kQThreads / 32) + (threadIdx.x >> 5);
+  if (r >= n) return;
+  const float* wr = w + r * k;
+  uint8_t* cr = codes + r * k;
+  float amax = 0.f;
+  bool finite = true;
+  for (int64_t i = lane; i < k; i += 32) {
+    const float v = wr[i];
+    finite = finite && isfinite(v);
+    amax = fmaxf(amax, fabsf(v));
+  }
+  amax = warp_max(amax);
+  finite = __all_sync(0xffffffffu, finite);
+  if (!finite) {
+    for (int64_t i = lane; i < k; i += 32) cr[i] = 0;
+    if (lane == 0) {
+      scales[r] = __int_as_float(0x7FC00000);
+      if (status) atomicOr(status, kErrNonfinite);
+    }
+    return;
+  }
+  const float s = __double2float_rn((double)amax / 448.0);
+  if (lane == 0) scales[r] = s;
+  if (s == 0.f) {  // amax = 0, or below what an fp32 scale can hold
+    for (int64_t i = lane; i < k; i += 32) cr[i] = 0;
+    return;
+  }
+  const double sd = (double)s;
+  for (int64_t i = lane; i < k; i += 32) cr[i] = uint8_t(e4m3_from_double((double)wr[i] / sd));
+}
+
+// Two E4M3 codes per 16-bit half -> f16x2 (the lower byte in the low half).
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+constexpr int kWarps = 8;
+constexpr int kGroupsPerStep = 4;  // 512-byte groups per row in flight per step
+
+// MT: batch rows staged (m <= MT); SWIGLU: the row pair is (gate, up) of
+// one output, else rows (2p, 2p + 1) of one matrix.
+template <int MT, bool SWIGLU>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    fp8_pair_kernel(const uint8_t* __restrict__ wa, const float* __restrict__ sa,
+                    const uint8_t* __restrict__ wb, const float* __restrict__ sb, int n, int k,
+                    const uint16_t* __restrict__ x, int m, uint16_t* __restrict__ y) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ngrp = (k + 511) >> 9;
+  uint4* xf = reinterpret_cast<uint4*>(smem);  // [MT][ngrp][32 lanes][2] f16 fragments
+  int* sx = reinterpret_cast<int*>(xf + (size_t)MT * ngrp * 64);  // [MT] prescale exponents
+  unsigned* xmax = reinterpret_cast<unsigned*>(sx + MT);            // [MT] max |x| bits
+  const int npairs = SWIGLU ? n : (n + 1) / 2;
+  const int gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
+  const int g = lane >> 2, t = lane & 3;
+
+  pdl_allow_next_grid();
+  // The first pair's first step of weights does not depend on the previous
+  // kernel: request it before waiting.
+  auto load_step = [&](int p, int q0, uint4 (&ca)[kGroupsPerStep], uint4 (&cb)[kGroupsPerStep]) {
+    const int ra = SWIGLU ? p : 2 * p, rb = SWIGLU ? p : 2 * p + 1;
+    const uint8_t* pa = wa + (size_t)ra * k;
+    const uint8_t* pb = (SWIGLU || rb < n) ? wb + (size_t)rb * k : nullptr;
+#pragma unroll
+    for (int u = 0; u < kGroupsPerStep; ++u) {
+      const int off = (q0 + u) * 512 + 16 * lane;
+      ca[u] = cb[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (q0 + u < ngrp && off < k) {
+        ca[u] = __ldcs(reinterpret_cast<const uint4*>(pa + off));
+        if (pb) cb[u] = __ldcs(reinterpret_cast<const uint4*>(pb + off));
+      }
+    }
+  };
+  uint4 ca[kGroupsPerStep], cb[kGroupsPerStep];
+  if (gw < npairs) load_step(gw, 0, ca, cb);
+  pdl_wait_prior_grid();
+
+  // x: per batch row, the max |x| (bits of a non-negative float order like
+  // the values), then the prescaled f16 fragments.
+  if (threadIdx.x < MT) xmax[threadIdx.x] = 0u;
+  __syncthreads();
+  for (int i = 0; i < m; ++i) {
+    float mx = 0.f;
+    for (int c = threadIdx.x; c < k / 8; c += kWarps * 32) {
+      const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)i * k + 8 * c);
+      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(vw[e] & 0xFFFFu)),
+                             fabsf(bf16_bits_to_f32(vw[e] >> 16))));
+    }
+    mx = warp_max(mx);
+    if (lane == 0) atomicMax(&xmax[i], __float_as_uint(mx));
+  }
+  __syncthreads();
+  if (threadIdx.x < MT) {
+    const float mx = __uint_as_float(xmax[threadIdx.x]);
+    sx[threadIdx.x] = threadIdx.x < m && mx > 0.f ? min(f16_prescale_exponent(mx), 127) : 0;
+  }
+  __syncthreads();
+  // fragment (i, q, l): x[i][512 q + 16 l .. +15] as 8 f16x2 (2 uint4)
+  for (int it = threadIdx.x; it < MT * ngrp * 32; it += kWarps * 32) {
+    const int i = it / (ngrp * 32), rem = it - i * ngrp * 32;
+    const int off = (rem >> 5) * 512 + 16 * (rem & 31);
+    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+    if (i < m && off < k) {
+      v0 = *reinterpret_cast<const uint4*>(x + (size_t)i * k + off);
+      v1 = *reinterpret_cast<const uint4*>(x + (size_t)i * k + off + 8);
+    }
+    const float two_s = scalbnf(1.0f, sx[i]);
+    uint4 o0, o1;
+    o0.x = pack_f16x2_scaled(bf16_bits_to_f32(v0.x & 0xFFFFu), bf16_bits_to_f32(v0.x >> 16), two_s);
+    o0.y = pack_f16x2_scaled(bf16_bits_to_f32(v0.y & 0xFFFFu), bf16_bits_to_f32(v0.y >> 16), two_s);
+    o0.z = pack_f16x2_scaled(bf16_bits_to_f32(v0.z & 0xFFFFu), bf16_bits_to_f32(v0.z >> 16), two_s);
+    o0.w = pack_f16x2_scaled(bf16_bits_to_f32(v0.w & 0xFFFFu), bf16_bits_to_f32(v0.w >> 16), two_s);
+    o1.x = pack_f16x2_scaled(bf16_bits_to_f32(v1.x & 0xFFFFu), bf16_bits_to_f32(v1.x >> 16), two_s);
+    o1.y = pack_f16x2_scaled(bf16_bits_to_f32(v1.y & 0xFFFFu), bf16_bits_to_f32(v1.y >> 16), two_s);
+    o1.z = pack_f16x2_scaled(bf16_bits_to_f32(v1.z & 0xFFFFu), bf16_bits_to_f32(v1.z >> 16), two_s);
+    o1.w = pack_f16x2_scaled(bf16_bits_to_f32(v1.w & 0xFFFFu), bf16_bits_to_f32(v1.w >> 16), two_s);
+    xf[2 * it] = o0;
+    xf[2 * it + 1] = o1;
+  }
+  __syncthreads();
+
+  const bool diag = (t == (g >> 1));  // holds D[g][g] and D[8 + g][g]
+  const bool odd = (g & 1) != 0;
+  for (int p = gw; p < npairs; p += nw) {
+    float d[MT][4];
+#pragma unroll
+    for (int i = 0; i < MT; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
+    for (int q0 = 0; q0 < ngrp; q0 += kGroupsPerStep) {
+      if (q0 > 0) load_step(p, q0, ca, cb);
+#pragma unroll
+      for (int u = 0; u < kGroupsPerStep; ++u) {
+        const int q = q0 + u;
+        if (q < ngrp) {
+          const uint32_t wa4[4] = {ca[u].x, ca[u].y, ca[u].z, ca[u].w};
+          const uint32_t wb4[4] = {cb[u].x, cb[u].y, cb[u].z, cb[u].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {  // MMA j: bytes 4j..4j+3 of the thread's 16
+            uint32_t a0, a2, b0, b2;
+            e4m3x4_to_f16x2(wa4[j], a0, a2);
+            e4m3x4_to_f16x2(wb4[j], b0, b2);
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+              if (i < m) {
+                const uint4 xv = xf[((size_t)(i * ngrp + q) * 32 + lane) * 2 + (j >> 1)];
+                const uint32_t x0 = (j & 1) ? xv.z : xv.x, x1 = (j & 1) ? xv.w : xv.y;
+                mma_16816(d[i], a0, b0, a2, b2, x0, x1);
+              }
+            }
+          }
+        }
+      }
+    }
+    // next pair's first step in flight during the reduction and the stores
+    const int pn = p + nw;
+    if (pn < npairs) load_step(pn, 0, ca, cb);
+    const int ra = SWIGLU ? p : 2 * p;
+    const float fa = sa[ra];
+    const float fb = SWIGLU ? sb[p] : (2 * p + 1 < n ? sb[2 * p + 1] : 0.f);
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+      if (i < m) {
+        const float va = diag ? (odd ? d[i][1] : d[i][0]) : 0.f;
+        const float vb = diag ? (odd ? d[i][3] : d[i][2]) : 0.f;
+        const float v = warp_sum2(va, vb, lane);  // lanes 0-15: first row, 16-31: second
+        const float vu = __shfl_sync(0xffffffffu, v, 16);
+        if (lane == 0) {
+          const float inv = scalbnf(1.0f, -sx[i]);
+          const float ga = v * inv * fa, gb = vu * inv * fb;
+          if (SWIGLU) {
+            y[(size_t)i * n + p] = f32_to_bf16_rne(silu_mul(ga, gb));
+          } else {
+            y[(size_t)i * n + 2 * p] = f32_to_bf16_rne(ga);
+            if (2 * p + 1 < n) y[(size_t)i * n + 2 * p + 1] = f32_to_bf16_rne(gb);
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int MT, bool SWIGLU>
+cudaError_t run_pair(const DeviceInfo& di, const uint8_t* wa, const float* sa, const uint8_t* wb,
+                     const float* sb, int n, int k, const uint16_t* x, int m, uint16_t* y,
+                     cudaStream_t s, bool pdl) {
+  const int ngrp = (k + 511) / 512;
+  const int smem = MT * ngrp * 64 * 16 + MT * 8;
+  if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
+  auto kern = fp8_pair_kernel<MT, SWIGLU>;
+  cudaError_t e = ensure_smem(di, kern, smem);
+  if (e != cudaSuccess) return e;
+  const int npairs = SWIGLU ? n : (n + 1) / 2;
+  int grid = 2 * di.sms;
+  const int need = (npairs + kWarps - 1) / kWarps;
+  if (grid > need) grid = need;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, wa, sa, wb, sb, n, k, x, m, y);
+}
+
+template <bool SWIGLU>
+cudaError_t run_fp8(const uint8_t* wa, const float* sa, const uint8_t* wb, const float* sb, int n,
+                    int k, const uint16_t* x, int m, uint16_t* y, cudaStream_t s, bool pdl) {
+  const DeviceInfo* di = device_info();
+  if (!di) return cudaErrorNoDevice;
+  if (m == 1) return run_pair<1, SWIGLU>(*di, wa, sa, wb, sb, n, k, x, m, y, s, pdl);
+  if (m == 2) return run_pair<2, SWIGLU>(*di, wa, sa, wb, sb, n, k, x, m, y, s, pdl);
+  if (m <= 4) return run_pair<4, SWIGLU>(*di, wa, sa, wb, sb, n, k, x, m, y, s, pdl);
+  return run_pair<8, SWIGLU>(*di, wa, sa, wb, sb, n, k, x, m, y, s, pdl);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_fp8(const float* w, int64_t n, int64_t k, uint8_t* codes,
+                                float* scales, int32_t* status, cudaStream_t s) {
+  const int64_t blocks = (n + kQThreads / 32 - 1) / (kQThreads / 32);
+  quantize_fp8_kernel<<<dim3(unsigned(blocks)), kQThreads, 0, s>>>(w, n, k, codes, scales, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_matvec(const uint8_t* codes, const float* scales, int n, int k,
+                              const uint16_t* x, int m, uint16_t* y, cudaStream_t s, bool pdl) {
+  return run_fp8<false>(codes, scales, codes, scales, n, k, x, m, y, s, pdl);
+}
+
+cudaError_t launch_fp8_swiglu(const uint8_t* gc, const float* gs, const uint8_t* uc,
+                              const float* us, int n, int k, const uint16_t* x, int m,
+                              uint16_t* h, cudaStream_t s, bool pdl) {
+  return run_fp8<true>(gc, gs, uc, us, n, k, x, m, h, s, pdl);
+}
+
+}  // namespace tt

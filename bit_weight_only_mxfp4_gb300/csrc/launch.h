@@ -80,6 +80,17 @@ cudaError_t launch_moe_fused(const uint16_t* x, int hidden, int inter, const uin
 constexpr int kMoeStaticMaxHidden = 4096;  // hidden limit of the static scratch
 cudaError_t moe_static_scratch(void** ptr, size_t* bytes);
 
+// fp8.cu — E4M3 weights with one fp32 scale per row: quantiser, matvec and
+// gate/up SwiGLU (m in [1, 8]); x staging that does not fit the shared
+// memory: cudaErrorInvalidConfiguration
+cudaError_t launch_quantize_fp8(const float* w, int64_t n, int64_t k, uint8_t* codes,
+                                float* scales, int32_t* status, cudaStream_t s);
+cudaError_t launch_fp8_matvec(const uint8_t* codes, const float* scales, int n, int k,
+                              const uint16_t* x, int m, uint16_t* y, cudaStream_t s, bool pdl);
+cudaError_t launch_fp8_swiglu(const uint8_t* gc, const float* gs, const uint8_t* uc,
+                              const float* us, int n, int k, const uint16_t* x, int m,
+                              uint16_t* h, cudaStream_t s, bool pdl);
+
 // gemv_bf16.cu
 cudaError_t launch_swiglu_bf16(const uint16_t* wg, const uint16_t* wu, int n, int k,
                                const uint16_t* x, int m, uint16_t* h, cudaStream_t s, bool pdl);

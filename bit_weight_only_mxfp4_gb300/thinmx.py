@@ -48,6 +48,9 @@ SIGNATURES = {
                                               _P, _SZ, _P]),
     "tt_moe_mxfp4_topk_mlp_static": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _P,
                                                      _P, _P, _P]),
+    "tt_quantize_fp8": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P]),
+    "tt_fp8_matvec": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _I64, _P, _P]),
+    "tt_fp8_swiglu_matvec": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _P]),
     "tt_quantize_int4_grouped": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
     "tt_int4_grouped_matvec": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _P]),
 }
@@ -160,6 +163,23 @@ def tt_mxfp4_swiglu_matvec(packed, n, k, x_bf16, m, h_bf16, stream=None):
 def tt_bf16_swiglu_matvec(wg, wu, n, k, x_bf16, m, h_bf16, stream=None):
     _check("tt_bf16_swiglu_matvec", load().tt_bf16_swiglu_matvec(
         _ptr(wg), _ptr(wu), n, k, _ptr(x_bf16), m, _ptr(h_bf16), _stream(stream)))
+
+
+def tt_quantize_fp8(w, n, k, codes, scales, status_dev=None, stream=None):
+    _check("tt_quantize_fp8", load().tt_quantize_fp8(
+        _ptr(w), n, k, _ptr(codes), _ptr(scales), _ptr(status_dev), _stream(stream)))
+
+
+def tt_fp8_matvec(codes, scales, n, k, x_bf16, m, y_bf16, stream=None):
+    _check("tt_fp8_matvec", load().tt_fp8_matvec(
+        _ptr(codes), _ptr(scales), n, k, _ptr(x_bf16), m, _ptr(y_bf16), _stream(stream)))
+
+
+def tt_fp8_swiglu_matvec(gate_codes, gate_scales, up_codes, up_scales, n, k, x_bf16, m, h_bf16,
+                         stream=None):
+    _check("tt_fp8_swiglu_matvec", load().tt_fp8_swiglu_matvec(
+        _ptr(gate_codes), _ptr(gate_scales), _ptr(up_codes), _ptr(up_scales), n, k,
+        _ptr(x_bf16), m, _ptr(h_bf16), _stream(stream)))
 
 
 def tt_quantize_int4_grouped(w, n, k, group, codes, scales_f16, zp_u4, status_dev=None,

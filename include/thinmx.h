@@ -7,7 +7,8 @@
  *   - the MoE variant: router, top-k, softmax and only the selected
  *     experts' gate/up/down;
  *   - grouped affine INT4 matvec for the dense Q/K/V/O projections;
- *   - bf16 gate/up SwiGLU matvec for the layers kept in bf16.
+ *   - bf16 gate/up SwiGLU matvec for the layers kept in bf16;
+ *   - FP8 (E4M3, one scale per row) matvec and gate/up SwiGLU matvec.
  *
  * Sources.  The method is the ThinTensor decode runtime's:
  *   [DL4]  kerbin.cskartikey.dev/@satvikhardat, "Dev Log #4 — 91–96 tok/s
@@ -19,6 +20,8 @@
  *          problem ("Why gate/up was the right target").
  *   [DL2]  same feed, "Dev Log #2": the gated_activation, router and expert
  *          operators of the execution tape.
+ *   [DL3]  same feed, "Dev Log #3 — SmolLM3-3B Results": the quality FP8
+ *          profile and its per-row-scaled matvec.
  *   [SHIP] stardance.hackclub.com/projects/29750, "Hitting 100hrs and final
  *          ship" (production MXFP4/INT4 quantizers, exact routing, expert
  *          routing on the decode hot path), the MoE drift devlog (block-
@@ -266,6 +269,44 @@ tt_status tt_moe_mxfp4_topk_mlp_static(const uint16_t* x_bf16, int64_t hidden, i
                                        int32_t top_k, const void* const* gate_up_packed,
                                        const void* const* down_packed, uint16_t* out_bf16,
                                        int32_t* out_idx, float* out_prob, void* stream);
+
+/* ------------------------------------------------------------------------
+ * FP8 (E4M3) weights with one fp32 scale per row  [DL3 "Dev Log #3 —
+ * SmolLM3-3B Results": the quality FP8 profile keeps gate/up and the middle
+ * down projections in FP8; its scaled matvec sums code value times x along
+ * the row, then multiplies by the row's scale]
+ *
+ * E4M3 code: bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0 mantissa;
+ * exponent 0 is subnormal (m/8 * 2^-6); 0x7F/0xFF are NaN; no infinities;
+ * largest magnitude 448.  Canonical matrix [n][k]: codes uint8 [n][k] (row
+ * major), scales fp32 [n].
+ *
+ * Quantiser, per row: amax = max |w|; scale = fp32 round-to-nearest of
+ * amax / 448 (computed in fp64); code = E4M3 round-to-nearest-even of
+ * w / scale (the division in fp64), saturating at +-448, the sign kept on a
+ * zero result (0x80).  A row with scale 0 (amax = 0, or below fp32's range)
+ * gets zero codes; a row holding NaN/Inf gets scale NaN, zero codes, and
+ * TT_ERR_NONFINITE OR-ed into *status_dev (device int32, may be NULL, zeroed
+ * by the caller).  Setup step.  Requires n >= 0, k >= 0.
+ * --------------------------------------------------------------------- */
+tt_status tt_quantize_fp8(const float* w, int64_t n, int64_t k, uint8_t* codes, float* scales,
+                          int32_t* status_dev, void* stream);
+
+/* y[i][r] = bf16_rne( scale[r] * sum_k E4M3(codes[r][k]) * x[i][k] ), fp32
+   accumulation (the down projection of the FP8 profile).  x [m][k], y [m][n].
+   Requires n >= 1, 16 <= k <= 16384, k % 16 == 0, 1 <= m <= 8; codes and x
+   16-byte aligned.  A batch whose x does not fit the kernel's shared-memory
+   staging (m * k f16 values, at most the device's per-block limit) returns
+   TT_ERR_UNSUPPORTED before any launch. */
+tt_status tt_fp8_matvec(const uint8_t* codes, const float* scales, int64_t n, int64_t k,
+                        const uint16_t* x_bf16, int64_t m, uint16_t* y_bf16, void* stream);
+
+/* h[i][r] = bf16_rne( silu(g) * u ) with g, u the FP8 matvecs of the gate and
+   up matrices (same shapes and rules as tt_fp8_matvec). */
+tt_status tt_fp8_swiglu_matvec(const uint8_t* gate_codes, const float* gate_scales,
+                               const uint8_t* up_codes, const float* up_scales, int64_t n,
+                               int64_t k, const uint16_t* x_bf16, int64_t m, uint16_t* h_bf16,
+                               void* stream);
 
 /* ------------------------------------------------------------------------
  * Grouped affine INT4  [SHIP 97.87 tok/s notes: dense_int4_layers="all" for

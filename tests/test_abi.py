@@ -122,6 +122,26 @@ def test_moe_validation_before_launch(lib):
     assert call(2880, 2880, 32, 4, td=A + 4) == 3             # expert table not 8-byte aligned
 
 
+def test_fp8_validation_before_launch(lib):
+    A = 1 << 20  # never dereferenced: every case fails validation first
+    s = None
+    mv = lambda n, k, m, codes=A, x=A: _st("tt_fp8_matvec", codes, A, n, k, x, m, A, s)
+    sw = lambda n, k, m, uc=A: _st("tt_fp8_swiglu_matvec", A, A, uc, A, n, k, A, m, A, s)
+    assert mv(2048, 11008, 9) == 2        # m beyond 8
+    assert mv(2048, 11000, 1) == 2        # k not a multiple of 16
+    assert mv(2048, 32768, 1) == 2        # k beyond 16384
+    assert mv(0, 2048, 1) == 2
+    assert mv(2048, 2048, 1, codes=None) == 1
+    assert mv(2048, 2048, 1, codes=A + 8) == 3
+    assert mv(2048, 2048, 1, x=A + 2) == 3
+    assert sw(11008, 2048, 0) == 2
+    assert sw(11008, 2048, 1, uc=None) == 1
+    assert sw(11008, 2048, 1, uc=A + 4) == 3
+    # the quantiser: an empty matrix is a no-op, a NULL output an error
+    assert _st("tt_quantize_fp8", None, 0, 64, None, None, None, s) == 0
+    assert _st("tt_quantize_fp8", A, 4, 64, None, A, None, s) == 1
+
+
 def test_int4_validation_before_launch(lib):
     A = 1 << 20
     s = None
