@@ -309,7 +309,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--only", default=None,
-                    choices=["gate_up", "bf16", "moe", "int4", "sweep", "fp8"],
+                    choices=["gate_up", "bf16", "moe", "int4", "sweep", "fp8", "mlp"],
                     help="run one small workload only (for profiler captures)")
     ap.add_argument("--layers", type=int, default=None,
                     help="with --only moe: MoE layers to build (default: the full stack)")
@@ -356,6 +356,8 @@ def main():
         elif args.only == "int4":
             l2 = torch.cuda.get_device_properties(device).L2_cache_size
             r = int4_workload(torch, synth, thinmx, device, hbm, l2, reps=args.steps)
+        elif args.only == "mlp":
+            r = mlp_stack_workload(torch, synth, loader, thinmx, device, hbm, reps=args.steps)
         elif args.only == "fp8":
             l2 = torch.cuda.get_device_properties(device).L2_cache_size
             r = fp8_workload(torch, synth, thinmx, device, hbm, l2, reps=args.steps)
@@ -581,6 +583,8 @@ def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
     torch.cuda.empty_cache()
     out.update(fp8_workload(torch, synth, thinmx, device, hbm, l2))
     torch.cuda.empty_cache()
+    out.update(mlp_stack_workload(torch, synth, loader, thinmx, device, hbm))
+    torch.cuda.empty_cache()
     out.update(moe_workload(torch, synth, loader, thinmx, device, hbm))
     torch.cuda.empty_cache()
     out["peak"] = {"hbm_gbs": hbm, "source": peak_kind,
@@ -630,35 +634,56 @@ def secondary_sweep(torch, synth, loader, thinmx, device, hbm, reps=20, ms=None)
 
 
 def fp8_workload(torch, synth, thinmx, device, hbm, l2, reps=50):
-    """The quality-FP8 profile's MLP matvecs at SmolLM3 sizes, M=1: the gate/up
-    SwiGLU (K=2048, N=11008) and the down projection (K=11008, N=2048), each
-    over rotating weight copies whose total exceeds twice the L2 size."""
+    """The MLP matvecs at SmolLM3 sizes, M=1, each over rotating weight
+    copies whose total exceeds twice the L2 size: the quality-FP8 profile's
+    gate/up SwiGLU (K=2048, N=11008) and down projection (K=11008, N=2048),
+    and the down projection in bf16 and in MXFP4."""
     c = synth.GATE_UP
     out = {}
-    for name, (n, k, swiglu) in {
-            "fp8_gate_up_k2048_n11008_m1": (c.n, c.k, True),
-            "fp8_down_k11008_n2048_m1": (c.k, c.n, False)}.items():
+    cases = {"fp8_gate_up_k2048_n11008_m1": ("fp8", c.n, c.k, True),
+             "fp8_down_k11008_n2048_m1": ("fp8", c.k, c.n, False),
+             "bf16_down_k11008_n2048_m1": ("bf16", c.k, c.n, False),
+             "mxfp4_down_k11008_n2048_m1": ("mxfp4", c.k, c.n, False)}
+    for name, (kind, n, k, swiglu) in cases.items():
         mats = 2 if swiglu else 1
-        per = mats * (n * k + 4 * n) + 2 * k + 2 * n
+        if kind == "fp8":
+            per = mats * (n * k + 4 * n) + 2 * k + 2 * n
+        elif kind == "bf16":
+            per = 2 * n * k + 2 * k + 2 * n
+        else:
+            per = n * k // 2 + n * k // 32 + 2 * k + 2 * n
         copies = max(4, int(2 * l2 // per) + 2)
         bufs = []
         for i in range(copies):
             ws = []
             for j in range(mats):
                 w = synth.torch_normal((n, k), synth.WEIGHT_STD, 20, i, j, device)
-                codes = torch.empty((n, k), dtype=torch.uint8, device=device)
-                scales = torch.empty(n, dtype=torch.float32, device=device)
-                thinmx.tt_quantize_fp8(w, n, k, codes, scales)
+                if kind == "fp8":
+                    codes = torch.empty((n, k), dtype=torch.uint8, device=device)
+                    scales = torch.empty(n, dtype=torch.float32, device=device)
+                    thinmx.tt_quantize_fp8(w, n, k, codes, scales)
+                    ws.append((codes, scales))
+                elif kind == "bf16":
+                    ws.append(w.to(torch.bfloat16))
+                else:
+                    codes = torch.empty((n, k // 2), dtype=torch.uint8, device=device)
+                    scales = torch.empty((n, k // 32), dtype=torch.uint8, device=device)
+                    thinmx.tt_quantize_mxfp4(w, n, k, codes, scales)
+                    ws.append((codes, scales))
                 del w
-                ws.append((codes, scales))
             x = synth.torch_normal((1, k), 1.0, 20, i, 9, device).to(torch.bfloat16)
             y = torch.empty((1, n), dtype=torch.bfloat16, device=device)
             bufs.append((ws, x, y))
-        if swiglu:
+        if kind == "fp8" and swiglu:
             fn = lambda: [thinmx.tt_fp8_swiglu_matvec(w[0][0], w[0][1], w[1][0], w[1][1], n, k, x,
                                                       1, y) for w, x, y in bufs]
-        else:
+        elif kind == "fp8":
             fn = lambda: [thinmx.tt_fp8_matvec(w[0][0], w[0][1], n, k, x, 1, y)
+                          for w, x, y in bufs]
+        elif kind == "bf16":
+            fn = lambda: [thinmx.tt_bf16_matvec(w[0], n, k, x, 1, y) for w, x, y in bufs]
+        else:
+            fn = lambda: [thinmx.tt_mxfp4_matvec(w[0][0], w[0][1], None, n, k, x, 1, y)
                           for w, x, y in bufs]
         g = capture(torch, fn)
         ms = time_graph(torch, g, reps) / copies
@@ -667,6 +692,78 @@ def fp8_workload(torch, synth, thinmx, device, hbm, l2, reps=50):
         out[name] = {"us": round(ms * 1e3, 3), "GBps": round(per / (ms * 1e-3) / 1e9, 1),
                      "frac": round(per / (ms * 1e-3) / 1e9 / hbm, 4), "bytes": per,
                      "rotating_copies": copies}
+    return out
+
+
+def mlp_stack_workload(torch, synth, loader, thinmx, device, hbm, reps=20):
+    """The SmolLM3-3B-shaped decode MLP stack at M=1 (36 layers, hidden 2048,
+    intermediate 11008), every layer gate/up SwiGLU then the down projection,
+    layer l + 1 reading layer l's output: 72 PDL-chained calls in one CUDA
+    graph, in two profiles -- the selective one (MXFP4 gate/up in layers
+    0:24, bf16 elsewhere, bf16 down projections) and the FP8 one (FP8
+    everywhere).  All weights resident (3.3 GB and 2.4 GB, far beyond L2)."""
+    c = synth.STACK
+    H, I = c.k, c.n
+    out = {}
+    b_mx = 2 * (I * H // 2 + I * H // 32 + 4 * I) + 2 * H + 2 * I
+    b_bf = 4 * I * H + 2 * H + 2 * I
+    b_bfd = 2 * H * I + 2 * I + 2 * H
+    b_f8 = 2 * (I * H + 4 * I) + 2 * H + 2 * I
+    b_f8d = H * I + 4 * H + 2 * I + 2 * H
+
+    def fp8(w, n, k):
+        codes = torch.empty((n, k), dtype=torch.uint8, device=device)
+        scales = torch.empty(n, dtype=torch.float32, device=device)
+        thinmx.tt_quantize_fp8(w, n, k, codes, scales)
+        return codes, scales
+
+    for profile in ("selective_mxfp4", "fp8"):
+        layers, nbytes = [], 0
+        for l in range(c.layers):
+            wg = synth.torch_normal((I, H), synth.WEIGHT_STD, 30, l, 0, device)
+            wu = synth.torch_normal((I, H), synth.WEIGHT_STD, 30, l, 1, device)
+            wd = synth.torch_normal((H, I), synth.WEIGHT_STD, 30, l, 2, device)
+            h = torch.empty((1, I), dtype=torch.bfloat16, device=device)
+            y = torch.empty((1, H), dtype=torch.bfloat16, device=device)
+            if profile == "fp8":
+                layers.append(("fp8", fp8(wg, I, H), fp8(wu, I, H), fp8(wd, H, I), h, y))
+                nbytes += b_f8 + b_f8d
+            elif l < c.mxfp4_layers:
+                pg = synth.torch_uniform((I,), 0.9, 1.1, 30, l, 3, device)
+                pu = synth.torch_uniform((I,), 0.9, 1.1, 30, l, 4, device)
+                layers.append(("mxfp4", loader.mxfp4_gate_up_from_f32(wg, wu, pg, pu), None,
+                               wd.to(torch.bfloat16), h, y))
+                nbytes += b_mx + b_bfd
+            else:
+                layers.append(("bf16", wg.to(torch.bfloat16), wu.to(torch.bfloat16),
+                               wd.to(torch.bfloat16), h, y))
+                nbytes += b_bf + b_bfd
+            del wg, wu, wd
+        x0 = synth.torch_normal((1, H), 1.0, 30, 99, 0, device).to(torch.bfloat16)
+
+        def step():
+            x = x0
+            for kind, a, b, d, h, y in layers:
+                if kind == "fp8":
+                    thinmx.tt_fp8_swiglu_matvec(a[0], a[1], b[0], b[1], I, H, x, 1, h)
+                    thinmx.tt_fp8_matvec(d[0], d[1], H, I, h, 1, y)
+                else:
+                    if kind == "mxfp4":
+                        thinmx.tt_mxfp4_swiglu_matvec(a, I, H, x, 1, h)
+                    else:
+                        thinmx.tt_bf16_swiglu_matvec(a, b, I, H, x, 1, h)
+                    thinmx.tt_bf16_matvec(d, H, I, h, 1, y)
+                x = y
+
+        g = capture(torch, step)
+        ms = time_graph(torch, g, reps)
+        out[f"smollm3_3b_mlp_stack_36l_{profile}"] = {
+            "us": round(ms * 1e3, 2), "us_per_layer": round(ms * 1e3 / c.layers, 3),
+            "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4), "bytes": nbytes,
+            "kernels": 2 * c.layers}
+        del layers, g
+        torch.cuda.empty_cache()
     return out
 
 

@@ -195,6 +195,31 @@ tt_status tt_bf16_swiglu_matvec(const uint16_t* wg, const uint16_t* wu, int64_t 
                                           as_stream(stream), kPdl));
 }
 
+tt_status tt_mxfp4_matvec(const uint8_t* codes, const uint8_t* scales, const float* postscale,
+                          int64_t n, int64_t k, const uint16_t* x_bf16, int64_t m,
+                          uint16_t* y_bf16, void* stream) {
+  if (n < 1 || k < 32 || k % 32 != 0 || k > kMaxK || n > kMaxRows) return TT_ERR_SHAPE;
+  if (m < 1 || m > 8) return TT_ERR_SHAPE;
+  if (!codes || !scales || !x_bf16 || !y_bf16) return TT_ERR_NULL;
+  if (!aligned(codes, 16) || (postscale && !aligned(postscale, 4)) || !aligned(x_bf16, 16) ||
+      !aligned(y_bf16, 2))
+    return TT_ERR_ALIGN;
+  const cudaError_t e = tt::launch_mxfp4_rows(codes, scales, postscale, int(n), int(k), x_bf16,
+                                              int(m), y_bf16, as_stream(stream), kPdl);
+  if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+tt_status tt_bf16_matvec(const uint16_t* w, int64_t n, int64_t k, const uint16_t* x_bf16,
+                         int64_t m, uint16_t* y_bf16, void* stream) {
+  if (n < 1 || k < 8 || k % 8 != 0 || k > (int64_t(1) << 30) || n > kMaxRows) return TT_ERR_SHAPE;
+  if (m < 1 || m > 8) return TT_ERR_SHAPE;
+  if (!w || !x_bf16 || !y_bf16) return TT_ERR_NULL;
+  if (!aligned(w, 16) || !aligned(x_bf16, 16) || !aligned(y_bf16, 2)) return TT_ERR_ALIGN;
+  return from_cuda(tt::launch_bf16_rows(w, int(n), int(k), x_bf16, int(m), y_bf16,
+                                        as_stream(stream), kPdl));
+}
+
 size_t tt_mxfp4_rows_packed_bytes(int64_t n, int64_t k) {
   if (n < 1 || k < 32 || k % 32 != 0 || k > kMaxK || n > kMaxRows) return 0;
   return size_t(tt::ColSlices(n, int(k)).bytes);

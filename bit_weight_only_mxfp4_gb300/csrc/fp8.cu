@@ -11,8 +11,9 @@
 // Matvec design.  With one scale per row there is no per-block factor, so
 // the whole row can accumulate inside the tensor core (mma.sync m16n8k16,
 // f16 x f16 -> fp32):
-//  * one warp streams a pair of weight rows (gate and up, or rows r and r+1)
-//    with plain 128-bit loads, all of a step's loads in flight;
+//  * a warp streams a pair of weight rows (gate and up, or rows r and r+1),
+//    or a slice of the pair's K when rows are few and long, with plain
+//    128-bit loads, double-buffered steps;
 //  * a 512-byte group of a row splits into 8 chunks of 64 k (chunk g = the
 //    bytes of lanes 4g..4g+3); in each of 4 MMAs, A row g holds 16 k of
 //    chunk g of the first row and A row 8 + g the same k of the second row,
@@ -112,19 +113,27 @@ constexpr int kGroupsPerStep = 4;  // 512-byte groups per row in flight per step
 
 // MT: batch rows staged (m <= MT); SWIGLU: the row pair is (gate, up) of
 // one output, else rows (2p, 2p + 1) of one matrix.
+// ks warps share a pair (a down projection has few, long rows): the CTA's
+// 8 warps take 8 / ks pairs at a time, warp (lp, sl) the sl-th slice of the
+// groups of pair pb + lp; the slices' sums meet in shared memory and are
+// added in slice order.
 template <int MT, bool SWIGLU>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     fp8_pair_kernel(const uint8_t* __restrict__ wa, const float* __restrict__ sa,
                     const uint8_t* __restrict__ wb, const float* __restrict__ sb, int n, int k,
-                    const uint16_t* __restrict__ x, int m, uint16_t* __restrict__ y) {
+                    const uint16_t* __restrict__ x, int m, uint16_t* __restrict__ y, int ks) {
   extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ float red[kWarps][MT][2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ngrp = (k + 511) >> 9;
+  const int R = kWarps / ks, lp = warp / ks, sl = warp % ks;
+  const int gs = (ngrp + ks - 1) / ks;  // groups per slice
+  const int gbeg = sl * gs, gend = min(ngrp, gbeg + gs);
   uint4* xf = reinterpret_cast<uint4*>(smem);  // [MT][ngrp][32 lanes][2] f16 fragments
   int* sx = reinterpret_cast<int*>(xf + (size_t)MT * ngrp * 64);  // [MT] prescale exponents
   unsigned* xmax = reinterpret_cast<unsigned*>(sx + MT);            // [MT] max |x| bits
   const int npairs = SWIGLU ? n : (n + 1) / 2;
-  const int gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
+  const int pstep = gridDim.x * R;
   const int g = lane >> 2, t = lane & 3;
 
   pdl_allow_next_grid();
@@ -138,14 +147,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     for (int u = 0; u < kGroupsPerStep; ++u) {
       const int off = (q0 + u) * 512 + 16 * lane;
       ca[u] = cb[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (q0 + u < ngrp && off < k) {
+      if (p < npairs && q0 + u < gend && off < k) {
         ca[u] = __ldcs(reinterpret_cast<const uint4*>(pa + off));
         if (pb) cb[u] = __ldcs(reinterpret_cast<const uint4*>(pb + off));
       }
     }
   };
   uint4 ca[kGroupsPerStep], cb[kGroupsPerStep];
-  if (gw < npairs) load_step(gw, 0, ca, cb);
+  load_step(blockIdx.x * R + lp, gbeg, ca, cb);
   pdl_wait_prior_grid();
 
   // x: per batch row, the max |x| (bits of a non-negative float order like
@@ -154,13 +163,22 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   __syncthreads();
   for (int i = 0; i < m; ++i) {
     float mx = 0.f;
-    for (int c = threadIdx.x; c < k / 8; c += kWarps * 32) {
-      const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)i * k + 8 * c);
-      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+    for (int c0 = 0; c0 < k / 8; c0 += 4 * kWarps * 32) {  // four loads in flight
+      uint4 v[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(vw[e] & 0xFFFFu)),
-                             fabsf(bf16_bits_to_f32(vw[e] >> 16))));
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + u * kWarps * 32 + threadIdx.x;
+        v[u] = c < k / 8 ? *reinterpret_cast<const uint4*>(x + (size_t)i * k + 8 * c)
+                         : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t vw[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(vw[e] & 0xFFFFu)),
+                               fabsf(bf16_bits_to_f32(vw[e] >> 16))));
+      }
     }
     mx = warp_max(mx);
     if (lane == 0) atomicMax(&xmax[i], __float_as_uint(mx));
@@ -197,18 +215,20 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 
   const bool diag = (t == (g >> 1));  // holds D[g][g] and D[8 + g][g]
   const bool odd = (g & 1) != 0;
-  for (int p = gw; p < npairs; p += nw) {
+  uint4 wa2[kGroupsPerStep], wb2[kGroupsPerStep];  // the second step buffer
+  for (int pb = blockIdx.x * R; pb < npairs; pb += pstep) {  // uniform over the CTA
+    const int p = pb + lp;
     float d[MT][4];
 #pragma unroll
     for (int i = 0; i < MT; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
-    for (int q0 = 0; q0 < ngrp; q0 += kGroupsPerStep) {
-      if (q0 > 0) load_step(p, q0, ca, cb);
+    auto compute = [&](const uint4 (&xa)[kGroupsPerStep], const uint4 (&xb)[kGroupsPerStep],
+                       int q0) {
 #pragma unroll
       for (int u = 0; u < kGroupsPerStep; ++u) {
         const int q = q0 + u;
-        if (q < ngrp) {
-          const uint32_t wa4[4] = {ca[u].x, ca[u].y, ca[u].z, ca[u].w};
-          const uint32_t wb4[4] = {cb[u].x, cb[u].y, cb[u].z, cb[u].w};
+        if (q < gend) {
+          const uint32_t wa4[4] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w};
+          const uint32_t wb4[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {  // MMA j: bytes 4j..4j+3 of the thread's 16
             uint32_t a0, a2, b0, b2;
@@ -225,32 +245,64 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
           }
         }
       }
+    };
+    // steps double-buffered: one step's loads in flight while the previous
+    // one is computed; the next pair's first step follows the last
+    for (int q0 = gbeg;; q0 += 2 * kGroupsPerStep) {
+      const bool has_w = q0 + kGroupsPerStep < gend;
+      if (has_w) load_step(p, q0 + kGroupsPerStep, wa2, wb2);
+      if (p < npairs) compute(ca, cb, q0);
+      const bool more = q0 + 2 * kGroupsPerStep < gend;
+      if (more) load_step(p, q0 + 2 * kGroupsPerStep, ca, cb);
+      else load_step(p + pstep, gbeg, ca, cb);
+      if (has_w && p < npairs) compute(wa2, wb2, q0 + kGroupsPerStep);
+      if (!more) break;
     }
-    // next pair's first step in flight during the reduction and the stores
-    const int pn = p + nw;
-    if (pn < npairs) load_step(pn, 0, ca, cb);
-    const int ra = SWIGLU ? p : 2 * p;
-    const float fa = sa[ra];
-    const float fb = SWIGLU ? sb[p] : (2 * p + 1 < n ? sb[2 * p + 1] : 0.f);
+    auto store = [&](int pp, int i, float v, float vu) {
+      const int ra = SWIGLU ? pp : 2 * pp;
+      const float fa = sa[ra];
+      const float fb = SWIGLU ? sb[pp] : (2 * pp + 1 < n ? sb[2 * pp + 1] : 0.f);
+      const float inv = scalbnf(1.0f, -sx[i]);
+      const float ga = v * inv * fa, gb = vu * inv * fb;
+      if (SWIGLU) {
+        y[(size_t)i * n + pp] = f32_to_bf16_rne(silu_mul(ga, gb));
+      } else {
+        y[(size_t)i * n + 2 * pp] = f32_to_bf16_rne(ga);
+        if (2 * pp + 1 < n) y[(size_t)i * n + 2 * pp + 1] = f32_to_bf16_rne(gb);
+      }
+    };
+    if (ks == 1) {  // whole pairs per warp: no exchange
 #pragma unroll
-    for (int i = 0; i < MT; ++i) {
-      if (i < m) {
+      for (int i = 0; i < MT; ++i) {
         const float va = diag ? (odd ? d[i][1] : d[i][0]) : 0.f;
         const float vb = diag ? (odd ? d[i][3] : d[i][2]) : 0.f;
         const float v = warp_sum2(va, vb, lane);  // lanes 0-15: first row, 16-31: second
         const float vu = __shfl_sync(0xffffffffu, v, 16);
-        if (lane == 0) {
-          const float inv = scalbnf(1.0f, -sx[i]);
-          const float ga = v * inv * fa, gb = vu * inv * fb;
-          if (SWIGLU) {
-            y[(size_t)i * n + p] = f32_to_bf16_rne(silu_mul(ga, gb));
-          } else {
-            y[(size_t)i * n + 2 * p] = f32_to_bf16_rne(ga);
-            if (2 * p + 1 < n) y[(size_t)i * n + 2 * p + 1] = f32_to_bf16_rne(gb);
-          }
+        if (lane == 0 && p < npairs && i < m) store(p, i, v, vu);
+      }
+      continue;
+    }
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+      const float va = diag ? (odd ? d[i][1] : d[i][0]) : 0.f;
+      const float vb = diag ? (odd ? d[i][3] : d[i][2]) : 0.f;
+      const float v = warp_sum2(va, vb, lane);  // lanes 0-15: first row, 16-31: second
+      if ((lane & 15) == 0) red[warp][i][lane >> 4] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < R * MT) {
+      const int lq = threadIdx.x / MT, i = threadIdx.x - lq * MT;
+      const int pp = pb + lq;
+      if (pp < npairs && i < m) {
+        float v = 0.f, vu = 0.f;
+        for (int s2 = 0; s2 < ks; ++s2) {
+          v += red[lq * ks + s2][i][0];
+          vu += red[lq * ks + s2][i][1];
         }
+        store(pp, i, v, vu);
       }
     }
+    __syncthreads();
   }
 }
 
@@ -265,8 +317,14 @@ cudaError_t run_pair(const DeviceInfo& di, const uint8_t* wa, const float* sa, c
   cudaError_t e = ensure_smem(di, kern, smem);
   if (e != cudaSuccess) return e;
   const int npairs = SWIGLU ? n : (n + 1) / 2;
+  // warps per pair: enough work items for a full grid several times over,
+  // while a slice keeps at least 4 KB of the pair
+  int ks = 1;
+  while (ks < kWarps && (int64_t)npairs * ks < (int64_t)2 * 2 * di.sms * kWarps &&
+         (int64_t)2 * k / (2 * ks) >= 4096)
+    ks *= 2;
   int grid = 2 * di.sms;
-  const int need = (npairs + kWarps - 1) / kWarps;
+  const int need = (npairs + kWarps / ks - 1) / (kWarps / ks);
   if (grid > need) grid = need;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -278,7 +336,7 @@ cudaError_t run_pair(const DeviceInfo& di, const uint8_t* wa, const float* sa, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, wa, sa, wb, sb, n, k, x, m, y);
+  return cudaLaunchKernelEx(&cfg, kern, wa, sa, wb, sb, n, k, x, m, y, ks);
 }
 
 template <bool SWIGLU>

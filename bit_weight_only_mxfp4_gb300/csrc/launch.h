@@ -91,6 +91,15 @@ cudaError_t launch_fp8_swiglu(const uint8_t* gc, const float* gs, const uint8_t*
                               const float* us, int n, int k, const uint16_t* x, int m,
                               uint16_t* h, cudaStream_t s, bool pdl);
 
+// gemv_rows.cu — single-matrix matvecs (dense down projection), m in [1, 8]:
+// MXFP4 on canonical buffers (x staging that does not fit the shared memory:
+// cudaErrorInvalidConfiguration) and bf16
+cudaError_t launch_mxfp4_rows(const uint8_t* codes, const uint8_t* scales, const float* post,
+                              int n, int k, const uint16_t* x, int m, uint16_t* y, cudaStream_t s,
+                              bool pdl);
+cudaError_t launch_bf16_rows(const uint16_t* w, int n, int k, const uint16_t* x, int m,
+                             uint16_t* y, cudaStream_t s, bool pdl);
+
 // gemv_bf16.cu
 cudaError_t launch_swiglu_bf16(const uint16_t* wg, const uint16_t* wu, int n, int k,
                                const uint16_t* x, int m, uint16_t* h, cudaStream_t s, bool pdl);

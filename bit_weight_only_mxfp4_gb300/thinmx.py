@@ -41,6 +41,8 @@ SIGNATURES = {
     "tt_mxfp4_pack_swiglu": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P]),
     "tt_mxfp4_swiglu_matvec": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _P, _P]),
     "tt_bf16_swiglu_matvec": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _I64, _P, _P]),
+    "tt_mxfp4_matvec": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _I64, _P, _P]),
+    "tt_bf16_matvec": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _P, _P]),
     "tt_mxfp4_rows_packed_bytes": (_SZ, [_I64, _I64]),
     "tt_mxfp4_pack_rows": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _SZ, _P]),
     "tt_moe_workspace_bytes": (_SZ, [_I64, _I64, _I32, _I32]),
@@ -194,6 +196,17 @@ def tt_int4_grouped_matvec(codes, scales_f16, zp_u4, n, k, group, x_bf16, m, y_b
     _check("tt_int4_grouped_matvec", load().tt_int4_grouped_matvec(
         _ptr(codes), _ptr(scales_f16), _ptr(zp_u4), n, k, group, _ptr(x_bf16), m, _ptr(y_bf16),
         _stream(stream)))
+
+
+def tt_mxfp4_matvec(codes, scales, postscale, n, k, x_bf16, m, y_bf16, stream=None):
+    _check("tt_mxfp4_matvec", load().tt_mxfp4_matvec(
+        _ptr(codes), _ptr(scales), _ptr(postscale), n, k, _ptr(x_bf16), m, _ptr(y_bf16),
+        _stream(stream)))
+
+
+def tt_bf16_matvec(w, n, k, x_bf16, m, y_bf16, stream=None):
+    _check("tt_bf16_matvec", load().tt_bf16_matvec(
+        _ptr(w), n, k, _ptr(x_bf16), m, _ptr(y_bf16), _stream(stream)))
 
 
 def tt_mxfp4_rows_packed_bytes(n, k) -> int:

@@ -180,6 +180,32 @@ tt_status tt_bf16_swiglu_matvec(const uint16_t* wg, const uint16_t* wu,
                                 int64_t m, uint16_t* h_bf16, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Down projection of a dense decode MLP: single-matrix matvecs.  [DL4 "Why
+ * this was not just normal quantization": the MLP block is gate/up SwiGLU
+ * then the down projection, each projection in the precision its profile
+ * gives it; SHIP 97.87 tok/s notes: layer stacks run as captured CUDA
+ * graphs]  Like the gate/up calls they start streaming weights before
+ * waiting for the preceding kernel (programmatic dependent launch), so a
+ * gate/up -> down pair on one stream overlaps the two.
+ * --------------------------------------------------------------------- */
+
+/* y[i][r] = bf16_rne( post[r] * sum_k W[r][k] * x[i][k] ) on the canonical
+   MXFP4 buffers (codes [n][k/2], scales [n][k/32], postscale [n] or NULL),
+   fp32 accumulation.  x [m][k], y [m][n].  Requires n >= 1,
+   32 <= k <= 16384, k % 32 == 0, 1 <= m <= 8; codes and x 16-byte aligned.
+   A batch whose x does not fit the kernel's shared-memory staging
+   (m * (2k + k/8) bytes) returns TT_ERR_UNSUPPORTED before any launch. */
+tt_status tt_mxfp4_matvec(const uint8_t* codes, const uint8_t* scales, const float* postscale,
+                          int64_t n, int64_t k, const uint16_t* x_bf16, int64_t m,
+                          uint16_t* y_bf16, void* stream);
+
+/* y[i][r] = bf16_rne( sum_k W[r][k] * x[i][k] ), W bf16 [n][k], fp32
+   accumulation.  Requires n >= 1, k % 8 == 0, 1 <= m <= 8; w and x 16-byte
+   aligned. */
+tt_status tt_bf16_matvec(const uint16_t* w, int64_t n, int64_t k, const uint16_t* x_bf16,
+                         int64_t m, uint16_t* y_bf16, void* stream);
+
+/* ------------------------------------------------------------------------
  * Packed single-matrix layout (MoE down projections), sliced by columns:
  * for each 16-wide slice of k, the 8 code bytes of every row in row order,
  * then for each 32-block the E8M0 byte of every row; each part padded to 16
