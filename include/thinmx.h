@@ -158,14 +158,16 @@ tt_status tt_mxfp4_pack_swiglu(const uint8_t* gate_codes,
  *   u[i][r] = post_u[r] * sum_k Wu[r][k] * x[i][k]
  *   h[i][r] = bf16_rne( silu(g) * u ),  silu(g) = g / (1 + exp(-g))
  * with fp32 accumulation.  packed: from tt_mxfp4_pack_swiglu(n, k).
- * x_bf16 [m][k], h_bf16 [m][n]; 1 <= m <= 64.  m <= 3 runs the CUDA-core
- * streaming kernels; m >= 4 the tcgen05 tensor-core kernel when k % 64 == 0
- * and its shared-memory plan fits, else (m <= 8) the CUDA cores again.
- * m > 8 with k % 64 != 0, or a plan that does not fit, returns
- * TT_ERR_UNSUPPORTED before any launch.  The tensor-core kernel multiplies
- * x in f16 after an exact power-of-two prescale per batch row (a row whose
- * first 64 values stay below 1 is lifted to [1, 2)); a scaled value beyond
- * 65504 sets TT_ERR_UNSUPPORTED in the device error word.
+ * x_bf16 [m][k], h_bf16 [m][n]; 1 <= m <= 64.  m = 1 streams the packed
+ * records on CUDA cores; m = 2..8 runs a tile kernel whose multiply-adds go
+ * to the warp-level tensor-core instruction (k <= 5120); the tcgen05
+ * tensor-core kernel serves m >= 9, and m = 4..8 beyond k = 5120, when
+ * k % 64 == 0; the CUDA-core kernels serve the rest of m <= 8.  m > 8 with
+ * k % 64 != 0, or a tensor-core plan that does not fit, returns
+ * TT_ERR_UNSUPPORTED before any launch.  Every kernel multiplies x in f16
+ * after an exact power-of-two prescale (per 32-block and batch row, or on
+ * the tensor-core kernel per batch row from its largest value over all of
+ * k), so every finite bf16 input is served.
  * Requires n >= 1, 32 <= k <= 16384, k % 32 == 0.
  * --------------------------------------------------------------------- */
 tt_status tt_mxfp4_swiglu_matvec(const void* packed, int64_t n, int64_t k,
