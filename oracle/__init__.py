@@ -88,6 +88,8 @@ def _declare(lib):
         "orc_fp8_dequantize": (None, [_P, _P, _I64, _I64, _P]),
         "orc_fp8_matvec": (None, [_P, _P, _I64, _I64, _P, _I64, _P]),
         "orc_fp8_swiglu_matvec": (None, [_P, _P, _P, _P, _I64, _I64, _P, _I64, _P]),
+        "orc_gqa_decode": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I64, _I64,
+                                          ctypes.c_double, _P]),
         "orc_int4_quantize": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P, _P]),
         "orc_int4_dequantize": (None, [_P, _P, _P, _I64, _I64, _I32, _P]),
         "orc_int4_matvec": (None, [_P, _P, _P, _I64, _I64, _I32, _P, _I64, _P]),
@@ -368,3 +370,18 @@ def fp8_swiglu_matvec(gate, up, x_bf16):
     _load().orc_fp8_swiglu_matvec(_ptr(gc), _ptr(gs), _ptr(uc), _ptr(us), n, k,
                                   _ptr(x), m, _ptr(h))
     return h
+
+
+# ---- single-token GQA attention [DL3] --------------------------------------
+def gqa_decode(q_bf16, k_bf16, v_bf16, length, scale):
+    """q [heads, d]; k, v [kv_heads, cap, d] bf16 bits; attends over the
+    first `length` tokens.  Returns (o fp64 [heads, d], status)."""
+    q = _c(q_bf16, np.uint16)
+    k = _c(k_bf16, np.uint16)
+    v = _c(v_bf16, np.uint16)
+    heads, d = q.shape
+    kvh, cap, _ = k.shape
+    o = np.zeros((heads, d), np.float64)
+    st = _load().orc_gqa_decode(_ptr(q), _ptr(k), _ptr(v), heads, kvh, d, cap, int(length),
+                                float(scale), _ptr(o))
+    return o, st

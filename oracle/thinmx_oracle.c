@@ -607,3 +607,50 @@ void orc_fp8_swiglu_matvec(const uint8_t* g_codes, const float* g_scales,
     free(g);
     free(u);
 }
+
+/* ===================================================================== */
+/* Single-token grouped-query attention over a bf16 KV cache             */
+/* ===================================================================== */
+
+/* For query head h, kv_head = h / (heads / kv_heads); over the cached
+   tokens t < len of that kv head: s_t = scale * sum_i q[h][i] * k[t][i],
+   p = softmax(s) over t (with the max subtracted), o[h][i] = sum_t p_t *
+   v[t][i].  q bf16 [heads][d]; k, v bf16 [kv_heads][cap][d] (token t of kv
+   head j at (j * cap + t) * d); o fp64 [heads][d].  Everything in fp64. */
+int orc_gqa_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                   int32_t heads, int32_t kv_heads, int32_t d, int64_t cap,
+                   int64_t len, double scale, double* o)
+{
+    if (heads < 1 || kv_heads < 1 || heads % kv_heads != 0 || d < 1 ||
+        len < 1 || cap < len)
+        return ORC_ERR_SHAPE;
+    const int32_t group = heads / kv_heads;
+    double* s = (double*)malloc(sizeof(double) * (size_t)len);
+    for (int32_t h = 0; h < heads; ++h) {
+        const int32_t j = h / group;
+        const uint16_t* kh = k + (int64_t)j * cap * d;
+        const uint16_t* vh = v + (int64_t)j * cap * d;
+        double mx = -INFINITY;
+        for (int64_t t = 0; t < len; ++t) {
+            double acc = 0.0;
+            for (int32_t i = 0; i < d; ++i)
+                acc += orc_bf16_value(q[(int64_t)h * d + i]) *
+                       orc_bf16_value(kh[t * d + i]);
+            s[t] = acc * scale;
+            if (s[t] > mx) mx = s[t];
+        }
+        double sum = 0.0;
+        for (int64_t t = 0; t < len; ++t) {
+            s[t] = exp(s[t] - mx);
+            sum += s[t];
+        }
+        for (int32_t i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < len; ++t)
+                acc += s[t] * orc_bf16_value(vh[t * d + i]);
+            o[(int64_t)h * d + i] = acc / sum;
+        }
+    }
+    free(s);
+    return ORC_OK;
+}

@@ -27,6 +27,10 @@
  *          BF16) and its FP8 MLP kernel, a scaled matvec whose row sum of
  *          w * x is multiplied by the row's scale.  The element format
  *          (E4M3) and the scale rule (row amax / 448) are not printed.
+ *          The same section's attention kernel: single-token GQA, each
+ *          query head mapped to kv_head = head // (heads // kv_heads),
+ *          scores = sum(key * q) * scale over the cached tokens, with the
+ *          KV cache kept in BF16 ("KV cache: full BF16", causal KV).
  * The pages never spell out the bit formats; E2M1 (1 sign, 2 exponent bits
  * with bias 1, 1 mantissa bit) and E8M0 (8 exponent bits, bias 127, 0xFF =
  * NaN) are the MXFP4 element and scale formats, and the scale rule
@@ -134,6 +138,13 @@ void orc_int4_dequantize(const uint8_t* codes, const uint16_t* scales_f16,
 void orc_int4_matvec(const uint8_t* codes, const uint16_t* scales_f16,
                      const uint8_t* zp, int64_t n, int64_t k, int32_t group,
                      const uint16_t* x_bf16, int64_t m, double* y);
+
+/* ---- single-token GQA attention [DL3] --------------------------------- */
+/* o[h][:] = sum_t softmax_t(scale * q[h] . k[kvh][t]) * v[kvh][t], with
+   kvh = h / (heads / kv_heads), t < len; k, v [kv_heads][cap][d] bf16. */
+int orc_gqa_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                   int32_t heads, int32_t kv_heads, int32_t d, int64_t cap,
+                   int64_t len, double scale, double* o);
 
 #ifdef __cplusplus
 }

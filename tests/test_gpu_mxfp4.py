@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import oracle
-from bit_weight_only_mxfp4_gb300 import synth
+from bit_weight_only_mxfp4_gb300 import synth, thinmx
 
 from . import gpu_util as gu
 from .parity import assert_float_parity, bf16_to_f64
@@ -332,3 +332,57 @@ def test_small_batches_serve_large_activations(k):
                                      (gu.host(uc), gu.host(us), d["pu"]), x)
     for i in range(m):
         assert_float_parity(h[i], ref[i], f"row {i}")
+
+
+@pytest.mark.parametrize("n,k,post", [(5, 32, True), (37, 96, False), (64, 2048, True),
+                                      (7, 2880, True), (3, 5152, False)])
+def test_pack_swiglu_is_a_byte_rearrangement(n, k, post):
+    """The packed gate/up buffer holds exactly the canonical bytes, moved:
+    per output row r, one record [gate codes k/2][up codes k/2][gate scales
+    k/32][up scales k/32][pad to 8][post_g f32][post_u f32][pad to 16], the
+    records back to back (the layout the kernels read).  Every byte is
+    compared, so a layout slip that cancels inside a dot product still
+    fails here."""
+    d = synth.gate_up_inputs(140, 0, n, k, m=1, postscale=post)
+    gc, gs, _ = gu.quantize(d["wg"])
+    uc, us, _ = gu.quantize(d["wu"])
+    gp = None if d["pg"] is None else gu.dev(d["pg"])
+    up = None if d["pu"] is None else gu.dev(d["pu"])
+    packed = gu.host(gu.pack_swiglu(gc, gs, gp, uc, us, up, n, k))
+    nblk = k // 32
+    post_off = (k + 2 * nblk + 7) & ~7
+    rec = (post_off + 8 + 15) & ~15
+    assert packed.size == n * rec
+    recs = packed.reshape(n, rec)
+    assert np.array_equal(recs[:, :k // 2], gu.host(gc))
+    assert np.array_equal(recs[:, k // 2:k], gu.host(uc))
+    assert np.array_equal(recs[:, k:k + nblk], gu.host(gs))
+    assert np.array_equal(recs[:, k + nblk:k + 2 * nblk], gu.host(us))
+    ps = np.ascontiguousarray(recs[:, post_off:post_off + 8]).view(np.float32)
+    want_g = d["pg"] if post else np.ones(n, np.float32)
+    want_u = d["pu"] if post else np.ones(n, np.float32)
+    assert np.array_equal(ps[:, 0].view(np.uint32), want_g.view(np.uint32))
+    assert np.array_equal(ps[:, 1].view(np.uint32), want_u.view(np.uint32))
+    assert not recs[:, k + 2 * nblk:post_off].any() and not recs[:, post_off + 8:].any()
+
+
+@pytest.mark.parametrize("n,k", [(5, 32), (37, 96), (2880, 2880), (9, 5152)])
+def test_pack_rows_is_a_byte_rearrangement(n, k):
+    """The column-sliced single-matrix layout (the MoE down projections):
+    for each 16-wide slice s of k, the 8 code bytes 8s..8s+7 of every row in
+    row order, then for each 32-block b the E8M0 byte of every row; each
+    part padded to 16 bytes."""
+    import torch
+    w = synth.normal_f32(synth.rng(141), (n, k), synth.WEIGHT_STD)
+    codes, scales, _ = gu.quantize(w)
+    nbytes = thinmx.tt_mxfp4_rows_packed_bytes(n, k)
+    packed = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    thinmx.tt_mxfp4_pack_rows(codes, scales, n, k, packed, nbytes)
+    p = gu.host(packed)
+    c, s = gu.host(codes), gu.host(scales)
+    cbytes = (n * (k // 2) + 15) // 16 * 16
+    assert nbytes == cbytes + (n * (k // 32) + 15) // 16 * 16
+    got_codes = p[:n * (k // 2)].reshape(k // 16, n, 8)
+    assert np.array_equal(got_codes, c.reshape(n, k // 16, 8).transpose(1, 0, 2))
+    got_scales = p[cbytes:cbytes + n * (k // 32)].reshape(k // 32, n)
+    assert np.array_equal(got_scales, s.T)

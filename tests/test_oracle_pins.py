@@ -558,3 +558,93 @@ def test_fp8_swiglu_against_expit_and_gate_up_order():
     np.testing.assert_allclose(h, g * expit(g) * u, rtol=1e-12, atol=1e-300)
     swapped = oracle.fp8_swiglu_matvec((uc, us), (gc, gs), x)
     assert not np.allclose(h, swapped)
+
+
+# ---- single-token GQA attention ----------------------------------------------
+def _gqa_inputs(seed, heads, kvh, d, cap, std=1.0):
+    g = np.random.default_rng(seed)
+    q = synth.normal_bf16(g, (heads, d), std)
+    k = synth.normal_bf16(g, (kvh, cap, d), std)
+    v = synth.normal_bf16(g, (kvh, cap, d), 1.0)
+    return q, k, v
+
+
+def _f(b):
+    return synth.bf16_bits_to_f32(b).astype(np.float64)
+
+
+def test_gqa_single_token_returns_its_value_row():
+    q, k, v = _gqa_inputs(1, 8, 2, 16, 5)
+    o, st = oracle.gqa_decode(q, k, v, 1, 0.25)
+    assert st == oracle.OK
+    want = np.repeat(_f(v[:, 0, :]), 4, axis=0)  # heads 0-3 -> kv 0, 4-7 -> kv 1
+    assert np.array_equal(o, want)
+
+
+def test_gqa_zero_scale_gives_the_mean_of_values():
+    q, k, v = _gqa_inputs(2, 4, 4, 8, 37)
+    o, _ = oracle.gqa_decode(q, k, v, 29, 0.0)
+    assert np.allclose(o, _f(v[:, :29, :]).mean(axis=1), rtol=0, atol=1e-15)
+
+
+def test_gqa_head_mapping_is_the_group_of_consecutive_heads():
+    """kv head j serves query heads j*G .. j*G+G-1 (G = heads / kv_heads):
+    with v of kv head j constant j + 1, output head h is h // G + 1."""
+    heads, kvh, d, cap = 12, 3, 8, 6
+    q, k, _ = _gqa_inputs(3, heads, kvh, d, cap)
+    v = np.stack([np.full((cap, d), float(j + 1), np.float32) for j in range(kvh)])
+    o, _ = oracle.gqa_decode(q, k, synth.f32_to_bf16_bits(v), cap, 0.5)
+    # (sum_t p_t c) / (sum_t p_t) is c up to fp64 rounding; a wrong mapping is off by >= 1
+    assert np.allclose(o[:, 0], np.array([h // 4 + 1 for h in range(heads)], np.float64),
+                       rtol=0, atol=1e-12)
+
+
+def test_gqa_equals_multi_head_attention_on_repeated_kv():
+    heads, kvh, d, cap, n = 8, 2, 16, 20, 17
+    q, k, v = _gqa_inputs(4, heads, kvh, d, cap)
+    o, _ = oracle.gqa_decode(q, k, v, n, 0.25)
+    o_mha, _ = oracle.gqa_decode(q, np.repeat(k, 4, axis=0), np.repeat(v, 4, axis=0), n, 0.25)
+    assert np.array_equal(o, o_mha)
+
+
+def test_gqa_matches_scipy_softmax_on_tiny_cases():
+    from scipy.special import softmax
+    for seed, (heads, kvh, d, cap, n) in enumerate([(4, 1, 8, 9, 9), (6, 3, 16, 12, 7),
+                                                    (2, 2, 32, 40, 33)]):
+        q, k, v = _gqa_inputs(10 + seed, heads, kvh, d, cap)
+        scale = 1.0 / np.sqrt(d)
+        o, _ = oracle.gqa_decode(q, k, v, n, scale)
+        G = heads // kvh
+        for h in range(heads):
+            kk, vv = _f(k[h // G, :n]), _f(v[h // G, :n])
+            p = softmax(kk @ _f(q[h]) * scale)
+            assert np.allclose(o[h], p @ vv, rtol=1e-13, atol=1e-14)
+
+
+def test_gqa_token_order_and_tokens_past_len_do_not_matter():
+    heads, kvh, d, cap, n = 4, 2, 8, 16, 11
+    q, k, v = _gqa_inputs(5, heads, kvh, d, cap)
+    o, _ = oracle.gqa_decode(q, k, v, n, 0.3)
+    perm = np.random.default_rng(5).permutation(n)
+    k2, v2 = k.copy(), v.copy()
+    k2[:, :n], v2[:, :n] = k[:, perm], v[:, perm]
+    k2[:, n:] = v2[:, n:] = 0x7FC0  # bf16 NaN beyond len
+    o2, _ = oracle.gqa_decode(q, k2, v2, n, 0.3)
+    assert np.allclose(o, o2, rtol=1e-14, atol=1e-15)
+
+
+def test_gqa_dominant_token_takes_all_the_weight():
+    heads, kvh, d, cap = 2, 1, 4, 6
+    q = synth.f32_to_bf16_bits(np.ones((heads, d), np.float32))
+    k = np.zeros((kvh, cap, d), np.float32)
+    k[0, 3] = 256.0  # score 1024 * scale above every other token's 0
+    v = np.random.default_rng(6).standard_normal((kvh, cap, d)).astype(np.float32)
+    o, _ = oracle.gqa_decode(q, synth.f32_to_bf16_bits(k), synth.f32_to_bf16_bits(v), cap, 1.0)
+    assert np.array_equal(o, np.repeat(_f(synth.f32_to_bf16_bits(v))[:, 3], heads, axis=0))
+
+
+def test_gqa_shape_errors():
+    q, k, v = _gqa_inputs(7, 6, 4, 8, 4)  # 6 heads over 4 kv heads: not a group
+    assert oracle.gqa_decode(q, k, v, 4, 1.0)[1] == oracle.ERR_SHAPE
+    q, k, v = _gqa_inputs(7, 4, 2, 8, 4)
+    assert oracle.gqa_decode(q, k, v, 5, 1.0)[1] == oracle.ERR_SHAPE  # len beyond the cache
