@@ -309,7 +309,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--only", default=None,
-                    choices=["gate_up", "bf16", "moe", "int4", "sweep", "fp8", "mlp"],
+                    choices=["gate_up", "bf16", "moe", "int4", "sweep", "fp8", "mlp", "gqa"],
                     help="run one small workload only (for profiler captures)")
     ap.add_argument("--layers", type=int, default=None,
                     help="with --only moe: MoE layers to build (default: the full stack)")
@@ -356,6 +356,9 @@ def main():
         elif args.only == "int4":
             l2 = torch.cuda.get_device_properties(device).L2_cache_size
             r = int4_workload(torch, synth, thinmx, device, hbm, l2, reps=args.steps)
+        elif args.only == "gqa":
+            l2 = torch.cuda.get_device_properties(device).L2_cache_size
+            r = gqa_workload(torch, synth, thinmx, device, hbm, l2, reps=args.steps)
         elif args.only == "mlp":
             r = mlp_stack_workload(torch, synth, loader, thinmx, device, hbm, reps=args.steps)
         elif args.only == "fp8":
@@ -585,6 +588,8 @@ def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
     torch.cuda.empty_cache()
     out.update(mlp_stack_workload(torch, synth, loader, thinmx, device, hbm))
     torch.cuda.empty_cache()
+    out.update(gqa_workload(torch, synth, thinmx, device, hbm, l2))
+    torch.cuda.empty_cache()
     out.update(moe_workload(torch, synth, loader, thinmx, device, hbm))
     torch.cuda.empty_cache()
     out["peak"] = {"hbm_gbs": hbm, "source": peak_kind,
@@ -792,6 +797,46 @@ def int4_workload(torch, synth, thinmx, device, hbm, l2, reps=50):
     return {c.name: {"us": round(ms * 1e3, 3), "GBps": round(per / (ms * 1e-3) / 1e9, 1),
                      "frac": round(per / (ms * 1e-3) / 1e9 / hbm, 4), "bytes": per,
                      "rotating_copies": copies}}
+
+
+def gqa_bytes(heads, kvh, d, length):
+    """Algorithmic bytes of one decode attention call: the K and V rows read
+    once, q read, out written (bf16)."""
+    return 2 * kvh * length * d * 2 + 2 * heads * d * 2
+
+
+def gqa_workload(torch, synth, thinmx, device, hbm, l2, reps=50):
+    """Single-token GQA attention over a bf16 KV cache (SmolLM3-3B heads
+    16/4/128 and gpt-oss-20b heads 64/8/64; 4096 and 32768 cached tokens),
+    each over rotating caches whose total exceeds twice the L2 size; one
+    workspace shared by the stream-ordered calls."""
+    c = synth.GQA
+    out = {}
+    for model, heads, kvh, d in c.shapes:
+        ws_bytes = thinmx.tt_gqa_decode_workspace_bytes(heads, kvh, d)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
+        for length in c.lens:
+            per = gqa_bytes(heads, kvh, d, length)
+            copies = max(3, int(2 * l2 // per) + 2)
+            bufs = []
+            for i in range(copies):
+                k = synth.torch_normal((kvh, length, d), 1.0, c.wid, i, 1, device).to(torch.bfloat16)
+                v = synth.torch_normal((kvh, length, d), 1.0, c.wid, i, 2, device).to(torch.bfloat16)
+                q = synth.torch_normal((heads, d), 1.0, c.wid, i, 0, device).to(torch.bfloat16)
+                o = torch.empty((heads, d), dtype=torch.bfloat16, device=device)
+                bufs.append((q, k, v, o))
+            scale = 1.0 / d ** 0.5
+            g = capture(torch, lambda: [thinmx.tt_gqa_decode_attention(
+                q, k, v, heads, kvh, d, length, length, scale, o, ws, ws_bytes)
+                for q, k, v, o in bufs])
+            ms = time_graph(torch, g, reps) / copies
+            del bufs, g
+            torch.cuda.empty_cache()
+            gbs = per / (ms * 1e-3) / 1e9
+            out[f"gqa_decode_{model}_h{heads}_kv{kvh}_d{d}_len{length}"] = {
+                "us": round(ms * 1e3, 3), "GBps": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                "bytes": per, "rotating_copies": copies}
+    return out
 
 
 def moe_workload(torch, synth, loader, thinmx, device, hbm, reps=20, layers=None):

@@ -1,6 +1,7 @@
 // The C ABI (include/thinmx.h): host-side validation, then one launch on
 // the caller's stream.  Nothing here allocates device memory or
 // synchronises, except the diagnostic tt_device_error_read.
+#include <cmath>
 #include <map>
 #include <mutex>
 
@@ -373,6 +374,36 @@ tt_status tt_int4_grouped_matvec(const uint8_t* codes, const uint16_t* scales_f1
   const cudaError_t e = tt::launch_int4_matvec(codes, scales_f16, zp_u4, int(n), int(k),
                                                int(group), x_bf16, int(m), y_bf16,
                                                as_stream(stream), kPdl);
+  if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+size_t tt_gqa_decode_workspace_bytes(int32_t heads, int32_t kv_heads, int32_t head_dim) {
+  if (heads < 1 || kv_heads < 1 || heads % kv_heads != 0) return 0;
+  if (head_dim != 64 && head_dim != 128) return 0;
+  if (heads / kv_heads > 16 || kv_heads > tt::kGqaMaxKvHeads) return 0;
+  return tt::gqa_decode_workspace_bytes(heads, kv_heads, head_dim);
+}
+
+tt_status tt_gqa_decode_attention(const uint16_t* q_bf16, const uint16_t* k_cache,
+                                  const uint16_t* v_cache, int32_t heads, int32_t kv_heads,
+                                  int32_t head_dim, int64_t cap, int64_t len, float scale,
+                                  uint16_t* out_bf16, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (heads < 1 || kv_heads < 1 || heads % kv_heads != 0 || head_dim < 1) return TT_ERR_SHAPE;
+  if (len < 1 || cap < len) return TT_ERR_SHAPE;
+  if (!std::isfinite(scale)) return TT_ERR_NONFINITE;
+  if (head_dim != 64 && head_dim != 128) return TT_ERR_UNSUPPORTED;
+  if (heads / kv_heads > 16 || kv_heads > tt::kGqaMaxKvHeads) return TT_ERR_UNSUPPORTED;
+  if (!q_bf16 || !k_cache || !v_cache || !out_bf16 || !workspace) return TT_ERR_NULL;
+  if (workspace_bytes < tt::gqa_decode_workspace_bytes(heads, kv_heads, head_dim))
+    return TT_ERR_SIZE;
+  if (!aligned(q_bf16, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(out_bf16, 16) || !aligned(workspace, 16))
+    return TT_ERR_ALIGN;
+  const cudaError_t e =
+      tt::launch_gqa_decode(q_bf16, k_cache, v_cache, heads, kv_heads, head_dim, cap, len, scale,
+                            out_bf16, workspace, as_stream(stream), kPdl);
   if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
   return from_cuda(e);
 }

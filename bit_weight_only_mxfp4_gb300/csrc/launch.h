@@ -100,6 +100,17 @@ cudaError_t launch_mxfp4_rows(const uint8_t* codes, const uint8_t* scales, const
 cudaError_t launch_bf16_rows(const uint16_t* w, int n, int k, const uint16_t* x, int m,
                              uint16_t* y, cudaStream_t s, bool pdl);
 
+// attention.cu — single-token GQA over a bf16 KV cache, head_dim 64 or 128,
+// up to 16 query heads per kv head, up to 64 kv heads; the workspace holds
+// a counter per kv head (zero between calls) and the split partials.
+constexpr int kGqaCounterBytes = 256;
+constexpr int kGqaMaxKvHeads = kGqaCounterBytes / 4;
+constexpr int kGqaMaxSplits = 256;
+size_t gqa_decode_workspace_bytes(int heads, int kv_heads, int head_dim);
+cudaError_t launch_gqa_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, int heads,
+                              int kv_heads, int head_dim, int64_t cap, int64_t len, float scale,
+                              uint16_t* out, void* ws, cudaStream_t s, bool pdl);
+
 // gemv_bf16.cu
 cudaError_t launch_swiglu_bf16(const uint16_t* wg, const uint16_t* wu, int n, int k,
                                const uint16_t* x, int m, uint16_t* h, cudaStream_t s, bool pdl);

@@ -121,11 +121,23 @@ class Int4QKV:
     name: str = "gptoss20b_int4_qkv_k2880_n5120_g128"
 
 
+@dataclass(frozen=True)
+class GQADecode:
+    """Single-token GQA attention over a bf16 KV cache: SmolLM3-3B heads
+    (16 query heads, 4 kv heads, head_dim 128) and gpt-oss-20b heads (64,
+    8, 64), at short and long contexts."""
+    wid: int = 5
+    shapes: tuple = (("smollm3_3b", 16, 4, 128), ("gptoss20b", 64, 8, 64))
+    lens: tuple = (4096, 32768)
+    name: str = "gqa_decode"
+
+
 GATE_UP = GateUpMLP()
 STACK = DecodeStack()
 SWEEP = BatchSweep()
 MOE = MoELayer()
 QKV = Int4QKV()
+GQA = GQADecode()
 
 
 # --------------------------------------------------------------------------
@@ -164,6 +176,16 @@ def moe_expert_weights(wid: int, layer: int, expert: int, hidden: int, inter: in
     gu = normal_f32(rng(wid, layer, 100 + 2 * expert), (2 * inter, hidden), WEIGHT_STD)
     dn = normal_f32(rng(wid, layer, 101 + 2 * expert), (hidden, inter), WEIGHT_STD)
     return gu, dn
+
+
+def gqa_inputs(wid: int, case: int, heads: int, kv_heads: int, d: int, cap: int,
+               k_std: float = 1.0):
+    """q bf16 [heads][d] ~ N(0,1); k, v bf16 [kv_heads][cap][d] ~ N(0, k_std^2),
+    N(0,1)."""
+    q = normal_bf16(rng(wid, case, 0), (heads, d), 1.0)
+    k = normal_bf16(rng(wid, case, 1), (kv_heads, cap, d), k_std)
+    v = normal_bf16(rng(wid, case, 2), (kv_heads, cap, d), 1.0)
+    return dict(q=q, k=k, v=v)
 
 
 def int4_inputs(wid: int, layer: int, n: int, k: int, m: int = 1):

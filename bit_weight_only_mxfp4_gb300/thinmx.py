@@ -55,6 +55,9 @@ SIGNATURES = {
     "tt_fp8_swiglu_matvec": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _P]),
     "tt_quantize_int4_grouped": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
     "tt_int4_grouped_matvec": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _P]),
+    "tt_gqa_decode_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
+    "tt_gqa_decode_attention": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I64, _I64,
+                                                ctypes.c_float, _P, _P, _SZ, _P]),
 }
 
 
@@ -244,3 +247,14 @@ def tt_moe_mxfp4_topk_mlp_static(x_bf16, hidden, inter, router_w_bf16, n_experts
         _ptr(x_bf16), hidden, inter, _ptr(router_w_bf16), n_experts, top_k,
         _ptr(gate_up_packed), _ptr(down_packed), _ptr(out_bf16), _ptr(out_idx), _ptr(out_prob),
         _stream(stream)))
+
+
+def tt_gqa_decode_workspace_bytes(heads, kv_heads, head_dim) -> int:
+    return int(load().tt_gqa_decode_workspace_bytes(heads, kv_heads, head_dim))
+
+
+def tt_gqa_decode_attention(q_bf16, k_cache, v_cache, heads, kv_heads, head_dim, cap, length,
+                            scale, out_bf16, workspace, workspace_bytes, stream=None):
+    _check("tt_gqa_decode_attention", load().tt_gqa_decode_attention(
+        _ptr(q_bf16), _ptr(k_cache), _ptr(v_cache), heads, kv_heads, head_dim, cap, length,
+        float(scale), _ptr(out_bf16), _ptr(workspace), workspace_bytes, _stream(stream)))

@@ -8,7 +8,8 @@
  *     experts' gate/up/down;
  *   - grouped affine INT4 matvec for the dense Q/K/V/O projections;
  *   - bf16 gate/up SwiGLU matvec for the layers kept in bf16;
- *   - FP8 (E4M3, one scale per row) matvec and gate/up SwiGLU matvec.
+ *   - FP8 (E4M3, one scale per row) matvec and gate/up SwiGLU matvec;
+ *   - single-token grouped-query attention over a bf16 KV cache.
  *
  * Sources.  The method is the ThinTensor decode runtime's:
  *   [DL4]  kerbin.cskartikey.dev/@satvikhardat, "Dev Log #4 — 91–96 tok/s
@@ -21,15 +22,17 @@
  *   [DL2]  same feed, "Dev Log #2": the gated_activation, router and expert
  *          operators of the execution tape.
  *   [DL3]  same feed, "Dev Log #3 — SmolLM3-3B Results": the quality FP8
- *          profile and its per-row-scaled matvec.
+ *          profile and its per-row-scaled matvec; its single-token GQA
+ *          attention kernel over a bf16 KV cache.
  *   [SHIP] stardance.hackclub.com/projects/29750, "Hitting 100hrs and final
  *          ship" (production MXFP4/INT4 quantizers, exact routing, expert
  *          routing on the decode hot path), the MoE drift devlog (block-
  *          scaled matvec over the selected experts; fast_math lost accuracy),
  *          the 97.87 tok/s notes (dense_int4_layers for Q/K/V/O), the fixes
  *          list (affine INT4 with a partial last group; no allocations on
- *          the hot path; device given by the caller) and the wide-matvec
- *          devlog (always loop over K with a bounded tile).
+ *          the hot path; device given by the caller), the wide-matvec
+ *          devlog (always loop over K with a bounded tile) and the graph-mode
+ *          devlog's "What I've Done" (attention over a token bucket).
  *
  * Formats (canonical layouts; the parity surface):
  *   E2M1 code: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa:
@@ -363,6 +366,41 @@ tt_status tt_int4_grouped_matvec(const uint8_t* codes, const uint16_t* scales_f1
                                  const uint8_t* zp_u4, int64_t n, int64_t k, int32_t group,
                                  const uint16_t* x_bf16, int64_t m, uint16_t* y_bf16,
                                  void* stream);
+
+/* ------------------------------------------------------------------------
+ * Single-token GQA attention  [DL3 "Dev Log #3 — SmolLM3-3B Results": the
+ * attention path is single-token GQA, query head h reads kv head
+ * h // (heads // kv_heads), scores = sum(key * q) * scale, KV cache bf16;
+ * SHIP graph-mode devlog, "What I've Done" item 3: the same kernel over a
+ * context of up to a fixed token bucket]
+ *
+ *   G = heads / kv_heads,  j = h / G,  for t < len:
+ *   s[h][t] = scale * sum_i q[h][i] * k[j][t][i]
+ *   o[h][i] = bf16_rne( sum_t softmax_t(s[h][.]) * v[j][t][i] )
+ *
+ * q_bf16 [heads][head_dim]; k_cache, v_cache bf16 [kv_heads][cap][head_dim]
+ * (token t of kv head j at (j * cap + t) * head_dim; only t < len is read);
+ * out_bf16 [heads][head_dim].  Scores are exact bf16 products summed in
+ * fp32; the softmax and the weighted sum are fp32 (the weights carried as
+ * two bf16 terms into the tensor-core product).
+ * Requires heads >= 1, kv_heads >= 1, heads % kv_heads == 0, 1 <= len <= cap,
+ * scale finite (else TT_ERR_SHAPE / TT_ERR_NONFINITE); head_dim 64 or 128,
+ * G <= 16 and kv_heads <= 64 (else TT_ERR_UNSUPPORTED).  q, k_cache,
+ * v_cache, out and workspace 16-byte aligned.
+ * workspace: device, >= tt_gqa_decode_workspace_bytes(...) bytes,
+ * ZERO-FILLED before its first use; its first 256 bytes hold one counter
+ * per kv head, which every call leaves at zero; the split partials follow.
+ * Calls that share a workspace must be ordered on one stream.  After a call
+ * that reported TT_ERR_TIMEOUT through tt_device_error_read, zero the
+ * workspace again.  q and the cache are read after the call waits for the
+ * preceding kernel on the stream (that kernel may append the newest token).
+ * --------------------------------------------------------------------- */
+size_t tt_gqa_decode_workspace_bytes(int32_t heads, int32_t kv_heads, int32_t head_dim);
+tt_status tt_gqa_decode_attention(const uint16_t* q_bf16, const uint16_t* k_cache,
+                                  const uint16_t* v_cache, int32_t heads, int32_t kv_heads,
+                                  int32_t head_dim, int64_t cap, int64_t len, float scale,
+                                  uint16_t* out_bf16, void* workspace, size_t workspace_bytes,
+                                  void* stream);
 
 #ifdef __cplusplus
 }

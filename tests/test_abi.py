@@ -154,3 +154,33 @@ def test_int4_validation_before_launch(lib):
     assert call(0, 2880, 128, 1) == 2
     assert call(5120, 2880, 128, 1, codes=None) == 1
     assert call(5120, 2880, 128, 1, x=A + 2) == 3
+
+
+def test_gqa_validation_before_launch(lib):
+    A = 1 << 20  # never dereferenced: every case fails validation first
+    s = None
+    ws = _st("tt_gqa_decode_workspace_bytes", 64, 8, 64)
+    # counters + 256 split partials of 8 heads x (64 + 2) floats per kv head
+    assert ws == 256 + 8 * 256 * 8 * 66 * 4
+    assert _st("tt_gqa_decode_workspace_bytes", 16, 4, 128) == 256 + 4 * 256 * 4 * 130 * 4
+    assert _st("tt_gqa_decode_workspace_bytes", 12, 1, 64) == 256 + 256 * 12 * 66 * 4
+    assert _st("tt_gqa_decode_workspace_bytes", 15, 4, 128) == 0   # not a group
+    assert _st("tt_gqa_decode_workspace_bytes", 16, 4, 96) == 0    # head_dim
+    assert _st("tt_gqa_decode_workspace_bytes", 68, 4, 64) == 0    # 17-wide groups
+    assert _st("tt_gqa_decode_workspace_bytes", 65, 65, 64) == 0   # more than 64 kv heads
+    call = lambda heads=64, kvh=8, d=64, cap=4096, ln=4096, scale=0.125, q=A, out=A, wsp=A, \
+        wsb=ws: _st("tt_gqa_decode_attention", q, A, A, heads, kvh, d, cap, ln,
+                    ctypes.c_float(scale), out, wsp, wsb, s)
+    assert call(ln=0) == 2
+    assert call(ln=4097) == 2                 # len beyond the cache
+    assert call(heads=60) == 2                # heads not a multiple of kv_heads
+    assert call(d=80) == 5                    # head_dim other than 64 / 128
+    assert call(heads=136, kvh=8, wsb=1 << 30) == 5   # 17-wide groups
+    assert call(heads=65, kvh=65, wsb=1 << 30) == 5   # more than 64 kv heads
+    assert call(scale=float("inf")) == 4
+    assert call(q=None) == 1
+    assert call(wsp=None) == 1
+    assert call(wsb=ws - 16) == 8
+    assert call(q=A + 8) == 3
+    assert call(out=A + 2) == 3
+    assert call(wsp=A + 4) == 3
