@@ -9,6 +9,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "layout.cuh"
+#include "tensor_map.h"
 
 namespace tt {
 
@@ -41,6 +42,20 @@ const DeviceInfo* device_info() {
     g_info_ok[dev] = true;
   }
   return &g_info[dev];
+}
+
+EncodeTiledFn tensor_map_encoder() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
 }
 
 cudaError_t ensure_dynamic_smem(const void* kern, int device, int bytes) {
@@ -393,6 +408,7 @@ tt_status tt_gqa_decode_attention(const uint16_t* q_bf16, const uint16_t* k_cach
   if (heads < 1 || kv_heads < 1 || heads % kv_heads != 0 || head_dim < 1) return TT_ERR_SHAPE;
   if (len < 1 || cap < len) return TT_ERR_SHAPE;
   if (!std::isfinite(scale)) return TT_ERR_NONFINITE;
+  if (cap > (int64_t(1) << 31)) return TT_ERR_UNSUPPORTED;  // TMA coordinates and strides
   if (head_dim != 64 && head_dim != 128) return TT_ERR_UNSUPPORTED;
   if (heads / kv_heads > 16 || kv_heads > tt::kGqaMaxKvHeads) return TT_ERR_UNSUPPORTED;
   if (!q_bf16 || !k_cache || !v_cache || !out_bf16 || !workspace) return TT_ERR_NULL;

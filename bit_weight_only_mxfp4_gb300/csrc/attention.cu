@@ -28,18 +28,21 @@
 // Work layout ("split the tokens"): grid (S splits, kv_heads), 4 warps per
 // CTA, one CTA per SM.  A CTA takes a contiguous range of 32-token tiles of
 // one kv head; its warps take every 4th tile, each with its own ring of
-// shared-memory stages filled by bulk copies (one per cache row, into padded
-// rows so the fragment loads are free of bank conflicts) and an mbarrier per
-// stage.  Each warp keeps an online softmax (running max, sum and output in
+// shared-memory stages and an mbarrier per stage.  A stage is filled by TMA
+// tensor copies of 32 tokens x 64 dims (128 bytes a row, 128-byte swizzle,
+// so the fragment loads are free of bank conflicts); the tensor maps end at
+// len, so rows past the end arrive as zeros and the cache beyond len is
+// never read.  Each warp keeps an online softmax (running max, sum and output in
 // log2 units); the CTA merges its warps and writes one partial (max, sum,
-// unnormalised output per head) to the caller's workspace; the last CTA of a
-// kv head (a counter per kv head) merges the S partials in split order,
-// normalises, rounds to bf16 and resets the counter.
+// unnormalised output per head) to the caller's workspace.  A second kernel,
+// launched programmatically behind the first, merges the S partials of each
+// query head in a fixed order, normalises and rounds to bf16.
 #include <cmath>
 
 #include "common.cuh"
 #include "launch.h"
 #include "mxfp4_core.cuh"
+#include "tensor_map.h"
 
 namespace tt {
 namespace {
@@ -47,15 +50,19 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kTok = 32;  // tokens per tile
+constexpr int kMergeThreads = 256;
+constexpr int kMergeBatch = 8;  // split partials one merge thread loads at once
 constexpr uint32_t kFull = 0xffffffffu;
+
+constexpr int kBox = kTok * 128;  // one TMA box: 32 tokens x 64 dims of bf16
 
 template <int D>
 struct AttnPlan {
-  static constexpr int kRow = 2 * D + 16;         // padded shared-memory row (bytes)
-  static constexpr int kStage = 2 * kTok * kRow;  // K rows, then V rows
+  static constexpr int kCh = D / 64;              // boxes per token range
+  static constexpr int kStage = 2 * kCh * kBox;   // K boxes, then V boxes
   static constexpr int kStages = D == 64 ? 6 : 3;
   static constexpr int kRing = kWarps * kStages * kStage;
-  static constexpr int kSmem = kRing + kWarps * kStages * 8;
+  static constexpr int kSmem = 1024 + kRing + kWarps * kStages * 8;  // + 1024-byte alignment
 };
 
 // Floats per split partial: O [G][D], then max [G], then sum [G]; padded to
@@ -74,6 +81,24 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+__device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// TMA tensor copy of one box at (x = dim, y = token, z = kv head).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Byte offset of 16-byte chunk c of row r in a box written with the 128-byte
+// swizzle (chunk index XOR row mod 8; boxes start 1024-byte aligned).
+__device__ __forceinline__ int swz(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
 // (a, b) -> bf16x2 with a in the low half, round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -91,21 +116,22 @@ __device__ __forceinline__ uint32_t pair_halves(uint32_t a, uint32_t b, int h) {
 }
 
 // The 16-byte piece of a row that lane quad position qd reads for 32-dim
-// chunk c of the score contraction: pieces 2qd (+1 for odd c), so the eight
-// lanes of one shared-memory phase hit eight different bank groups.
+// chunk c of the score contraction: pieces 2qd (+1 for odd c); with the
+// swizzle the eight lanes of one shared-memory phase hit eight different
+// bank groups.
 __device__ __forceinline__ int score_piece(int c, int qd) { return 8 * (c >> 1) + 2 * qd + (c & 1); }
 
 template <int D, int NH>
 __global__ void __launch_bounds__(kThreads, 1)
-    gqa_decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc,
-                      const uint16_t* __restrict__ vc, int G, int64_t cap, int64_t len,
-                      float sl2, uint16_t* __restrict__ out, uint8_t* __restrict__ ws,
+    gqa_decode_kernel(const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const uint16_t* __restrict__ q,
+                      int G, int64_t len, float sl2, float* __restrict__ part0,
                       int32_t* __restrict__ err) {
   using P = AttnPlan<D>;
   constexpr int KC = D / 32;  // 32-dim chunks of the score contraction
   constexpr int MT = D / 16;  // 16-dim tiles of the output
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int last;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, qd = lane & 3;
   const int s = blockIdx.x, S = gridDim.x, j = blockIdx.y;
@@ -115,40 +141,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int mine = te - tb > warp ? int((te - tb - warp + kWarps - 1) / kWarps) : 0;
   uint8_t* ring = smem + warp * (P::kStages * P::kStage);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::kRing) + warp * P::kStages;
-  const uint16_t* kh = kc + int64_t(j) * cap * D;
-  const uint16_t* vh = vc + int64_t(j) * cap * D;
-  unsigned* counter = reinterpret_cast<unsigned*>(ws) + j;
-  float* part0 = reinterpret_cast<float*>(ws + kGqaCounterBytes);
 
   if (lane == 0) {
     for (int i = 0; i < P::kStages; ++i) mbar_init(smem_u32(&bars[i]), 1);
     fence_mbar_init();
+    prefetch_tensor_map(&tmk);
+    prefetch_tensor_map(&tmv);
   }
   __syncwarp();
   pdl_allow_next_grid();
   pdl_wait_prior_grid();  // q and the newest cache rows come from earlier kernels
 
   const uint64_t pol = l2_evict_first_policy();
-  // The warp's i-th tile (tile tb + warp + 4i) into stage i % kStages.
+  // The warp's i-th tile (tile tb + warp + 4i) into stage i % kStages; rows
+  // past len arrive as zeros (their weights are zero too).
   auto issue = [&](int i) {
     const int st = i % P::kStages;
-    const int64_t t0 = (tb + warp + int64_t(kWarps) * i) * kTok;
-    const int nt = len - t0 < kTok ? int(len - t0) : kTok;
-    uint8_t* kd = ring + st * P::kStage;
-    uint8_t* vd = kd + kTok * P::kRow;
-    const uint32_t bar = smem_u32(&bars[st]);
-    if (lane >= nt) {  // rows past the end: zero values (their weights are zero too)
-      uint4* z = reinterpret_cast<uint4*>(vd + lane * P::kRow);
+    const int t0 = int((tb + warp + int64_t(kWarps) * i) * kTok);
+    const uint32_t kd = smem_u32(ring + st * P::kStage), bar = smem_u32(&bars[st]);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, uint32_t(P::kStage));
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    fence_proxy_async_smem();  // this lane's reads and writes of the stage before the copies
-    __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(bar, uint32_t(nt) * 4u * D);
-    __syncwarp();
-    if (lane < nt) {
-      bulk_g2s(smem_u32(kd + lane * P::kRow), kh + (t0 + lane) * D, 2 * D, bar, pol);
-      bulk_g2s(smem_u32(vd + lane * P::kRow), vh + (t0 + lane) * D, 2 * D, bar, pol);
+      for (int h = 0; h < P::kCh; ++h) {
+        tma_load_3d(kd + h * kBox, &tmk, 64 * h, t0, j, bar, pol);
+        tma_load_3d(kd + (P::kCh + h) * kBox, &tmv, 64 * h, t0, j, bar, pol);
+      }
     }
   };
   for (int i = 0; i < mine && i < P::kStages; ++i) issue(i);
@@ -199,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       break;
     }
     const uint8_t* kd = ring + st * P::kStage;
-    const uint8_t* vd = kd + kTok * P::kRow;
+    const uint8_t* vd = kd + P::kCh * kBox;
     const int64_t t0 = (tb + warp + int64_t(kWarps) * i) * kTok;
     const int nt = len - t0 < kTok ? int(len - t0) : kTok;
 
@@ -210,13 +227,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int nh = 0; nh < NH; ++nh)
         sc[tm][nh][0] = sc[tm][nh][1] = sc[tm][nh][2] = sc[tm][nh][3] = 0.f;
-      const uint8_t* r0 = kd + (16 * tm + g) * P::kRow;
-      const uint8_t* r1 = r0 + 8 * P::kRow;
+      const int r0 = 16 * tm + g, r1 = r0 + 8;
 #pragma unroll
       for (int c = 0; c < KC; ++c) {
-        const int off = 16 * score_piece(c, qd);
-        const uint4 a = *reinterpret_cast<const uint4*>(r0 + off);
-        const uint4 b = *reinterpret_cast<const uint4*>(r1 + off);
+        const int p = score_piece(c, qd);
+        const uint8_t* box = kd + (p >> 3) * kBox;
+        const uint4 a = *reinterpret_cast<const uint4*>(box + swz(r0, p & 7));
+        const uint4 b = *reinterpret_cast<const uint4*>(box + swz(r1, p & 7));
 #pragma unroll
         for (int nh = 0; nh < NH; ++nh) {
           mma_bf16(sc[tm][nh], a.x, b.x, a.y, b.y, qf[nh][c].x, qf[nh][c].y);
@@ -290,15 +307,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // V rows 2qd, 2qd + 1, 2qd + 8, 2qd + 9 of the chunk; 16-byte piece g
       // (dims 8g..8g+7) and, for D = 128, piece g + 8 (dims 64 + 8g..)
-      const uint8_t* vr = vd + (16 * tm + 2 * qd) * P::kRow + 16 * g;
-      constexpr int CH = D / 64;
+      constexpr int CH = P::kCh;
+      const int rv = 16 * tm + 2 * qd;
       uint4 v[4][CH];
 #pragma unroll
       for (int ch = 0; ch < CH; ++ch) {
-        v[0][ch] = *reinterpret_cast<const uint4*>(vr + 128 * ch);
-        v[1][ch] = *reinterpret_cast<const uint4*>(vr + P::kRow + 128 * ch);
-        v[2][ch] = *reinterpret_cast<const uint4*>(vr + 8 * P::kRow + 128 * ch);
-        v[3][ch] = *reinterpret_cast<const uint4*>(vr + 9 * P::kRow + 128 * ch);
+        const uint8_t* box = vd + ch * kBox;
+        v[0][ch] = *reinterpret_cast<const uint4*>(box + swz(rv, g));
+        v[1][ch] = *reinterpret_cast<const uint4*>(box + swz(rv + 1, g));
+        v[2][ch] = *reinterpret_cast<const uint4*>(box + swz(rv + 8, g));
+        v[3][ch] = *reinterpret_cast<const uint4*>(box + swz(rv + 9, g));
       }
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
@@ -324,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    fence_proxy_async_smem();  // this lane's reads of the stage before the copy that refills it
     __syncwarp();
     if (i + P::kStages < mine) issue(i + P::kStages);
   }
@@ -382,51 +401,104 @@ __global__ void __launch_bounds__(kThreads, 1)
       part[G * D + G + r] = L;
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(counter, 1u) == unsigned(S - 1);
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
+}
 
-  // ---- the last CTA of this kv head: merge the S partials in split order
+// One query head per CTA: o[h] = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s
+// over the S split partials of its kv head, M = max_s m_s; thread
+// (group sg, chunk c) sums splits sg, sg + NG, ... of dims 4c..4c+3 in
+// order, then the groups are added in order: a fixed summation order.
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads)
+    gqa_merge_kernel(const float* __restrict__ part0, int G, int S, uint16_t* __restrict__ out) {
+  constexpr int NC = D / 4;                // float4 chunks of a head
+  constexpr int NG = kMergeThreads / NC;   // split groups
+  __shared__ float wsh[kGqaMaxSplits];     // 2^(m_s - M) / L
+  __shared__ float red[kMergeThreads / 32];
+  __shared__ float4 acc_sh[NG][NC];
+  const int h = blockIdx.x, j = h / G, r = h - j * G;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = tid % NC, sg = tid / NC;
+  const int PS = partial_floats(G, D);
   const float* pj = part0 + size_t(j) * kGqaMaxSplits * PS;
-  float* wt = reinterpret_cast<float*>(smem);  // [S][16] weights 2^(m_s - M) / L
-  for (int r = warp; r < G; r += kWarps) {
-    float M = -INFINITY;
-    for (int s2 = lane; s2 < S; s2 += 32) M = fmaxf(M, __ldcg(pj + size_t(s2) * PS + G * D + r));
-    M = warp_max(M);
-    float L = 0.f;
-    for (int s2 = lane; s2 < S; s2 += 32) {
-      const float* pp = pj + size_t(s2) * PS + G * D;
-      const float f = exp2f(__ldcg(pp + r) - M);
-      wt[s2 * 16 + r] = f;
-      L = fmaf(__ldcg(pp + G + r), f, L);
+  pdl_allow_next_grid();
+  pdl_wait_prior_grid();  // the split kernel's partials
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 buf[kMergeBatch];
+  auto load_batch = [&](int s0) {
+#pragma unroll
+    for (int b = 0; b < kMergeBatch; ++b) {
+      const int s2 = s0 + NG * b;
+      buf[b] = s2 < S ? __ldcg(reinterpret_cast<const float4*>(pj + size_t(s2) * PS + r * D + 4 * c))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    L = warp_sum(L);
-    const float inv = 1.f / L;
-    for (int s2 = lane; s2 < S; s2 += 32) wt[s2 * 16 + r] *= inv;
-  }
+  };
+  load_batch(sg);  // requested before the weights are known
+  // weights: block max of m, then L = sum l 2^(m - M)
+  const float m = tid < S ? __ldcg(pj + size_t(tid) * PS + G * D + r) : -INFINITY;
+  const float l = tid < S ? __ldcg(pj + size_t(tid) * PS + G * D + G + r) : 0.f;
+  float v = warp_max(m);
+  if (lane == 0) red[warp] = v;
   __syncthreads();
-  for (int c = threadIdx.x; c < G * (D / 4); c += kThreads) {
-    const int r = c / (D / 4), d = 4 * (c - r * (D / 4));
-    const float* src = pj + r * D + d;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int s2 = 0; s2 < S; ++s2) {
-      const float4 p = __ldcg(reinterpret_cast<const float4*>(src + size_t(s2) * PS));
-      const float w = wt[s2 * 16 + r];
-      acc.x = fmaf(p.x, w, acc.x);
-      acc.y = fmaf(p.y, w, acc.y);
-      acc.z = fmaf(p.z, w, acc.z);
-      acc.w = fmaf(p.w, w, acc.w);
+  float M = red[0];
+#pragma unroll
+  for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
+  const float f = tid < S ? exp2f(m - M) : 0.f;
+  __syncthreads();
+  v = warp_sum(l * f);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float L = red[0];
+#pragma unroll
+  for (int w = 1; w < kMergeThreads / 32; ++w) L += red[w];
+  if (tid < S) wsh[tid] = f / L;
+  __syncthreads();
+  for (int s0 = sg;; s0 += NG * kMergeBatch) {
+#pragma unroll
+    for (int b = 0; b < kMergeBatch; ++b) {
+      const int s2 = s0 + NG * b;
+      const float w = s2 < S ? wsh[s2] : 0.f;
+      acc.x = fmaf(buf[b].x, w, acc.x);
+      acc.y = fmaf(buf[b].y, w, acc.y);
+      acc.z = fmaf(buf[b].z, w, acc.z);
+      acc.w = fmaf(buf[b].w, w, acc.w);
+    }
+    if (s0 + NG * kMergeBatch >= S) break;
+    load_batch(s0 + NG * kMergeBatch);
+  }
+  acc_sh[sg][c] = acc;
+  __syncthreads();
+  if (sg == 0) {
+#pragma unroll
+    for (int g2 = 1; g2 < NG; ++g2) {
+      const float4 a = acc_sh[g2][c];
+      acc.x += a.x;
+      acc.y += a.y;
+      acc.z += a.z;
+      acc.w += a.w;
     }
     const uint2 packed = make_uint2(
         uint32_t(f32_to_bf16_rne(acc.x)) | (uint32_t(f32_to_bf16_rne(acc.y)) << 16),
         uint32_t(f32_to_bf16_rne(acc.z)) | (uint32_t(f32_to_bf16_rne(acc.w)) << 16));
-    *reinterpret_cast<uint2*>(out + (int64_t(j) * G + r) * D + d) = packed;
+    *reinterpret_cast<uint2*>(out + int64_t(h) * D + 4 * c) = packed;
   }
-  if (threadIdx.x == 0) *counter = 0u;  // ready for the next call
+}
+
+// Tensor map over one cache: dims (head_dim, len, kv_heads), rows of
+// head_dim bf16 at a stride of cap rows per kv head; box 64 x 32 x 1, 128-byte
+// swizzle; out-of-range rows (t >= len) read as zeros.
+cudaError_t cache_map(CUtensorMap* map, const uint16_t* base, int D, int kv_heads, int64_t cap,
+                      int64_t len) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(len), cuuint64_t(kv_heads)};
+  const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(cap) * D * 2};
+  const cuuint32_t box[3] = {64u, cuuint32_t(kTok), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides,
+          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
 }
 
 template <int D, int NH>
@@ -435,6 +507,9 @@ cudaError_t launch_dn(const DeviceInfo& di, const uint16_t* q, const uint16_t* k
                       float scale, uint16_t* out, void* ws, cudaStream_t s, bool pdl) {
   using P = AttnPlan<D>;
   auto kern = gqa_decode_kernel<D, NH>;
+  CUtensorMap tmk, tmv;
+  if (cudaError_t e = cache_map(&tmk, k, D, kv_heads, cap, len)) return e;
+  if (cudaError_t e = cache_map(&tmv, v, D, kv_heads, cap, len)) return e;
   if (cudaError_t e = ensure_smem(di, kern, P::kSmem)) return e;
   const int64_t T = (len + kTok - 1) / kTok;
   int64_t S = (di.sms + kv_heads - 1) / kv_heads;  // one CTA per SM over all kv heads
@@ -442,6 +517,7 @@ cudaError_t launch_dn(const DeviceInfo& di, const uint16_t* q, const uint16_t* k
   if (S > kGqaMaxSplits) S = kGqaMaxSplits;
   if (S < 1) S = 1;
   const float sl2 = float(double(scale) * 1.4426950408889634);  // log2(e)
+  float* part = static_cast<float*>(ws);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(S), unsigned(kv_heads));
   cfg.blockDim = dim3(kThreads);
@@ -452,16 +528,23 @@ cudaError_t launch_dn(const DeviceInfo& di, const uint16_t* q, const uint16_t* k
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, G, cap, len, sl2, out,
-                            static_cast<uint8_t*>(ws), di.error_word);
+  if (cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmk, tmv, q, G, len, sl2, part,
+                                         di.error_word))
+    return e;
+  // the merge always follows the split kernel programmatically
+  cfg.gridDim = dim3(unsigned(G * kv_heads));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gqa_merge_kernel<D>, static_cast<const float*>(part), G,
+                            int(S), out);
 }
 
 }  // namespace
 
 size_t gqa_decode_workspace_bytes(int heads, int kv_heads, int head_dim) {
   const int G = heads / kv_heads;
-  return size_t(kGqaCounterBytes) +
-         size_t(kv_heads) * kGqaMaxSplits * size_t(partial_floats(G, head_dim)) * 4;
+  return size_t(kv_heads) * kGqaMaxSplits * size_t(partial_floats(G, head_dim)) * 4;
 }
 
 cudaError_t launch_gqa_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, int heads,

@@ -101,10 +101,9 @@ cudaError_t launch_bf16_rows(const uint16_t* w, int n, int k, const uint16_t* x,
                              uint16_t* y, cudaStream_t s, bool pdl);
 
 // attention.cu — single-token GQA over a bf16 KV cache, head_dim 64 or 128,
-// up to 16 query heads per kv head, up to 64 kv heads; the workspace holds
-// a counter per kv head (zero between calls) and the split partials.
-constexpr int kGqaCounterBytes = 256;
-constexpr int kGqaMaxKvHeads = kGqaCounterBytes / 4;
+// up to 16 query heads per kv head, up to 64 kv heads; a split kernel writes
+// per-split partials to the workspace, a merge kernel combines them.
+constexpr int kGqaMaxKvHeads = 64;
 constexpr int kGqaMaxSplits = 256;
 size_t gqa_decode_workspace_bytes(int heads, int kv_heads, int head_dim);
 cudaError_t launch_gqa_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, int heads,

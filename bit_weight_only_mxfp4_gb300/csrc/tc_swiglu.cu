@@ -31,13 +31,11 @@
 // releases the stage.  Warps 0-3 finally read D with tcgen05.ld (warp w owns
 // TMEM lanes 32w..32w+31 = rows), scale by 2^X_row and the postscale, apply
 // silu(g)*u and store bf16.
-#include <cuda.h>  // CUtensorMap (types only; the encoder comes from the runtime's driver entry point)
-
-#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
 #include "layout.cuh"
+#include "tensor_map.h"
 
 namespace tt {
 namespace {
@@ -527,27 +525,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (the
-// library does not link the driver library directly).
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static std::once_flag once;
-  static EncodeTiledFn fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
 }  // namespace
 
 // Deepest raw ring (most k-tiles of packed weights in flight) that fits.
@@ -567,7 +544,7 @@ cudaError_t launch_swiglu_mxfp4_tc(const uint8_t* packed, int n, int k, const ui
   const int nraw = pick_nraw(m, k, di->smem_optin);
   if (nraw == 0) return cudaErrorInvalidConfiguration;
   const TcPlan P(m, k, nraw);
-  EncodeTiledFn enc = encode_fn();
+  EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   const SwigluRecord L(k);
   CUtensorMap map_w, map_x;

@@ -385,15 +385,15 @@ tt_status tt_int4_grouped_matvec(const uint8_t* codes, const uint16_t* scales_f1
  * two bf16 terms into the tensor-core product).
  * Requires heads >= 1, kv_heads >= 1, heads % kv_heads == 0, 1 <= len <= cap,
  * scale finite (else TT_ERR_SHAPE / TT_ERR_NONFINITE); head_dim 64 or 128,
- * G <= 16 and kv_heads <= 64 (else TT_ERR_UNSUPPORTED).  q, k_cache,
+ * G <= 16, kv_heads <= 64 and cap <= 2^31 (else TT_ERR_UNSUPPORTED).  q, k_cache,
  * v_cache, out and workspace 16-byte aligned.
- * workspace: device, >= tt_gqa_decode_workspace_bytes(...) bytes,
- * ZERO-FILLED before its first use; its first 256 bytes hold one counter
- * per kv head, which every call leaves at zero; the split partials follow.
- * Calls that share a workspace must be ordered on one stream.  After a call
- * that reported TT_ERR_TIMEOUT through tt_device_error_read, zero the
- * workspace again.  q and the cache are read after the call waits for the
- * preceding kernel on the stream (that kernel may append the newest token).
+ * workspace: device, >= tt_gqa_decode_workspace_bytes(...) bytes: scratch for
+ * the per-split partial results (no initial contents needed).  Calls that
+ * share a workspace must be ordered on one stream.  The call is two kernels:
+ * the split kernel (token ranges of each kv head, one CTA per SM) and the
+ * merge kernel, launched programmatically behind it.  q and the cache are
+ * read after the call waits for the preceding kernel on the stream (that
+ * kernel may append the newest token).
  * --------------------------------------------------------------------- */
 size_t tt_gqa_decode_workspace_bytes(int32_t heads, int32_t kv_heads, int32_t head_dim);
 tt_status tt_gqa_decode_attention(const uint16_t* q_bf16, const uint16_t* k_cache,

@@ -160,10 +160,10 @@ def test_gqa_validation_before_launch(lib):
     A = 1 << 20  # never dereferenced: every case fails validation first
     s = None
     ws = _st("tt_gqa_decode_workspace_bytes", 64, 8, 64)
-    # counters + 256 split partials of 8 heads x (64 + 2) floats per kv head
-    assert ws == 256 + 8 * 256 * 8 * 66 * 4
-    assert _st("tt_gqa_decode_workspace_bytes", 16, 4, 128) == 256 + 4 * 256 * 4 * 130 * 4
-    assert _st("tt_gqa_decode_workspace_bytes", 12, 1, 64) == 256 + 256 * 12 * 66 * 4
+    # 256 split partials of 8 heads x (64 + 2) floats per kv head
+    assert ws == 8 * 256 * 8 * 66 * 4
+    assert _st("tt_gqa_decode_workspace_bytes", 16, 4, 128) == 4 * 256 * 4 * 130 * 4
+    assert _st("tt_gqa_decode_workspace_bytes", 12, 1, 64) == 256 * 12 * 66 * 4
     assert _st("tt_gqa_decode_workspace_bytes", 15, 4, 128) == 0   # not a group
     assert _st("tt_gqa_decode_workspace_bytes", 16, 4, 96) == 0    # head_dim
     assert _st("tt_gqa_decode_workspace_bytes", 68, 4, 64) == 0    # 17-wide groups

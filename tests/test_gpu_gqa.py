@@ -27,10 +27,11 @@ def _lib():
 
 
 def _workspace(heads, kvh, d):
+    """Scratch with garbage in it: the call needs no initial contents."""
     import torch
     nb = thinmx.tt_gqa_decode_workspace_bytes(heads, kvh, d)
     assert nb > 0
-    return torch.zeros(nb, dtype=torch.uint8, device="cuda"), nb
+    return torch.full((nb,), 0xFF, dtype=torch.uint8, device="cuda"), nb
 
 
 def _run(q, k, v, length, scale, ws=None):
@@ -133,8 +134,6 @@ def test_gqa_workspace_is_reused_across_calls_and_shapes():
         assert thinmx.tt_gqa_decode_workspace_bytes(heads, kvh, d) <= ws[1]
         c = synth.gqa_inputs(WID, 70000 + i, heads, kvh, d, length)
         _check(c["q"], c["k"], c["v"], length, 1.0 / math.sqrt(d), f"reuse {i}", ws=ws)
-    # the counters are back at zero
-    assert int(ws[0][:256].sum().item()) == 0
     torch.cuda.synchronize()
 
 
