@@ -26,13 +26,16 @@
 // exact bf16 x bf16 products summed in fp32.
 //
 // Work layout ("split the tokens"): grid (S splits, kv_heads), 4 warps per
-// CTA, one CTA per SM.  A CTA takes a contiguous range of 32-token tiles of
-// one kv head; its warps take every 4th tile, each with its own ring of
+// CTA, one CTA per SM.  A CTA takes a contiguous range of tiles (64 tokens
+// for head_dim 64, 32 for head_dim 128: 16 KB of K and V either way) of one
+// kv head; its warps take every 4th tile, each with its own ring of
 // shared-memory stages and an mbarrier per stage.  A stage is filled by TMA
-// tensor copies of 32 tokens x 64 dims (128 bytes a row, 128-byte swizzle,
-// so the fragment loads are free of bank conflicts); the tensor maps end at
-// len, so rows past the end arrive as zeros and the cache beyond len is
-// never read.  Each warp keeps an online softmax (running max, sum and output in
+// tensor copies of a tile's tokens x 64 dims (128 bytes a row, 128-byte
+// swizzle, so the fragment loads are free of bank conflicts); the tensor
+// maps end at len, so rows past the end arrive as zeros and the cache beyond
+// len is never read.  Before waiting for the preceding kernel, each warp
+// prefetches its first tiles into L2.  Each warp keeps an online softmax
+// (running max, sum and output in
 // log2 units); the CTA merges its warps and writes one partial (max, sum,
 // unnormalised output per head) to the caller's workspace.  A second kernel,
 // launched programmatically behind the first, merges the S partials of each
@@ -49,18 +52,19 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kTok = 32;  // tokens per tile
 constexpr int kMergeThreads = 256;
 constexpr int kMergeBatch = 8;  // split partials one merge thread loads at once
 constexpr uint32_t kFull = 0xffffffffu;
 
-constexpr int kBox = kTok * 128;  // one TMA box: 32 tokens x 64 dims of bf16
-
+// A tile is kTok tokens; its K and V rows arrive as TMA boxes of kTok
+// tokens x 64 dims (128-byte rows); a stage is 16 KB either way.
 template <int D>
 struct AttnPlan {
+  static constexpr int kTok = D == 64 ? 64 : 32;  // tokens per tile
+  static constexpr int kBox = kTok * 128;         // one TMA box
   static constexpr int kCh = D / 64;              // boxes per token range
   static constexpr int kStage = 2 * kCh * kBox;   // K boxes, then V boxes
-  static constexpr int kStages = D == 64 ? 6 : 3;
+  static constexpr int kStages = 3;
   static constexpr int kRing = kWarps * kStages * kStage;
   static constexpr int kSmem = 1024 + kRing + kWarps * kStages * 8;  // + 1024-byte alignment
 };
@@ -93,6 +97,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// L2 prefetch of one box (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
 }
 
 // Byte offset of 16-byte chunk c of row r in a box written with the 128-byte
@@ -130,6 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using P = AttnPlan<D>;
   constexpr int KC = D / 32;  // 32-dim chunks of the score contraction
   constexpr int MT = D / 16;  // 16-dim tiles of the output
+  constexpr int kTok = P::kTok, kBox = P::kBox;
+  constexpr int TM = kTok / 16;  // 16-token tiles of the scores
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -150,6 +164,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
   pdl_allow_next_grid();
+  // While the preceding kernel finishes: pull the warp's first tiles into L2.
+  // L2 is where every write lands, so rows that kernel still appends are
+  // read fresh by the copies below, which start after the wait.
+  if (lane == 0)
+    for (int i = 0; i < mine && i < P::kStages; ++i) {
+      const int t0 = int((tb + warp + int64_t(kWarps) * i) * kTok);
+#pragma unroll
+      for (int h = 0; h < P::kCh; ++h) {
+        tma_prefetch_3d(&tmk, 64 * h, t0, j);
+        tma_prefetch_3d(&tmv, 64 * h, t0, j);
+      }
+    }
   pdl_wait_prior_grid();  // q and the newest cache rows come from earlier kernels
 
   const uint64_t pol = l2_evict_first_policy();
@@ -221,9 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nt = len - t0 < kTok ? int(len - t0) : kTok;
 
     // scores sc[tm][nh]: tokens 16 tm + (g | g + 8) x heads 8 nh + 2qd + (0 | 1)
-    float sc[2][NH][4];
+    float sc[TM][NH][4];
 #pragma unroll
-    for (int tm = 0; tm < 2; ++tm) {
+    for (int tm = 0; tm < TM; ++tm) {
 #pragma unroll
       for (int nh = 0; nh < NH; ++nh)
         sc[tm][nh][0] = sc[tm][nh][1] = sc[tm][nh][2] = sc[tm][nh][3] = 0.f;
@@ -246,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int nh = 0; nh < NH; ++nh) {
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int tm = 0; tm < 2; ++tm) {
+      for (int tm = 0; tm < TM; ++tm) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int tok = 16 * tm + g + 8 * (e >> 1);
@@ -267,14 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mrun[nh][h] = mn;
       }
 #pragma unroll
-      for (int tm = 0; tm < 2; ++tm) {
+      for (int tm = 0; tm < TM; ++tm) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc[tm][nh][e] = exp2f(sc[tm][nh][e] - mrun[nh][e & 1]);
       }
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        lsum[nh][h] = lsum[nh][h] * alpha[h] + (sc[0][nh][h] + sc[0][nh][h + 2]) +
-                      (sc[1][nh][h] + sc[1][nh][h + 2]);
+      for (int h = 0; h < 2; ++h) {
+        float t = 0.f;
+#pragma unroll
+        for (int tm = 0; tm < TM; ++tm) t += sc[tm][nh][h] + sc[tm][nh][h + 2];
+        lsum[nh][h] = lsum[nh][h] * alpha[h] + t;
+      }
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         o[nh][mt][0] *= alpha[0];
@@ -287,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // O^T += V^T P^T, one 16-token chunk (= score tile tm) at a time
     const int src0 = 4 * (2 * qd) + (g >> 1), src1 = src0 + 4;  // lanes holding tokens 2qd, 2qd+1
 #pragma unroll
-    for (int tm = 0; tm < 2; ++tm) {
+    for (int tm = 0; tm < TM; ++tm) {
       // P^T fragments (hi and lo) for head 8 nh + g, tokens 2qd, 2qd + 1 (b0)
       // and 2qd + 8, 2qd + 9 (b1) of this chunk
       uint32_t bh[NH][2], bl[NH][2];
@@ -484,15 +513,15 @@ __global__ void __launch_bounds__(kMergeThreads)
 }
 
 // Tensor map over one cache: dims (head_dim, len, kv_heads), rows of
-// head_dim bf16 at a stride of cap rows per kv head; box 64 x 32 x 1, 128-byte
+// head_dim bf16 at a stride of cap rows per kv head; box 64 x tok x 1, 128-byte
 // swizzle; out-of-range rows (t >= len) read as zeros.
 cudaError_t cache_map(CUtensorMap* map, const uint16_t* base, int D, int kv_heads, int64_t cap,
-                      int64_t len) {
+                      int64_t len, int tok) {
   EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(len), cuuint64_t(kv_heads)};
   const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(cap) * D * 2};
-  const cuuint32_t box[3] = {64u, cuuint32_t(kTok), 1u};
+  const cuuint32_t box[3] = {64u, cuuint32_t(tok), 1u};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides,
           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -508,10 +537,10 @@ cudaError_t launch_dn(const DeviceInfo& di, const uint16_t* q, const uint16_t* k
   using P = AttnPlan<D>;
   auto kern = gqa_decode_kernel<D, NH>;
   CUtensorMap tmk, tmv;
-  if (cudaError_t e = cache_map(&tmk, k, D, kv_heads, cap, len)) return e;
-  if (cudaError_t e = cache_map(&tmv, v, D, kv_heads, cap, len)) return e;
+  if (cudaError_t e = cache_map(&tmk, k, D, kv_heads, cap, len, P::kTok)) return e;
+  if (cudaError_t e = cache_map(&tmv, v, D, kv_heads, cap, len, P::kTok)) return e;
   if (cudaError_t e = ensure_smem(di, kern, P::kSmem)) return e;
-  const int64_t T = (len + kTok - 1) / kTok;
+  const int64_t T = (len + P::kTok - 1) / P::kTok;
   int64_t S = (di.sms + kv_heads - 1) / kv_heads;  // one CTA per SM over all kv heads
   if (S > T) S = T;
   if (S > kGqaMaxSplits) S = kGqaMaxSplits;

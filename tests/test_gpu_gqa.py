@@ -76,10 +76,12 @@ def test_gqa_shapes(heads, kvh, d, cap, length):
 
 
 @pytest.mark.parametrize("length", [1, 2, 31, 32, 33, 63, 64, 65, 127, 128, 129, 4095, 4097])
-def test_gqa_tile_edges(length):
-    heads, kvh, d = 16, 4, 128
-    c = synth.gqa_inputs(WID, 50000 + length, heads, kvh, d, length + 3)
-    _check(c["q"], c["k"], c["v"], length, 1.0 / math.sqrt(d), f"gqa len {length}")
+@pytest.mark.parametrize("heads,kvh,d", [(16, 4, 128), (64, 8, 64)])
+def test_gqa_tile_edges(heads, kvh, d, length):
+    """Tiles are 32 tokens (head_dim 128) or 64 (head_dim 64): lengths around
+    their multiples, and around the split boundaries of a short context."""
+    c = synth.gqa_inputs(WID, 50000 + length + d, heads, kvh, d, length + 3)
+    _check(c["q"], c["k"], c["v"], length, 1.0 / math.sqrt(d), f"gqa d {d} len {length}")
 
 
 @pytest.mark.parametrize("heads,kvh,d", [(16, 4, 128), (64, 8, 64)])
