@@ -442,7 +442,6 @@ __global__ void __launch_bounds__(kMergeThreads)
   constexpr int NC = D / 4;                // float4 chunks of a head
   constexpr int NG = kMergeThreads / NC;   // split groups
   __shared__ float wsh[kGqaMaxSplits];     // 2^(m_s - M) / L
-  __shared__ float red[kMergeThreads / 32];
   __shared__ float4 acc_sh[NG][NC];
   const int h = blockIdx.x, j = h / G, r = h - j * G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -462,24 +461,30 @@ __global__ void __launch_bounds__(kMergeThreads)
     }
   };
   load_batch(sg);  // requested before the weights are known
-  // weights: block max of m, then L = sum l 2^(m - M)
-  const float m = tid < S ? __ldcg(pj + size_t(tid) * PS + G * D + r) : -INFINITY;
-  const float l = tid < S ? __ldcg(pj + size_t(tid) * PS + G * D + G + r) : 0.f;
-  float v = warp_max(m);
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float M = red[0];
+  // warp 0: M = max m, L = sum l 2^(m - M), the weights 2^(m - M) / L
+  if (warp == 0) {
+    constexpr int kPer = kGqaMaxSplits / 32;
+    float m[kPer], l[kPer];
+    float M = -INFINITY;
 #pragma unroll
-  for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
-  const float f = tid < S ? exp2f(m - M) : 0.f;
-  __syncthreads();
-  v = warp_sum(l * f);
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float L = red[0];
+    for (int b = 0; b < kPer; ++b) {
+      const int s2 = lane + 32 * b;
+      m[b] = s2 < S ? __ldcg(pj + size_t(s2) * PS + G * D + r) : -INFINITY;
+      l[b] = s2 < S ? __ldcg(pj + size_t(s2) * PS + G * D + G + r) : 0.f;
+      M = fmaxf(M, m[b]);
+    }
+    M = warp_max(M);
+    float L = 0.f;
 #pragma unroll
-  for (int w = 1; w < kMergeThreads / 32; ++w) L += red[w];
-  if (tid < S) wsh[tid] = f / L;
+    for (int b = 0; b < kPer; ++b) {
+      m[b] = lane + 32 * b < S ? exp2f(m[b] - M) : 0.f;
+      L = fmaf(l[b], m[b], L);
+    }
+    const float inv = 1.f / warp_sum(L);
+#pragma unroll
+    for (int b = 0; b < kPer; ++b)
+      if (lane + 32 * b < S) wsh[lane + 32 * b] = m[b] * inv;
+  }
   __syncthreads();
   for (int s0 = sg;; s0 += NG * kMergeBatch) {
 #pragma unroll
