@@ -313,6 +313,8 @@ def main():
                     help="run one small workload only (for profiler captures)")
     ap.add_argument("--layers", type=int, default=None,
                     help="with --only moe: MoE layers to build (default: the full stack)")
+    ap.add_argument("--gqa", default=None,
+                    help="with --only gqa: one case, model:len (e.g. gptoss20b:32768)")
     ap.add_argument("--ms", default=None,
                     help="with --only sweep: comma-separated batch sizes (default: all)")
     args = ap.parse_args()
@@ -358,7 +360,8 @@ def main():
             r = int4_workload(torch, synth, thinmx, device, hbm, l2, reps=args.steps)
         elif args.only == "gqa":
             l2 = torch.cuda.get_device_properties(device).L2_cache_size
-            r = gqa_workload(torch, synth, thinmx, device, hbm, l2, reps=args.steps)
+            r = gqa_workload(torch, synth, thinmx, device, hbm, l2, reps=args.steps,
+                             case=args.gqa)
         elif args.only == "mlp":
             r = mlp_stack_workload(torch, synth, loader, thinmx, device, hbm, reps=args.steps)
         elif args.only == "fp8":
@@ -805,17 +808,22 @@ def gqa_bytes(heads, kvh, d, length):
     return 2 * kvh * length * d * 2 + 2 * heads * d * 2
 
 
-def gqa_workload(torch, synth, thinmx, device, hbm, l2, reps=50):
+def gqa_workload(torch, synth, thinmx, device, hbm, l2, reps=50, case=None):
     """Single-token GQA attention over a bf16 KV cache (SmolLM3-3B heads
     16/4/128 and gpt-oss-20b heads 64/8/64; 4096 and 32768 cached tokens),
     each over rotating caches whose total exceeds twice the L2 size; one
-    workspace shared by the stream-ordered calls."""
+    workspace shared by the stream-ordered calls.  `case` ("model:len")
+    keeps one of them."""
     c = synth.GQA
     out = {}
     for model, heads, kvh, d in c.shapes:
+        if case and not case.startswith(model + ":"):
+            continue
         ws_bytes = thinmx.tt_gqa_decode_workspace_bytes(heads, kvh, d)
         ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
         for length in c.lens:
+            if case and case != f"{model}:{length}":
+                continue
             per = gqa_bytes(heads, kvh, d, length)
             copies = max(3, int(2 * l2 // per) + 2)
             bufs = []
