@@ -90,6 +90,13 @@ def _declare(lib):
         "orc_fp8_swiglu_matvec": (None, [_P, _P, _P, _P, _I64, _I64, _P, _I64, _P]),
         "orc_gqa_decode": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I64, _I64,
                                           ctypes.c_double, _P]),
+        "orc_lowbit_plane_bytes": (_I64, [_I64]),
+        "orc_lowbit_scale_bytes": (_I64, [_I64]),
+        "orc_lowbit_matrix_bytes": (_I64, [_I32, _I64, _I64]),
+        "orc_lowbit_quantize": (ctypes.c_int, [_I32, _P, _I64, _I64, _P]),
+        "orc_lowbit_dequantize": (None, [_I32, _P, _I64, _I64, _P]),
+        "orc_moe_lowbit_mlp": (ctypes.c_int, [_I32, _P, _I64, _I64, _P, _I32, _I32, _P, _P,
+                                              _P, _P, _P, _P, _P]),
         "orc_int4_quantize": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P, _P]),
         "orc_int4_dequantize": (None, [_P, _P, _P, _I64, _I64, _I32, _P]),
         "orc_int4_matvec": (None, [_P, _P, _P, _I64, _I64, _I32, _P, _I64, _P]),
@@ -385,3 +392,54 @@ def gqa_decode(q_bf16, k_bf16, v_bf16, length, scale):
     st = _load().orc_gqa_decode(_ptr(q), _ptr(k), _ptr(v), heads, kvh, d, cap, int(length),
                                 float(scale), _ptr(o))
     return o, st
+
+
+# ---- Q1 / Q2 packed low-bit experts ----------------------------------------
+def lowbit_matrix_bytes(bits, n, k) -> int:
+    return int(_load().orc_lowbit_matrix_bytes(bits, n, k))
+
+
+def lowbit_plane_bytes(k) -> int:
+    return int(_load().orc_lowbit_plane_bytes(k))
+
+
+def lowbit_scale_bytes(k) -> int:
+    return int(_load().orc_lowbit_scale_bytes(k))
+
+
+def lowbit_quantize(bits, w):
+    """fp32 [n, k] -> (buffer uint8 [lowbit_matrix_bytes], status)."""
+    w = _c(w, np.float32)
+    n, k = w.shape
+    buf = np.zeros(lowbit_matrix_bytes(bits, n, k), np.uint8)
+    st = _load().orc_lowbit_quantize(bits, _ptr(w), n, k, _ptr(buf))
+    return buf, st
+
+
+def lowbit_dequantize(bits, buf, n, k):
+    buf = _c(buf, np.uint8)
+    out = np.zeros((n, k), np.float64)
+    _load().orc_lowbit_dequantize(bits, _ptr(buf), n, k, _ptr(out))
+    return out
+
+
+def moe_lowbit_mlp(bits, x_bf16, wr_bf16, top_k, gu, dn, inter):
+    """gu [E, gate/up matrix bytes] ([2 inter][hidden] each), dn [E, down
+    matrix bytes] ([hidden][inter] each).  Returns (out fp64 [hidden],
+    idx [top_k], p fp64 [top_k], logits32 [E], h fp64 [top_k, inter],
+    status)."""
+    x = _c(x_bf16, np.uint16).ravel()
+    wr = _c(wr_bf16, np.uint16)
+    gu = _c(gu, np.uint8)
+    dn = _c(dn, np.uint8)
+    e, hidden = wr.shape
+    out = np.zeros(hidden, np.float64)
+    idx = np.zeros(top_k, np.int32)
+    p = np.zeros(top_k, np.float64)
+    lg = np.zeros(e, np.float32)
+    h = np.zeros((top_k, inter), np.float64)
+    st = _load().orc_moe_lowbit_mlp(bits, _ptr(x), hidden, inter, _ptr(wr), e, top_k,
+                                    _ptr(gu), _ptr(dn), _ptr(out), _ptr(idx), _ptr(p),
+                                    _ptr(lg), _ptr(h))
+    return out, idx, p, lg, h, st
+

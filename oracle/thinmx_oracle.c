@@ -654,3 +654,170 @@ int orc_gqa_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     free(s);
     return ORC_OK;
 }
+
+/* ===================================================================== */
+/* Q1 / Q2 packed low-bit experts                                         */
+/* ===================================================================== */
+
+/* Layout of one matrix [n][k] (n rows = outputs, k = reduction), written
+   as one buffer:
+     plane 0 [n][P], then (Q2 only) plane 1 [n][P], then scales [n][S];
+   P = ceil(k/8) rounded up to 16 bytes, S = ceil(k/128) rounded up to 16.
+   Bit (kk mod 8) of byte kk/8 of a row's plane p holds bit p of the code
+   of element kk; padding bytes are zero.  Scale byte: E8M0 of the block's
+   step 2^X. */
+#define LB_BLOCK 128
+
+static int64_t round_up16(int64_t v) { return (v + 15) / 16 * 16; }
+
+int64_t orc_lowbit_plane_bytes(int64_t k) { return round_up16((k + 7) / 8); }
+int64_t orc_lowbit_scale_bytes(int64_t k)
+{
+    return round_up16((k + LB_BLOCK - 1) / LB_BLOCK);
+}
+int64_t orc_lowbit_matrix_bytes(int32_t bits, int64_t n, int64_t k)
+{
+    return n * ((int64_t)bits * orc_lowbit_plane_bytes(k) +
+                orc_lowbit_scale_bytes(k));
+}
+
+/* The block's step exponent X: m = (sum of |w| in order, in fp64) / count;
+   X = floor(log2 m) + (m's mantissa in [1, 2) above 1.5), so that 2^X is
+   the power of two nearest m (ties to the lower one); clamped to
+   [-127, 127].  An all-zero block gives -127; a block holding a NaN/Inf
+   gives 128 (no valid exponent). */
+static int lowbit_block_exponent(const float* w, int64_t cnt)
+{
+    double s = 0.0;
+    for (int64_t i = 0; i < cnt; ++i) {
+        if (!isfinite(w[i])) return 128;
+        s += fabs((double)w[i]);
+    }
+    if (s == 0.0) return -127;
+    const double m = s / (double)cnt;
+    int e;
+    const double f = frexp(m, &e); /* m = f * 2^e, f in [0.5, 1) */
+    int x = (e - 1) + (2.0 * f > 1.5 ? 1 : 0);
+    if (x < -127) x = -127;
+    if (x > 127) x = 127;
+    return x;
+}
+
+/* Q1: code 1 for w < 0, else 0 (value (1 - 2c) * 2^X).
+   Q2: code q = clamp(floor(w / 2^X) + 2, 0, 3) (value (q - 1.5) * 2^X:
+   the nearest of the levels -1.5, -0.5, 0.5, 1.5 steps, a tie at a
+   multiple of the step going up). */
+int orc_lowbit_quantize(int32_t bits, const float* w, int64_t n, int64_t k,
+                        uint8_t* buf)
+{
+    if ((bits != 1 && bits != 2) || n < 0 || k < 1) return ORC_ERR_SHAPE;
+    const int64_t P = orc_lowbit_plane_bytes(k), S = orc_lowbit_scale_bytes(k);
+    memset(buf, 0, (size_t)orc_lowbit_matrix_bytes(bits, n, k));
+    int status = ORC_OK;
+    for (int64_t r = 0; r < n; ++r) {
+        const float* row = w + r * k;
+        for (int64_t b0 = 0; b0 < k; b0 += LB_BLOCK) {
+            const int64_t cnt = (k - b0 < LB_BLOCK) ? k - b0 : LB_BLOCK;
+            const int x = lowbit_block_exponent(row + b0, cnt);
+            uint8_t* sc = buf + (int64_t)bits * n * P + r * S + b0 / LB_BLOCK;
+            if (x == 128) { /* NaN/Inf: NaN scale, zero codes */
+                *sc = 0xFF;
+                status = ORC_ERR_NONFINITE;
+                continue;
+            }
+            *sc = (uint8_t)(x + 127);
+            const double t = ldexp(1.0, x);
+            for (int64_t i = 0; i < cnt; ++i) {
+                const int64_t kk = b0 + i;
+                unsigned code;
+                if (bits == 1) {
+                    code = row[kk] < 0.0f ? 1u : 0u;
+                } else {
+                    double q = floor((double)row[kk] / t) + 2.0;
+                    if (q < 0.0) q = 0.0;
+                    if (q > 3.0) q = 3.0;
+                    code = (unsigned)q;
+                }
+                for (int32_t p = 0; p < bits; ++p)
+                    if ((code >> p) & 1u)
+                        buf[p * n * P + r * P + kk / 8] |= (uint8_t)(1u << (kk % 8));
+            }
+        }
+    }
+    return status;
+}
+
+static double lowbit_weight(int32_t bits, const uint8_t* buf, int64_t n,
+                            int64_t k, int64_t r, int64_t kk)
+{
+    const int64_t P = orc_lowbit_plane_bytes(k), S = orc_lowbit_scale_bytes(k);
+    unsigned code = 0;
+    for (int32_t p = 0; p < bits; ++p)
+        code |= ((buf[p * n * P + r * P + kk / 8] >> (kk % 8)) & 1u) << p;
+    const double t =
+        orc_e8m0_value(buf[(int64_t)bits * n * P + r * S + kk / LB_BLOCK]);
+    if (bits == 1) return (code ? -1.0 : 1.0) * t;
+    return ((double)code - 1.5) * t;
+}
+
+void orc_lowbit_dequantize(int32_t bits, const uint8_t* buf, int64_t n,
+                           int64_t k, double* out)
+{
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t kk = 0; kk < k; ++kk)
+            out[r * k + kk] = lowbit_weight(bits, buf, n, k, r, kk);
+}
+
+/* y[r] = sum_k deq[r][k] * v[k] with an fp64 vector v. */
+static void lowbit_matvec_f64(int32_t bits, const uint8_t* buf, int64_t n,
+                              int64_t k, const double* v, double* y)
+{
+    for (int64_t r = 0; r < n; ++r) {
+        double acc = 0.0;
+        for (int64_t kk = 0; kk < k; ++kk)
+            acc += lowbit_weight(bits, buf, n, k, r, kk) * v[kk];
+        y[r] = acc;
+    }
+}
+
+/* The MoE layer with Q1 / Q2 experts: router logits, top-k on their fp32
+   roundings, softmax over the selected, then for each selected expert j
+   h_j = silu(gate_j x) * up_j x (gate = rows [0, inter) of the expert's
+   gate/up matrix [2 inter][hidden], up = rows [inter, 2 inter)), and
+   out = sum_j p_j down_j h_j (down [hidden][inter]).  gu / dn hold the E
+   experts' buffers back to back; h [top_k][inter] returns the h_j. */
+int orc_moe_lowbit_mlp(int32_t bits, const uint16_t* x_bf16, int64_t hidden,
+                       int64_t inter, const uint16_t* wr_bf16,
+                       int32_t n_experts, int32_t top_k, const uint8_t* gu,
+                       const uint8_t* dn, double* out, int32_t* idx, double* p,
+                       float* logits32, double* h)
+{
+    if ((bits != 1 && bits != 2) || top_k < 1 || top_k > n_experts ||
+        hidden < 1 || inter < 1)
+        return ORC_ERR_SHAPE;
+    double* logits = (double*)malloc(sizeof(double) * (size_t)n_experts);
+    orc_router_logits(x_bf16, wr_bf16, n_experts, hidden, logits);
+    for (int32_t e = 0; e < n_experts; ++e) logits32[e] = (float)logits[e];
+    orc_topk(logits32, n_experts, top_k, idx);
+    orc_softmax_selected(logits32, idx, top_k, p);
+
+    double* xv = (double*)malloc(sizeof(double) * (size_t)hidden);
+    double* g = (double*)malloc(sizeof(double) * (size_t)(2 * inter));
+    double* y = (double*)malloc(sizeof(double) * (size_t)hidden);
+    for (int64_t kk = 0; kk < hidden; ++kk) xv[kk] = orc_bf16_value(x_bf16[kk]);
+    for (int64_t r = 0; r < hidden; ++r) out[r] = 0.0;
+    const int64_t gu_bytes = orc_lowbit_matrix_bytes(bits, 2 * inter, hidden);
+    const int64_t dn_bytes = orc_lowbit_matrix_bytes(bits, hidden, inter);
+    for (int32_t j = 0; j < top_k; ++j) {
+        const int64_t e = idx[j];
+        /* gate and up rows of one matrix: g[0, inter) and g[inter, 2 inter) */
+        lowbit_matvec_f64(bits, gu + e * gu_bytes, 2 * inter, hidden, xv, g);
+        double* hj = h + (int64_t)j * inter;
+        orc_swiglu(g, g + inter, inter, hj);
+        lowbit_matvec_f64(bits, dn + e * dn_bytes, hidden, inter, hj, y);
+        for (int64_t r = 0; r < hidden; ++r) out[r] += p[j] * y[r];
+    }
+    free(logits); free(xv); free(g); free(y);
+    return ORC_OK;
+}
+

@@ -31,6 +31,14 @@
  *          query head mapped to kv_head = head // (heads // kv_heads),
  *          scores = sum(key * q) * scale over the cached tokens, with the
  *          KV cache kept in BF16 ("KV cache: full BF16", causal KV).
+ *   [SHIP] also: the 97.87 tok/s notes pack the MoE experts of layers
+ *          0:24 as 1-bit "Q1" structures (packed_expert_q1_layers), 9.52
+ *          GB of MXFP4 experts becoming 2.38 GB, and the final devlog names
+ *          Q2 and Q1 quantizers and a low-bit selected-expert SwiGLU
+ *          kernel.  The encoding is not printed; the reading taken here is
+ *          the one the 4x footprint ratio fixes for an MX-style format: one
+ *          bit (Q1) or two (Q2) per weight plus one E8M0 byte per 128
+ *          weights (1 + 8/128 = 1.0625 bits against MXFP4's 4.25).
  * The pages never spell out the bit formats; E2M1 (1 sign, 2 exponent bits
  * with bias 1, 1 mantissa bit) and E8M0 (8 exponent bits, bias 127, 0xFF =
  * NaN) are the MXFP4 element and scale formats, and the scale rule
@@ -145,6 +153,25 @@ void orc_int4_matvec(const uint8_t* codes, const uint16_t* scales_f16,
 int orc_gqa_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                    int32_t heads, int32_t kv_heads, int32_t d, int64_t cap,
                    int64_t len, double scale, double* o);
+
+/* ---- Q1 / Q2 packed low-bit experts [SHIP] ---------------------------- */
+/* bits 1 or 2 per weight, one E8M0 step 2^X per block of 128 along k (the
+   last block may be partial); X = the power of two nearest the block's
+   mean |w|; Q1 code = sign, Q2 code = clamp(floor(w / 2^X) + 2, 0, 3).
+   Buffer layout: plane 0 [n][P] (+ plane 1 [n][P] for Q2), scales [n][S],
+   P = ceil(k/8) and S = ceil(k/128), each rounded up to 16 bytes. */
+int64_t orc_lowbit_plane_bytes(int64_t k);
+int64_t orc_lowbit_scale_bytes(int64_t k);
+int64_t orc_lowbit_matrix_bytes(int32_t bits, int64_t n, int64_t k);
+int  orc_lowbit_quantize(int32_t bits, const float* w, int64_t n, int64_t k,
+                         uint8_t* buf);
+void orc_lowbit_dequantize(int32_t bits, const uint8_t* buf, int64_t n,
+                           int64_t k, double* out);
+int  orc_moe_lowbit_mlp(int32_t bits, const uint16_t* x_bf16, int64_t hidden,
+                        int64_t inter, const uint16_t* wr_bf16,
+                        int32_t n_experts, int32_t top_k, const uint8_t* gu,
+                        const uint8_t* dn, double* out, int32_t* idx,
+                        double* p, float* logits32, double* h);
 
 #ifdef __cplusplus
 }

@@ -648,3 +648,165 @@ def test_gqa_shape_errors():
     assert oracle.gqa_decode(q, k, v, 4, 1.0)[1] == oracle.ERR_SHAPE
     q, k, v = _gqa_inputs(7, 4, 2, 8, 4)
     assert oracle.gqa_decode(q, k, v, 5, 1.0)[1] == oracle.ERR_SHAPE  # len beyond the cache
+
+
+# ---- Q1 / Q2 packed low-bit experts -----------------------------------------
+def _lowbit_plane_bits(buf, bits, n, k, p, r):
+    P = oracle.lowbit_plane_bytes(k)
+    row = buf[p * n * P + r * P: p * n * P + (r + 1) * P]
+    return np.unpackbits(row, bitorder="little")[:k]
+
+
+def _lowbit_scale(buf, bits, n, k, r, b):
+    P, S = oracle.lowbit_plane_bytes(k), oracle.lowbit_scale_bytes(k)
+    return int(buf[bits * n * P + r * S + b])
+
+
+def test_lowbit_worked_blocks():
+    for row in (" ".join(r) for r in _rows("lowbit_worked_blocks.txt")):
+        case, sb, q1b, q1v, q2b, q2v = [part.split() for part in row.split("|")]
+        w = np.array([[float(v) for v in case[1:]]], np.float32)
+        k = w.shape[1]
+        for bits, planes, vals in ((1, q1b, q1v), (2, q2b, q2v)):
+            buf, st = oracle.lowbit_quantize(bits, w)
+            assert st == oracle.OK
+            P = oracle.lowbit_plane_bytes(k)
+            assert _lowbit_scale(buf, bits, 1, k, 0, 0) == int(sb[0]), case[0]
+            for p, byte in enumerate(planes):
+                assert buf[p * P] == int(byte), (case[0], bits, p)
+            deq = oracle.lowbit_dequantize(bits, buf, 1, k)
+            assert np.array_equal(deq[0], np.array([float(v) for v in vals])), (case[0], bits)
+
+
+@pytest.mark.parametrize("bits", [1, 2])
+def test_lowbit_layout_and_padding(bits):
+    n, k = 3, 130  # a full block of 128 and a partial block of 2
+    P, S = oracle.lowbit_plane_bytes(k), oracle.lowbit_scale_bytes(k)
+    assert (P, S) == (32, 16)
+    assert oracle.lowbit_matrix_bytes(bits, n, k) == n * (bits * 32 + 16)
+    w = np.random.default_rng(40).standard_normal((n, k)).astype(np.float32)
+    buf, st = oracle.lowbit_quantize(bits, w)
+    assert st == oracle.OK
+    for p in range(bits):
+        for r in range(n):
+            row = buf[p * n * P + r * P: p * n * P + (r + 1) * P]
+            assert row[16] >> 2 == 0 and not row[17:].any()  # bits past k = 130
+    sc = buf[bits * n * P:].reshape(n, S)
+    assert not sc[:, 2:].any() and sc[:, :2].all()
+    # codes as documented: Q1 = sign bit, Q2 = the two planes' bits
+    signs = _lowbit_plane_bits(buf, bits, n, k, 0, 1)
+    if bits == 1:
+        assert np.array_equal(signs, (w[1] < 0).astype(np.uint8))
+
+
+def test_lowbit_q1_step_is_the_l2_best_power_of_two():
+    g = np.random.default_rng(41)
+    n, k = 40, 128 * 3
+    w = (g.standard_normal((n, k)) * np.exp(g.uniform(-6, 6, (n, 1)))).astype(np.float32)
+    w[0, :128] = g.uniform(0.0, 1.0, 128).astype(np.float32)   # one-signed block
+    w[1, :128] = np.float32(0.75)                              # the tie: mean on 1.5 * 2^-1
+    buf, st = oracle.lowbit_quantize(1, w)
+    assert st == oracle.OK
+    deq = oracle.lowbit_dequantize(1, buf, n, k)
+    for r in range(n):
+        for b in range(3):
+            blk = w[r, 128 * b:128 * (b + 1)].astype(np.float64)
+            x = _lowbit_scale(buf, 1, n, k, r, b) - 127
+            err = lambda e: float(np.sum((np.abs(blk) - 2.0 ** e) ** 2))
+            assert np.array_equal(np.abs(deq[r, 128 * b:128 * (b + 1)]), np.full(128, 2.0 ** x))
+            for d in (-2, -1, 1, 2):
+                assert err(x) <= err(x + d), (r, b, d)
+                if d == -1:
+                    assert err(x) < err(x - 1), (r, b)  # ties go to the lower step
+    assert _lowbit_scale(buf, 1, n, k, 1, 0) == 126
+
+
+def test_lowbit_q2_codes_are_the_nearest_level():
+    g = np.random.default_rng(42)
+    n, k = 30, 256
+    # values on a 2^-12 grid, so the block means need no rounding in any order
+    w = (np.round(g.standard_normal((n, k)) * 4096 * np.exp(g.uniform(-2, 2, (n, 1))))
+         / 4096).astype(np.float32)
+    buf, st = oracle.lowbit_quantize(2, w)
+    assert st == oracle.OK
+    deq = oracle.lowbit_dequantize(2, buf, n, k)
+    levels = np.array([-1.5, -0.5, 0.5, 1.5])
+    for r in range(n):
+        for b in range(2):
+            blk = w[r, 128 * b:128 * (b + 1)].astype(np.float64)
+            t = 2.0 ** (_lowbit_scale(buf, 2, n, k, r, b) - 127)
+            m = np.abs(blk).mean()
+            # the step is the power of two nearest the mean |w| (ties to the lower)
+            assert abs(t - m) <= abs(2 * t - m) and abs(t - m) < abs(t / 2 - m)
+            d = np.abs(blk[:, None] - levels[None, :] * t)
+            best = d.min(axis=1)
+            # nearest level; on a tie the upper of the two
+            choice = np.array([np.flatnonzero(dd == bb).max() for dd, bb in zip(d, best)])
+            assert np.array_equal(deq[r, 128 * b:128 * (b + 1)], levels[choice] * t)
+
+
+@pytest.mark.parametrize("bits", [1, 2])
+def test_lowbit_power_of_two_invariance_and_sign(bits):
+    g = np.random.default_rng(43 + bits)
+    n, k = 7, 300
+    w = g.standard_normal((n, k)).astype(np.float32)
+    buf, _ = oracle.lowbit_quantize(bits, w)
+    P = oracle.lowbit_plane_bytes(k)
+    for s in (-9, 5):
+        buf2, _ = oracle.lowbit_quantize(bits, w * np.float32(2.0 ** s))
+        assert np.array_equal(buf2[:bits * n * P], buf[:bits * n * P])
+        sc, sc2 = buf[bits * n * P:].reshape(n, -1)[:, :3], buf2[bits * n * P:].reshape(n, -1)[:, :3]
+        assert np.array_equal(sc2.astype(int), sc.astype(int) + s)
+    if bits == 1:  # negating the weights flips every sign code, keeps the steps
+        bufn, _ = oracle.lowbit_quantize(1, -w)
+        assert np.array_equal(bufn[:n * P].reshape(n, P)[:, :k // 8],
+                              (~buf[:n * P]).reshape(n, P)[:, :k // 8])
+        assert np.array_equal(bufn[n * P:], buf[n * P:])
+
+
+@pytest.mark.parametrize("bits", [1, 2])
+def test_lowbit_nonfinite_block(bits):
+    w = np.ones((2, 384), np.float32)
+    w[1, 200] = np.nan
+    buf, st = oracle.lowbit_quantize(bits, w)
+    assert st == oracle.ERR_NONFINITE
+    n, k = w.shape
+    assert [_lowbit_scale(buf, bits, n, k, 1, b) for b in range(3)] == [127, 0xFF, 127]
+    for p in range(bits):
+        assert not _lowbit_plane_bits(buf, bits, n, k, p, 1)[128:256].any()
+    assert np.isnan(oracle.lowbit_dequantize(bits, buf, n, k)[1, 128:256]).all()
+
+
+@pytest.mark.parametrize("bits", [1, 2])
+def test_moe_lowbit_layer_is_the_composition(bits):
+    """Router -> top-k -> softmax -> SwiGLU of the selected experts -> the
+    weighted down projections, checked against numpy / scipy on the
+    dequantised matrices."""
+    from scipy.special import expit, softmax
+    g = np.random.default_rng(50 + bits)
+    H, I, E, K = 64, 96, 6, 2
+    x = synth.f32_to_bf16_bits(g.standard_normal(H).astype(np.float32))
+    wr = synth.f32_to_bf16_bits((g.standard_normal((E, H)) * 0.3).astype(np.float32))
+    gus, dns = [], []
+    for e in range(E):
+        gu, _ = oracle.lowbit_quantize(bits, g.standard_normal((2 * I, H)).astype(np.float32) * 0.05)
+        dn, _ = oracle.lowbit_quantize(bits, g.standard_normal((H, I)).astype(np.float32) * 0.05)
+        gus.append(gu)
+        dns.append(dn)
+    out, idx, p, lg, h, st = oracle.moe_lowbit_mlp(bits, x, wr, K, np.stack(gus), np.stack(dns), I)
+    assert st == oracle.OK
+    xv = synth.bf16_bits_to_f32(x).astype(np.float64)
+    logits = synth.bf16_bits_to_f32(wr).astype(np.float64) @ xv
+    assert np.array_equal(lg, logits.astype(np.float32))
+    order = np.lexsort((np.arange(E), -lg.astype(np.float64)))  # descending, lower index first
+    assert np.array_equal(idx, order[:K])
+    assert np.allclose(p, softmax(lg[idx].astype(np.float64)), rtol=1e-14)
+    ref = np.zeros(H)
+    for j, e in enumerate(idx):
+        gu = oracle.lowbit_dequantize(bits, gus[e], 2 * I, H)
+        dn = oracle.lowbit_dequantize(bits, dns[e], H, I)
+        gg, uu = gu[:I] @ xv, gu[I:] @ xv
+        hj = gg * expit(gg) * uu
+        assert np.allclose(h[j], hj, rtol=1e-12, atol=1e-15)
+        ref += p[j] * (dn @ hj)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-14)
