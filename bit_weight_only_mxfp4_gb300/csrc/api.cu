@@ -424,4 +424,58 @@ tt_status tt_gqa_decode_attention(const uint16_t* q_bf16, const uint16_t* k_cach
   return from_cuda(e);
 }
 
+size_t tt_lowbit_matrix_bytes(int32_t bits, int64_t n, int64_t k) {
+  if ((bits != 1 && bits != 2) || n < 1 || k < 1 || n > kMaxRows || k > (int64_t(1) << 30))
+    return 0;
+  return tt::lowbit_matrix_bytes(bits, n, k);
+}
+
+tt_status tt_quantize_lowbit(int32_t bits, const float* w, int64_t n, int64_t k, void* buf,
+                             size_t buf_bytes, int32_t* status_dev, void* stream) {
+  if (bits != 1 && bits != 2) return TT_ERR_SHAPE;
+  if (n < 0 || k < 1 || n > kMaxRows || k > (int64_t(1) << 30)) return TT_ERR_SHAPE;
+  if (n == 0) return TT_OK;
+  if (!w || !buf) return TT_ERR_NULL;
+  if (buf_bytes < tt::lowbit_matrix_bytes(bits, n, k)) return TT_ERR_SIZE;
+  if (!aligned(w, 4) || !aligned(buf, 16) || (status_dev && !aligned(status_dev, 4)))
+    return TT_ERR_ALIGN;
+  return from_cuda(tt::launch_quantize_lowbit(bits, w, n, k, static_cast<uint8_t*>(buf),
+                                              status_dev, as_stream(stream)));
+}
+
+size_t tt_moe_lowbit_workspace_bytes(int64_t inter, int32_t n_experts, int32_t top_k) {
+  if (inter < 32 || inter > 8192 || n_experts < 1 || n_experts > 256 || top_k < 1 ||
+      top_k > 8 || top_k > n_experts)
+    return 0;
+  return size_t(top_k) * size_t(inter) * 4 + (size_t(n_experts) * 4 + 15) / 16 * 16;
+}
+
+tt_status tt_moe_lowbit_topk_mlp(int32_t bits, const uint16_t* x_bf16, int64_t hidden,
+                                 int64_t inter, const uint16_t* router_w_bf16, int32_t n_experts,
+                                 int32_t top_k, const void* const* gate_up,
+                                 const void* const* down, uint16_t* out_bf16, int32_t* out_idx,
+                                 float* out_prob, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if (bits != 1 && bits != 2) return TT_ERR_SHAPE;
+  if (hidden < 32 || hidden % 32 != 0 || hidden > 8192) return TT_ERR_SHAPE;
+  if (inter < 32 || inter % 32 != 0 || inter > 8192) return TT_ERR_SHAPE;
+  if (n_experts < 1 || n_experts > 256 || top_k < 1 || top_k > 8 || top_k > n_experts)
+    return TT_ERR_SHAPE;
+  if (!x_bf16 || !router_w_bf16 || !gate_up || !down || !out_bf16 || !out_idx || !out_prob ||
+      !workspace)
+    return TT_ERR_NULL;
+  if (workspace_bytes < tt_moe_lowbit_workspace_bytes(inter, n_experts, top_k)) return TT_ERR_SIZE;
+  if (!aligned(x_bf16, 16) || !aligned(router_w_bf16, 16) || !aligned(gate_up, 8) ||
+      !aligned(down, 8) || !aligned(out_bf16, 2) || !aligned(out_idx, 4) ||
+      !aligned(out_prob, 4) || !aligned(workspace, 16))
+    return TT_ERR_ALIGN;
+  const cudaError_t e = tt::launch_moe_lowbit(
+      bits, x_bf16, int(hidden), int(inter), router_w_bf16, n_experts, top_k,
+      reinterpret_cast<const uint8_t* const*>(gate_up),
+      reinterpret_cast<const uint8_t* const*>(down), out_bf16, out_idx, out_prob, workspace,
+      as_stream(stream), kPdl);
+  if (e == cudaErrorInvalidConfiguration) return TT_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
 }  // extern "C"

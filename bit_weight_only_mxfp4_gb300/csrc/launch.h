@@ -110,6 +110,18 @@ cudaError_t launch_gqa_decode(const uint16_t* q, const uint16_t* k, const uint16
                               int kv_heads, int head_dim, int64_t cap, int64_t len, float scale,
                               uint16_t* out, void* ws, cudaStream_t s, bool pdl);
 
+// moe_lowbit.cu — Q1 / Q2 low-bit experts: quantiser and the MoE layer
+// (router, selected-expert SwiGLU, weighted down projection; three kernels).
+// The workspace holds h fp32 [top_k][inter], then the E router logits.
+size_t lowbit_matrix_bytes(int bits, int64_t n, int64_t k);
+int lowbit_table_smem_bytes(int64_t k);
+cudaError_t launch_quantize_lowbit(int bits, const float* w, int64_t n, int64_t k, uint8_t* buf,
+                                   int32_t* status, cudaStream_t s);
+cudaError_t launch_moe_lowbit(int bits, const uint16_t* x, int hidden, int inter,
+                              const uint16_t* wr, int E, int top_k, const uint8_t* const* gu,
+                              const uint8_t* const* dn, uint16_t* out, int32_t* out_idx,
+                              float* out_prob, void* ws, cudaStream_t s, bool pdl);
+
 // gemv_bf16.cu
 cudaError_t launch_swiglu_bf16(const uint16_t* wg, const uint16_t* wu, int n, int k,
                                const uint16_t* x, int m, uint16_t* h, cudaStream_t s, bool pdl);

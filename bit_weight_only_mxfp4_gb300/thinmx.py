@@ -55,6 +55,11 @@ SIGNATURES = {
     "tt_fp8_swiglu_matvec": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _P]),
     "tt_quantize_int4_grouped": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
     "tt_int4_grouped_matvec": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _P]),
+    "tt_lowbit_matrix_bytes": (_SZ, [_I32, _I64, _I64]),
+    "tt_quantize_lowbit": (ctypes.c_int, [_I32, _P, _I64, _I64, _P, _SZ, _P, _P]),
+    "tt_moe_lowbit_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
+    "tt_moe_lowbit_topk_mlp": (ctypes.c_int, [_I32, _P, _I64, _I64, _P, _I32, _I32, _P, _P,
+                                               _P, _P, _P, _P, _SZ, _P]),
     "tt_gqa_decode_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
     "tt_gqa_decode_attention": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I64, _I64,
                                                 ctypes.c_float, _P, _P, _SZ, _P]),
@@ -258,3 +263,26 @@ def tt_gqa_decode_attention(q_bf16, k_cache, v_cache, heads, kv_heads, head_dim,
     _check("tt_gqa_decode_attention", load().tt_gqa_decode_attention(
         _ptr(q_bf16), _ptr(k_cache), _ptr(v_cache), heads, kv_heads, head_dim, cap, length,
         float(scale), _ptr(out_bf16), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def tt_lowbit_matrix_bytes(bits, n, k) -> int:
+    return int(load().tt_lowbit_matrix_bytes(bits, n, k))
+
+
+def tt_quantize_lowbit(bits, w, n, k, buf, buf_bytes, status_dev=None, stream=None):
+    _check("tt_quantize_lowbit", load().tt_quantize_lowbit(
+        bits, _ptr(w), n, k, _ptr(buf), buf_bytes, _ptr(status_dev), _stream(stream)))
+
+
+def tt_moe_lowbit_workspace_bytes(inter, n_experts, top_k) -> int:
+    return int(load().tt_moe_lowbit_workspace_bytes(inter, n_experts, top_k))
+
+
+def tt_moe_lowbit_topk_mlp(bits, x_bf16, hidden, inter, router_w_bf16, n_experts, top_k,
+                           gate_up, down, out_bf16, out_idx, out_prob, workspace,
+                           workspace_bytes, stream=None):
+    _check("tt_moe_lowbit_topk_mlp", load().tt_moe_lowbit_topk_mlp(
+        bits, _ptr(x_bf16), hidden, inter, _ptr(router_w_bf16), n_experts, top_k,
+        _ptr(gate_up), _ptr(down), _ptr(out_bf16), _ptr(out_idx), _ptr(out_prob),
+        _ptr(workspace), workspace_bytes, _stream(stream)))
+

@@ -9,7 +9,8 @@
  *   - grouped affine INT4 matvec for the dense Q/K/V/O projections;
  *   - bf16 gate/up SwiGLU matvec for the layers kept in bf16;
  *   - FP8 (E4M3, one scale per row) matvec and gate/up SwiGLU matvec;
- *   - single-token grouped-query attention over a bf16 KV cache.
+ *   - single-token grouped-query attention over a bf16 KV cache;
+ *   - the MoE layer with Q1 / Q2 packed low-bit experts.
  *
  * Sources.  The method is the ThinTensor decode runtime's:
  *   [DL4]  kerbin.cskartikey.dev/@satvikhardat, "Dev Log #4 — 91–96 tok/s
@@ -401,6 +402,61 @@ tt_status tt_gqa_decode_attention(const uint16_t* q_bf16, const uint16_t* k_cach
                                   int32_t head_dim, int64_t cap, int64_t len, float scale,
                                   uint16_t* out_bf16, void* workspace, size_t workspace_bytes,
                                   void* stream);
+
+/* ------------------------------------------------------------------------
+ * Q1 / Q2 packed low-bit experts  [SHIP 97.87 tok/s notes:
+ * packed_expert_q1_layers="0:24", the MoE experts packed as 1-bit "Q1"
+ * structures, 9.52 GB of MXFP4 experts becoming 2.38 GB; final devlog: Q2
+ * and Q1 quantizers, the low-bit selected-expert SwiGLU kernel]
+ *
+ * The pages do not print the encoding.  Reading taken (the one the 4x
+ * footprint fixes for an MX-style format): bits = 1 (Q1) or 2 (Q2) per
+ * weight and one E8M0 step 2^X per block of 128 weights along k (the last
+ * block may be partial).
+ *   X: m = (sum of |w| over the block, in k order, in fp64) / count;
+ *      2^X = the power of two nearest m (ties to the lower), clamped to
+ *      [2^-127, 2^127]; an all-zero block has X = -127.
+ *   Q1: code c = 1 if w < 0 else 0; value (1 - 2c) 2^X.
+ *   Q2: code q = clamp(floor(w / 2^X) + 2, 0, 3); value (q - 1.5) 2^X.
+ *   A block holding NaN/Inf: scale byte 0xFF, zero codes, TT_ERR_NONFINITE
+ *   OR-ed into *status_dev.
+ * Matrix buffer [n][k]: plane 0 [n][P] (and, for Q2, plane 1 [n][P]) then
+ * the scales [n][S]; P = 16 * ceil(k/128), S = ceil(k/128) rounded up to
+ * 16; bit (kk % 8) of byte kk / 8 of a row's plane p is bit p of element
+ * kk's code; padding is zero.  tt_lowbit_matrix_bytes gives the size.
+ * --------------------------------------------------------------------- */
+size_t tt_lowbit_matrix_bytes(int32_t bits, int64_t n, int64_t k);
+
+/* Quantise w fp32 [n][k] (device) into buf (device, >= the matrix bytes,
+   16-byte aligned).  status_dev: device int32, may be NULL.  Setup step. */
+tt_status tt_quantize_lowbit(int32_t bits, const float* w, int64_t n, int64_t k, void* buf,
+                             size_t buf_bytes, int32_t* status_dev, void* stream);
+
+/* The MoE layer with low-bit experts:
+ *   logits = fp32(Wr x) (exact products, compensated sums, rounded once),
+ *   idx = the top_k largest (ties to the lower index, descending), p =
+ *   softmax over them; for each selected expert j
+ *   h_j = silu(G_j x) * (U_j x) (fp32), out = bf16_rne( sum_j p_j D_j h_j ).
+ * gate_up: device array of E pointers, expert e's gate/up matrix buffer
+ * ([2 inter][hidden]: gate rows first, then up rows); down: device array of
+ * E pointers, expert e's down matrix buffer ([hidden][inter]); each buffer
+ * 16-byte aligned, only the selected experts' entries are read (a NULL or
+ * misaligned one is reported through tt_device_error_read and its expert
+ * contributes nothing).  router_w_bf16 [E][hidden].  out_idx int32
+ * [top_k], out_prob fp32 [top_k] (device).  workspace: device, >=
+ * tt_moe_lowbit_workspace_bytes(...) bytes, 16-byte aligned, no initial
+ * contents needed; after the call (in stream order) it holds h, fp32
+ * [top_k][inter], at its start.  Requires bits 1 or 2, hidden and inter
+ * multiples of 32 in [32, 8192], 1 <= top_k <= min(8, E), E <= 256.  Three
+ * kernels (router; selected-expert SwiGLU; weighted down projection).
+ * --------------------------------------------------------------------- */
+size_t tt_moe_lowbit_workspace_bytes(int64_t inter, int32_t n_experts, int32_t top_k);
+tt_status tt_moe_lowbit_topk_mlp(int32_t bits, const uint16_t* x_bf16, int64_t hidden,
+                                 int64_t inter, const uint16_t* router_w_bf16, int32_t n_experts,
+                                 int32_t top_k, const void* const* gate_up,
+                                 const void* const* down, uint16_t* out_bf16, int32_t* out_idx,
+                                 float* out_prob, void* workspace, size_t workspace_bytes,
+                                 void* stream);
 
 #ifdef __cplusplus
 }

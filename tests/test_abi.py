@@ -184,3 +184,36 @@ def test_gqa_validation_before_launch(lib):
     assert call(q=A + 8) == 3
     assert call(out=A + 2) == 3
     assert call(wsp=A + 4) == 3
+
+
+def test_lowbit_validation_before_launch(lib):
+    A = 1 << 20  # never dereferenced: every case fails validation first
+    s = None
+    assert _st("tt_lowbit_matrix_bytes", 1, 5760, 2880) == 5760 * (368 + 32)
+    assert _st("tt_lowbit_matrix_bytes", 2, 2880, 2880) == 2880 * (2 * 368 + 32)
+    assert _st("tt_lowbit_matrix_bytes", 1, 3, 130) == 3 * (32 + 16)
+    assert _st("tt_lowbit_matrix_bytes", 3, 8, 128) == 0
+    q = lambda bits=1, n=8, k=128, w=A, buf=A, nb=1 << 20, st=None: _st(
+        "tt_quantize_lowbit", bits, w, n, k, buf, nb, st, s)
+    assert q(bits=4) == 2
+    assert q(k=0) == 2
+    assert q(n=0, w=None, buf=None) == 0   # empty: a no-op
+    assert q(w=None) == 1
+    assert q(nb=10) == 8
+    assert q(buf=A + 8) == 3
+    assert q(st=A + 2) == 3
+    wsb = _st("tt_moe_lowbit_workspace_bytes", 2880, 32, 4)
+    assert wsb == 4 * 2880 * 4 + 128
+    call = lambda bits=1, H=2880, I=2880, E=32, K=4, x=A, tg=A, td=A, wsp=A, nb=wsb: _st(
+        "tt_moe_lowbit_topk_mlp", bits, x, H, I, A, E, K, tg, td, A, A, A, wsp, nb, s)
+    assert call(bits=3) == 2
+    assert call(H=2890) == 2
+    assert call(I=8224, nb=1 << 30) == 2
+    assert call(K=9) == 2
+    assert call(E=257) == 2
+    assert call(x=None) == 1
+    assert call(tg=None) == 1
+    assert call(nb=wsb - 4) == 8
+    assert call(x=A + 8) == 3
+    assert call(td=A + 4) == 3
+    assert call(wsp=A + 8) == 3
