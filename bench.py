@@ -309,10 +309,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--only", default=None,
-                    choices=["gate_up", "bf16", "moe", "int4", "sweep", "fp8", "mlp", "gqa"],
+                    choices=["gate_up", "bf16", "moe", "int4", "sweep", "fp8", "mlp", "gqa",
+                             "lowbit"],
                     help="run one small workload only (for profiler captures)")
     ap.add_argument("--layers", type=int, default=None,
-                    help="with --only moe: MoE layers to build (default: the full stack)")
+                    help="with --only moe / lowbit: MoE layers to build (default: the full stack)")
     ap.add_argument("--gqa", default=None,
                     help="with --only gqa: one case, model:len (e.g. gptoss20b:32768)")
     ap.add_argument("--ms", default=None,
@@ -358,6 +359,9 @@ def main():
         elif args.only == "int4":
             l2 = torch.cuda.get_device_properties(device).L2_cache_size
             r = int4_workload(torch, synth, thinmx, device, hbm, l2, reps=args.steps)
+        elif args.only == "lowbit":
+            r = moe_lowbit_workload(torch, synth, loader, thinmx, device, hbm, reps=args.steps,
+                                    layers=args.layers)
         elif args.only == "gqa":
             l2 = torch.cuda.get_device_properties(device).L2_cache_size
             r = gqa_workload(torch, synth, thinmx, device, hbm, l2, reps=args.steps,
@@ -594,6 +598,8 @@ def secondary(torch, synth, loader, thinmx, device, hbm, peak_kind):
     out.update(gqa_workload(torch, synth, thinmx, device, hbm, l2))
     torch.cuda.empty_cache()
     out.update(moe_workload(torch, synth, loader, thinmx, device, hbm))
+    torch.cuda.empty_cache()
+    out.update(moe_lowbit_workload(torch, synth, loader, thinmx, device, hbm))
     torch.cuda.empty_cache()
     out["peak"] = {"hbm_gbs": hbm, "source": peak_kind,
                    "tensor_tflops": tensor_peak_tflops()}
@@ -887,6 +893,62 @@ def moe_workload(torch, synth, loader, thinmx, device, hbm, reps=20, layers=None
                      "GBps": round(per / (ms * 1e-3) / 1e9, 1),
                      "frac": round(per / (ms * 1e-3) / 1e9 / hbm, 4), "bytes_per_layer": per,
                      "layers": n_layers, "kernels_per_layer": 1}}
+
+
+def moe_lowbit_workload(torch, synth, loader, thinmx, device, hbm, reps=20, layers=None):
+    """The gpt-oss-20b-shaped MoE stack with Q1 and with Q2 experts (the
+    pages' packed_expert_q1_layers="0:24"): 24 layers, 32 experts each
+    (hidden = inter = 2880), top-4; each layer three PDL-chained kernels.
+    One layer's experts are quantised on the GPU and copied into every
+    layer's own buffers (all resident, far beyond L2)."""
+    c = synth.MOE
+    H, I, E, K = c.hidden, c.inter, c.experts, c.top_k
+    n_layers = layers or c.layers
+    out = {}
+    for bits in (1, 2):
+        gnb = thinmx.tt_lowbit_matrix_bytes(bits, 2 * I, H)
+        dnb = thinmx.tt_lowbit_matrix_bytes(bits, H, I)
+        base_g, base_d = [], []
+        for e in range(E):
+            wgu = synth.torch_normal((2 * I, H), synth.WEIGHT_STD, c.wid, 0, 100 + 2 * e, device)
+            wdn = synth.torch_normal((H, I), synth.WEIGHT_STD, c.wid, 0, 101 + 2 * e, device)
+            g = torch.empty(gnb, dtype=torch.uint8, device=device)
+            d = torch.empty(dnb, dtype=torch.uint8, device=device)
+            thinmx.tt_quantize_lowbit(bits, wgu, 2 * I, H, g, gnb)
+            thinmx.tt_quantize_lowbit(bits, wdn, H, I, d, dnb)
+            base_g.append(g)
+            base_d.append(d)
+            del wgu, wdn
+        stack = []
+        for l in range(n_layers):
+            gb = [b.clone() for b in base_g]
+            db = [b.clone() for b in base_d]
+            wr = synth.torch_normal((E, H), synth.WEIGHT_STD, c.wid, l, 1, device).to(torch.bfloat16)
+            x = synth.torch_normal((H,), 1.0, c.wid, l, 0, device).to(torch.bfloat16)
+            stack.append((loader.expert_table(gb), loader.expert_table(db), wr, x, (gb, db)))
+        del base_g, base_d
+        o = torch.empty(H, dtype=torch.bfloat16, device=device)
+        idx = torch.empty(K, dtype=torch.int32, device=device)
+        prob = torch.empty(K, dtype=torch.float32, device=device)
+        wsb = thinmx.tt_moe_lowbit_workspace_bytes(I, E, K)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+        torch.cuda.synchronize()
+
+        def step():
+            for gt, dt, wr, x, _ in stack:
+                thinmx.tt_moe_lowbit_topk_mlp(bits, x, H, I, wr, E, K, gt, dt, o, idx, prob, ws,
+                                              wsb)
+
+        g = capture(torch, step)
+        ms = time_graph(torch, g, reps) / n_layers
+        per = E * H * 2 + 2 * H + K * (gnb + dnb) + 2 * H
+        del stack, g
+        torch.cuda.empty_cache()
+        out[f"gptoss20b_moe_q{bits}_h2880_e32_top4"] = {
+            "us_per_layer": round(ms * 1e3, 3), "GBps": round(per / (ms * 1e-3) / 1e9, 1),
+            "frac": round(per / (ms * 1e-3) / 1e9 / hbm, 4), "bytes_per_layer": per,
+            "layers": n_layers, "kernels_per_layer": 3}
+    return out
 
 
 def reference_arm(args, world, rank):

@@ -26,15 +26,19 @@
 //
 // Kernels, chained by programmatic dependent launch:
 //   lowbit_router_kernel   logits = Wr x (compensated fp32 sums, rounded
-//                          once), a warp per expert;
-//   lowbit_swiglu_kernel   every CTA takes the top-k + softmax from the
-//                          logits; CTAs take (selected expert, 32 rows)
-//                          tasks, their 8 warps splitting k; h = silu(g) u
+//                          once), a CTA per expert;
+//   lowbit_swiglu_kernel   one CTA per (selected expert, 32 rows); every
+//                          CTA takes the top-k + softmax from the logits,
+//                          requests its rows' chunks (8 warps splitting k),
+//                          builds the table of x meanwhile; h = silu(g) u
 //                          in fp32 to the workspace;
-//   lowbit_down_kernel     out = sum_j p_j down_j h_j: per selected expert a
-//                          table from h_j, 32 output rows per CTA, 8 warps
-//                          splitting k, experts summed in order; bf16 out.
+//   lowbit_down_kernel     out = sum_j p_j down_j h_j: a cluster of top_k
+//                          CTAs per 32 output rows, one per selected expert
+//                          (its own table of h_j), the experts' rows summed
+//                          in order through distributed shared memory.
 #include <cmath>
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "launch.h"
@@ -43,6 +47,8 @@
 
 namespace tt {
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int kLbBlock = 128;
 constexpr int kLbWarps = 8;
@@ -120,23 +126,38 @@ __global__ void quantize_lowbit_kernel(const float* __restrict__ w, int64_t n, i
 }
 
 // ---------------------------------------------------------------------------
-// Router: a warp per expert; products of bf16 are exact in fp32 and are
-// summed with their rounding errors carried (TwoSum), then rounded once.
+// Router: a CTA per expert, its 8 warps splitting k in 8-element chunks (at
+// most 4 per lane); products of bf16 are exact in fp32 and are summed with
+// their rounding errors carried (TwoSum), the warps' sums merged in order,
+// then rounded once.  The expert's weight row is requested before the wait.
 // ---------------------------------------------------------------------------
+constexpr int kRouterChunks = 4;  // 8-element chunks per lane (hidden <= 8192)
+
 __global__ void __launch_bounds__(kLbThreads)
     lowbit_router_kernel(const uint16_t* __restrict__ x, int hidden,
                          const uint16_t* __restrict__ wr, int E, float* __restrict__ logits) {
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * kLbWarps + (threadIdx.x >> 5);
+  __shared__ float ps[kLbWarps], pc[kLbWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x;
+  const int nch = hidden / 8, c0 = nch * warp / kLbWarps, c1 = nch * (warp + 1) / kLbWarps;
+  const uint16_t* row = wr + int64_t(e) * hidden;
+  uint4 a[kRouterChunks], b[kRouterChunks];
+#pragma unroll
+  for (int t = 0; t < kRouterChunks; ++t) {
+    const int ch = c0 + lane + 32 * t;
+    a[t] = ch < c1 ? __ldg(reinterpret_cast<const uint4*>(row) + ch) : make_uint4(0u, 0u, 0u, 0u);
+  }
   pdl_allow_next_grid();
   pdl_wait_prior_grid();  // x comes from the preceding kernel
-  if (e >= E) return;
-  const uint16_t* row = wr + int64_t(e) * hidden;
+#pragma unroll
+  for (int t = 0; t < kRouterChunks; ++t) {
+    const int ch = c0 + lane + 32 * t;
+    b[t] = ch < c1 ? __ldcg(reinterpret_cast<const uint4*>(x) + ch) : make_uint4(0u, 0u, 0u, 0u);
+  }
   float s = 0.f, c = 0.f;
-  for (int k0 = 8 * lane; k0 < hidden; k0 += 256) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(row + k0));
-    const uint4 b = __ldcg(reinterpret_cast<const uint4*>(x + k0));
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int t = 0; t < kRouterChunks; ++t) {
+    const uint32_t aw[4] = {a[t].x, a[t].y, a[t].z, a[t].w}, bw[4] = {b[t].x, b[t].y, b[t].z, b[t].w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       comp_add(s, c, __fmul_rn(bf16_bits_to_f32(aw[q] & 0xFFFFu), bf16_bits_to_f32(bw[q] & 0xFFFFu)));
@@ -148,30 +169,54 @@ __global__ void __launch_bounds__(kLbThreads)
     const float s2 = __shfl_xor_sync(kFullMask, s, o), c2 = __shfl_xor_sync(kFullMask, c, o);
     comp_merge(s, c, s2, c2);
   }
-  if (lane == 0) logits[e] = __fadd_rn(s, c);
+  if (lane == 0) {
+    ps[warp] = s;
+    pc[warp] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float ts = ps[0], tc = pc[0];
+    for (int w2 = 1; w2 < kLbWarps; ++w2) comp_merge(ts, tc, ps[w2], pc[w2]);
+    logits[e] = __fadd_rn(ts, tc);
+  }
 }
 
-// The signed table of a vector v (length len, zero past it): entry
-// [g][nib] = sum_{i<4} (bit i of nib ? -v[4g+i] : v[4g+i]), for g over
-// round_up(len, 128) / 4 groups.
+// Global -> shared copy of n float4 with up to U loads in flight per thread
+// (NT threads).
+template <int U, int NT>
+__device__ __forceinline__ void stage_f4(float4* __restrict__ dst, const float4* __restrict__ src,
+                                         int n, int tid) {
+  for (int base = tid; base < n; base += U * NT) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * NT;
+      if (i < n) v[u] = __ldcg(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * NT;
+      if (i < n) dst[i] = v[u];
+    }
+  }
+}
+
+// The signed table of a vector v (length len, zero past it; len % 4 == 0):
+// entry [g][nib] = ((s_0 v[4g] + s_1 v[4g+1]) + s_2 v[4g+2]) + s_3 v[4g+3],
+// s_i = -1 where bit i of nib is set, for g over round_up(len, 128) / 4
+// groups.  A thread per entry: the 16 threads of a group read its 4 values
+// as one broadcast float4 and store consecutive words (no bank conflicts).
 __device__ __forceinline__ void build_sign_table(float* __restrict__ tab, int len,
                                                  const float* __restrict__ v, int tid,
                                                  int nthreads) {
-  const int groups = (len + kLbBlock - 1) / kLbBlock * (kLbBlock / 4);
-  for (int g = tid; g < groups; g += nthreads) {
-    float a[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = 4 * g + i < len ? v[4 * g + i] : 0.f;
-    float e[16];
-    e[0] = ((a[0] + a[1]) + a[2]) + a[3];
-#pragma unroll
-    for (int nib = 1; nib < 16; ++nib) {
-      const int low = (nib & 1) ? 0 : (nib & 2) ? 1 : (nib & 4) ? 2 : 3;  // lowest set bit
-      e[nib] = e[nib & (nib - 1)] - 2.f * a[low];
-    }
-    float4* dst = reinterpret_cast<float4*>(tab + 16 * g);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) dst[q] = make_float4(e[4 * q], e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]);
+  const int entries = (len + kLbBlock - 1) / kLbBlock * (kLbBlock / 4) * 16;
+  for (int i = tid; i < entries; i += nthreads) {
+    const int g = i >> 4, nib = i & 15;
+    const float4 a = 4 * g < len ? *reinterpret_cast<const float4*>(v + 4 * g)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float t0 = (nib & 1) ? -a.x : a.x, t1 = (nib & 2) ? -a.y : a.y;
+    const float t2 = (nib & 4) ? -a.z : a.z, t3 = (nib & 8) ? -a.w : a.w;
+    tab[i] = ((t0 + t1) + t2) + t3;
   }
 }
 
@@ -190,36 +235,81 @@ __device__ __forceinline__ float chunk_sum(const float* __restrict__ tab, const 
   return acc0 + acc1;
 }
 
-// One row's dot product with a table over blocks [b0, b1) of a matrix
-// buffer (row r of n, k's layout L).
+// A row's plane chunks and block scales for up to kLbMaxBlk consecutive
+// blocks, requested in one go (the loads of a whole task are in flight
+// before any of them is used).
+constexpr int kLbMaxBlk = 4;
+
+// Passes of kLbMaxBlk blocks that cover the largest per-warp block range
+// (ceil(nb / 8) blocks): uniform over the CTA, since the passes hold
+// barriers.
+__device__ __forceinline__ int lb_passes(int nb, int warps) {
+  const int most = (nb + warps - 1) / warps;
+  const int p = (most + kLbMaxBlk - 1) / kLbMaxBlk;
+  return p < 1 ? 1 : p;
+}
+
 template <int BITS>
-__device__ __forceinline__ float row_dot(const uint8_t* __restrict__ buf, int64_t n,
-                                         const LbLayout& L, int64_t r, int b0, int b1,
-                                         const float* __restrict__ tab) {
-  float acc = 0.f;
-  const uint8_t* p0 = buf + r * L.P;
-  const uint8_t* sc = buf + BITS * n * L.P + r * L.S;
-  for (int b = b0; b < b1; ++b) {
-    const float* tb = tab + b * (16 * 32);
-    const float scale = e8m0_to_f32(__ldg(sc + b));
-    const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(p0 + 16 * b));
-    float v;
-    if (BITS == 1) {
-      v = chunk_sum(tb, c0);
+struct RowChunks {
+  uint4 c[BITS][kLbMaxBlk];
+  uint32_t sc[kLbMaxBlk];
+};
+
+template <int BITS>
+__device__ __forceinline__ void row_load(RowChunks<BITS>& rc, const uint8_t* __restrict__ buf,
+                                         int64_t n, const LbLayout& L, int64_t r, int b0,
+                                         int nblk) {
+  const uint8_t* p0 = buf + r * L.P + 16 * b0;
+  const uint8_t* sc = buf + BITS * n * L.P + r * L.S + b0;
+#pragma unroll
+  for (int i = 0; i < kLbMaxBlk; ++i) {
+    if (i < nblk) {
+#pragma unroll
+      for (int p = 0; p < BITS; ++p)
+        rc.c[p][i] = __ldg(reinterpret_cast<const uint4*>(p0 + p * n * L.P + 16 * i));
+      rc.sc[i] = __ldg(sc + i);
     } else {
-      const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(p0 + n * L.P + 16 * b));
-      v = -(0.5f * chunk_sum(tb, c0) + chunk_sum(tb, c1));
+#pragma unroll
+      for (int p = 0; p < BITS; ++p) rc.c[p][i] = make_uint4(0u, 0u, 0u, 0u);
+      rc.sc[i] = 0u;
     }
-    acc = fmaf(v, scale, acc);
+  }
+}
+
+// The row's dot product over those blocks with the table (block b0 first).
+template <int BITS>
+__device__ __forceinline__ float row_compute(const RowChunks<BITS>& rc, int b0, int nblk,
+                                             const float* __restrict__ tab) {
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kLbMaxBlk; ++i) {
+    if (i < nblk) {
+      const float* tb = tab + (b0 + i) * (16 * 32);
+      float v;
+      if (BITS == 1)
+        v = chunk_sum(tb, rc.c[0][i]);
+      else
+        v = -(0.5f * chunk_sum(tb, rc.c[0][i]) + chunk_sum(tb, rc.c[BITS - 1][i]));
+      acc = fmaf(v, e8m0_to_f32(rc.sc[i]), acc);
+    }
   }
   return acc;
 }
 
+__device__ __forceinline__ bool usable(const uint8_t* p) {
+  return p != nullptr && !(reinterpret_cast<uintptr_t>(p) & 15u);
+}
+
 // ---------------------------------------------------------------------------
-// Selected-expert gate/up SwiGLU.
+// Selected-expert gate/up SwiGLU.  Tasks are (selected expert, 32 rows); a
+// CTA takes tasks blockIdx.x, + gridDim.x, ...  After the routing it
+// requests its first task's chunks, then stages x and builds the table while
+// they arrive; each task's chunks are requested one task ahead (the first
+// pass of k, all of it when hidden <= 32 * 128).  The warps' partial sums
+// meet in a double-buffered shared array: one barrier per task.
 // ---------------------------------------------------------------------------
 template <int BITS>
-__global__ void __launch_bounds__(kLbThreads)
+__global__ void __launch_bounds__(kLbThreads, BITS == 1 ? 2 : 1)
     lowbit_swiglu_kernel(const uint16_t* __restrict__ x, int hidden, int inter,
                          const float* __restrict__ logits, int E, int top_k,
                          const uint8_t* const* __restrict__ gu_tab, int32_t* __restrict__ out_idx,
@@ -228,13 +318,21 @@ __global__ void __launch_bounds__(kLbThreads)
   extern __shared__ __align__(16) float tab[];  // [groups][16], then x as fp32
   __shared__ int sidx[kMaxTopK];
   __shared__ float sprob[kMaxTopK];
-  __shared__ const uint8_t* sbuf[kMaxTopK];
-  __shared__ float pg[kLbWarps][32], pu[kLbWarps][32];
+  __shared__ float pg[2][kLbWarps][32], pu[2][kLbWarps][32];
+  __shared__ const uint8_t* etab[kMaxExperts];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const LbLayout L(hidden);
   const int nb = int(L.nb);
   const int64_t rows = 2 * int64_t(inter);
   float* xs = tab + nb * 16 * 32;
+  const int groups = inter / 32, tasks = top_k * groups;
+  const int b0 = nb * warp / kLbWarps, b1 = nb * (warp + 1) / kLbWarps;
+  const int passes = lb_passes(nb, kLbWarps);  // the same for every warp of the CTA
+  auto pass_blocks = [&](int it) {
+    const int p0 = b0 + kLbMaxBlk * it;
+    return b1 - p0 < 0 ? 0 : (b1 - p0 < kLbMaxBlk ? b1 - p0 : kLbMaxBlk);
+  };
+  for (int e = tid; e < E; e += kLbThreads) etab[e] = gu_tab[e];  // weights: before the wait
   pdl_allow_next_grid();
   pdl_wait_prior_grid();  // the logits, and x
   if (warp == 0) {
@@ -243,97 +341,165 @@ __global__ void __launch_bounds__(kLbThreads)
     else
       warp_topk_softmax(logits, E, top_k, lane, sidx, sprob);
   }
-  for (int i = tid; i < hidden; i += kLbThreads) xs[i] = bf16_bits_to_f32(x[i]);
   __syncthreads();
-  if (tid < top_k) {
-    const uint8_t* p = gu_tab[sidx[tid]];
-    sbuf[tid] = p;
-    if (p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u)) flag_error(err, p ? kErrAlign : kErrNull);
-    if (blockIdx.x == 0) {
-      out_idx[tid] = sidx[tid];
-      out_prob[tid] = sprob[tid];
+  if (blockIdx.x == 0 && tid < top_k) {
+    out_idx[tid] = sidx[tid];
+    out_prob[tid] = sprob[tid];
+    const uint8_t* p = etab[sidx[tid]];
+    if (!usable(p)) flag_error(err, p ? kErrAlign : kErrNull);
+  }
+  // a task's expert buffer (null when unusable) and row
+  auto task_buf = [&](int task) {
+    const uint8_t* p = etab[sidx[task / groups]];
+    return usable(p) ? p : nullptr;
+  };
+  auto task_row = [&](int task) { return int64_t(task % groups) * 32 + lane; };
+  RowChunks<BITS> cg, cu, ng, nu;
+  int task = blockIdx.x;
+  const uint8_t* buf = task < tasks ? task_buf(task) : nullptr;
+  if (buf) {
+    row_load<BITS>(cg, buf, rows, L, task_row(task), b0, pass_blocks(0));
+    row_load<BITS>(cu, buf, rows, L, task_row(task) + inter, b0, pass_blocks(0));
+  }
+  // the table of x, built while the first chunks arrive
+  for (int i0 = tid; i0 < hidden / 8; i0 += 4 * kLbThreads) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kLbThreads;
+      if (i < hidden / 8) v[u] = __ldcg(reinterpret_cast<const uint4*>(x) + i);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kLbThreads;
+      if (i < hidden / 8) {
+        const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          xs[8 * i + 2 * q] = bf16_bits_to_f32(wv[q] & 0xFFFFu);
+          xs[8 * i + 2 * q + 1] = bf16_bits_to_f32(wv[q] >> 16);
+        }
+      }
     }
   }
+  __syncthreads();
   build_sign_table(tab, hidden, xs, tid, kLbThreads);
   __syncthreads();
-  // each warp: a contiguous range of the blocks
-  const int b0 = nb * warp / kLbWarps, b1 = nb * (warp + 1) / kLbWarps;
-  const int groups = inter / 32, tasks = top_k * groups;
-  for (int task = blockIdx.x; task < tasks; task += gridDim.x) {
-    const int j = task / groups, r = (task - j * groups) * 32 + lane;
-    const uint8_t* buf = sbuf[j];
+  for (int t = 0; task < tasks; ++t, task += gridDim.x) {
+    const int64_t r = task_row(task);
+    const int next = task + gridDim.x;
+    const uint8_t* nbuf = next < tasks ? task_buf(next) : nullptr;
     float g = 0.f, u = 0.f;
-    if (buf != nullptr && !(reinterpret_cast<uintptr_t>(buf) & 15u)) {
-      g = row_dot<BITS>(buf, rows, L, r, b0, b1, tab);
-      u = row_dot<BITS>(buf, rows, L, r + inter, b0, b1, tab);
+    for (int it = 0; it < passes; ++it) {
+      const int nblk = pass_blocks(it);
+      if (it > 0 && buf) {
+        row_load<BITS>(cg, buf, rows, L, r, b0 + kLbMaxBlk * it, nblk);
+        row_load<BITS>(cu, buf, rows, L, r + inter, b0 + kLbMaxBlk * it, nblk);
+      }
+      if (it == passes - 1 && nbuf) {  // the next task's first chunks
+        row_load<BITS>(ng, nbuf, rows, L, task_row(next), b0, pass_blocks(0));
+        row_load<BITS>(nu, nbuf, rows, L, task_row(next) + inter, b0, pass_blocks(0));
+      }
+      if (buf && nblk > 0) {
+        g += row_compute<BITS>(cg, b0 + kLbMaxBlk * it, nblk, tab);
+        u += row_compute<BITS>(cu, b0 + kLbMaxBlk * it, nblk, tab);
+      }
     }
-    pg[warp][lane] = g;
-    pu[warp][lane] = u;
+    pg[t & 1][warp][lane] = g;
+    pu[t & 1][warp][lane] = u;
     __syncthreads();
     if (warp == 0) {
-      float gs = pg[0][lane], us = pu[0][lane];
+      float gs = pg[t & 1][0][lane], us = pu[t & 1][0][lane];
 #pragma unroll
       for (int w2 = 1; w2 < kLbWarps; ++w2) {
-        gs += pg[w2][lane];
-        us += pu[w2][lane];
+        gs += pg[t & 1][w2][lane];
+        us += pu[t & 1][w2][lane];
       }
-      h[int64_t(j) * inter + r] = silu_mul(gs, us);
+      h[int64_t(task / groups) * inter + r] = silu_mul(gs, us);
     }
-    __syncthreads();
+    cg = ng;
+    cu = nu;
+    buf = nbuf;
   }
 }
 
 // ---------------------------------------------------------------------------
-// Weighted down projection of the selected experts.
+// Weighted down projection of the selected experts: one thread-block
+// cluster of top_k CTAs per 32 output rows; CTA rank j takes selected
+// expert j: the table of h_j, p_j * (D_j h_j) for the 32 rows (8 warps
+// splitting k; the first chunks requested before h_j is staged).  Rank 0
+// sums the ranks' rows in rank order through distributed shared memory.
 // ---------------------------------------------------------------------------
+constexpr int kDnWarps = 8;
+constexpr int kDnThreads = 32 * kDnWarps;
+
 template <int BITS>
-__global__ void __launch_bounds__(kLbThreads)
-    lowbit_down_kernel(int hidden, int inter, int top_k, const int32_t* __restrict__ idx,
-                       const float* __restrict__ prob, const uint8_t* const* __restrict__ dn_tab,
-                       const float* __restrict__ h, uint16_t* __restrict__ out,
-                       int32_t* __restrict__ err) {
-  extern __shared__ __align__(16) float tab[];  // [groups][16], then h_j as fp32
-  __shared__ float po[kLbWarps][32];
+__global__ void __launch_bounds__(kDnThreads)
+    lowbit_down_kernel(int hidden, int inter, int n_experts, int top_k,
+                       const int32_t* __restrict__ idx, const float* __restrict__ prob,
+                       const uint8_t* const* __restrict__ dn_tab, const float* __restrict__ h,
+                       uint16_t* __restrict__ out, int32_t* __restrict__ err) {
+  extern __shared__ __align__(16) float tab[];  // [groups][16], then h_j
+  __shared__ float po[kDnWarps][32];
+  __shared__ float part[32];  // this rank's rows, read by rank 0
+  __shared__ const uint8_t* etab[kMaxExperts];
+  cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int j = int(cluster.block_rank());  // the selected expert (cluster = top_k CTAs)
+  const int64_t c = int64_t(blockIdx.x / top_k) * 32 + lane;  // output row
+  const int64_t cr = c < hidden ? c : hidden - 1;             // rows past the end load a valid row
   const LbLayout L(inter);
   const int nb = int(L.nb);
   float* hs = tab + nb * 16 * 32;
-  const int b0 = nb * warp / kLbWarps, b1 = nb * (warp + 1) / kLbWarps;
-  const int64_t c = int64_t(blockIdx.x) * 32 + lane;  // output row
+  const int b0 = nb * warp / kDnWarps, b1 = nb * (warp + 1) / kDnWarps;
+  const int passes = lb_passes(nb, kDnWarps);  // the same for every warp of the CTA
+  auto pass_blocks = [&](int it) {
+    const int p0 = b0 + kLbMaxBlk * it;
+    return b1 - p0 < 0 ? 0 : (b1 - p0 < kLbMaxBlk ? b1 - p0 : kLbMaxBlk);
+  };
+  for (int e = tid; e < n_experts; e += kDnThreads) etab[e] = dn_tab[e];  // before the wait
   pdl_allow_next_grid();
   pdl_wait_prior_grid();  // h, the selection
+  __syncthreads();
+  const uint8_t* buf = etab[__ldcg(idx + j)];
+  const float pj = __ldcg(prob + j);
+  const bool ok = usable(buf);
+  if (!ok && tid == 0 && blockIdx.x < top_k) flag_error(err, buf ? kErrAlign : kErrNull);
+  RowChunks<BITS> cc;
+  if (ok) row_load<BITS>(cc, buf, hidden, L, cr, b0, pass_blocks(0));
+  stage_f4<8, kDnThreads>(reinterpret_cast<float4*>(hs),
+                          reinterpret_cast<const float4*>(h + int64_t(j) * inter), inter / 4, tid);
+  __syncthreads();
+  build_sign_table(tab, inter, hs, tid, kDnThreads);
+  __syncthreads();
   float acc = 0.f;
-  for (int j = 0; j < top_k; ++j) {
-    const int e = __ldcg(idx + j);
-    const float pj = __ldcg(prob + j);
-    const uint8_t* buf = dn_tab[e];
-    const bool ok = buf != nullptr && !(reinterpret_cast<uintptr_t>(buf) & 15u);
-    if (!ok && tid == 0 && blockIdx.x == 0) flag_error(err, buf ? kErrAlign : kErrNull);
-    __syncthreads();  // the previous expert's table is no longer read
-    for (int i = tid; i < inter; i += kLbThreads) hs[i] = __ldcg(h + int64_t(j) * inter + i);
-    __syncthreads();
-    build_sign_table(tab, inter, hs, tid, kLbThreads);
-    __syncthreads();
-    if (ok && c < hidden) acc = fmaf(pj, row_dot<BITS>(buf, hidden, L, c, b0, b1, tab), acc);
+  for (int it = 0; it < passes; ++it) {
+    const int nblk = pass_blocks(it);
+    if (it > 0 && ok) row_load<BITS>(cc, buf, hidden, L, cr, b0 + kLbMaxBlk * it, nblk);
+    if (ok && nblk > 0) acc += row_compute<BITS>(cc, b0 + kLbMaxBlk * it, nblk, tab);
   }
   po[warp][lane] = acc;
   __syncthreads();
-  if (warp == 0 && c < hidden) {
-    float s = po[0][lane];
+  if (warp == 0) {
+    float s2 = po[0][lane];
 #pragma unroll
-    for (int w2 = 1; w2 < kLbWarps; ++w2) s += po[w2][lane];
-    out[c] = f32_to_bf16_rne(s);
+    for (int w2 = 1; w2 < kDnWarps; ++w2) s2 += po[w2][lane];
+    part[lane] = pj * s2;
   }
+  cluster.sync();  // every rank's rows are in place
+  if (j == 0 && warp == 0) {
+    float t = 0.f;
+    for (int r = 0; r < top_k; ++r) t += cluster.map_shared_rank(part, r)[lane];
+    if (c < hidden) out[c] = f32_to_bf16_rne(t);
+  }
+  cluster.sync();  // rank 0 has read every rank's rows
 }
 
 }  // namespace
 
 size_t lowbit_matrix_bytes(int bits, int64_t n, int64_t k) { return size_t(LbLayout(k).bytes(bits, n)); }
 
-int lowbit_table_smem_bytes(int64_t k) {
-  const LbLayout L(k);
-  return int(L.nb * 16 * 32 * 4 + ((k + 3) / 4) * 16);
-}
+int lowbit_table_smem_bytes(int64_t k) { return int(LbLayout(k).nb * 16 * 32 * 4 + k * 4); }
 
 cudaError_t launch_quantize_lowbit(int bits, const float* w, int64_t n, int64_t k, uint8_t* buf,
                                    int32_t* status, cudaStream_t s) {
@@ -356,8 +522,10 @@ cudaError_t launch_moe_lowbit(int bits, const uint16_t* x, int hidden, int inter
   if (!di) return cudaErrorNoDevice;
   float* h = static_cast<float*>(ws);
   float* logits = h + int64_t(top_k) * inter;
-  const int smem_gu = lowbit_table_smem_bytes(hidden), smem_dn = lowbit_table_smem_bytes(inter);
+  const int smem_gu = lowbit_table_smem_bytes(hidden);
+  const int smem_dn = lowbit_table_smem_bytes(inter);
   if (smem_gu > di->smem_optin || smem_dn > di->smem_optin) return cudaErrorInvalidConfiguration;
+  int occ = 0;  // resident gate/up CTAs per SM
   auto kgu = bits == 1 ? lowbit_swiglu_kernel<1> : lowbit_swiglu_kernel<2>;
   auto kdn = bits == 1 ? lowbit_down_kernel<1> : lowbit_down_kernel<2>;
   if (cudaError_t e = ensure_smem(*di, kgu, smem_gu)) return e;
@@ -369,24 +537,38 @@ cudaError_t launch_moe_lowbit(int bits, const uint16_t* x, int hidden, int inter
   cfg.attrs = attr;
   cfg.stream = s;
   cfg.blockDim = dim3(kLbThreads);
-  // router
-  cfg.gridDim = dim3(unsigned((E + kLbWarps - 1) / kLbWarps));
+  // router: a CTA per expert
+  cfg.gridDim = dim3(unsigned(E));
   cfg.dynamicSmemBytes = 0;
   cfg.numAttrs = pdl ? 1 : 0;
   if (cudaError_t e = cudaLaunchKernelEx(&cfg, lowbit_router_kernel, x, hidden, wr, E, logits))
     return e;
   // gate/up SwiGLU of the selected experts, then the weighted down projection
   cfg.numAttrs = 1;
-  const int tasks = top_k * (inter / 32);
-  cfg.gridDim = dim3(unsigned(tasks < di->sms ? tasks : di->sms));
+  if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kgu, kLbThreads, smem_gu))
+    return e;
+  const int tasks = top_k * (inter / 32);  // (selected expert, 32 rows)
+  const int resident = (occ < 1 ? 1 : occ) * di->sms;
+  cfg.gridDim = dim3(unsigned(tasks < resident ? tasks : resident));
   cfg.dynamicSmemBytes = smem_gu;
   if (cudaError_t e = cudaLaunchKernelEx(&cfg, kgu, x, hidden, inter,
                                          static_cast<const float*>(logits), E, top_k, gu, out_idx,
                                          out_prob, h, di->error_word))
     return e;
-  cfg.gridDim = dim3(unsigned((hidden + 31) / 32));
+  // one cluster of top_k CTAs (one per selected expert) per 32 output rows
+  cudaLaunchAttribute dattr[2];
+  dattr[0] = attr[0];
+  dattr[1].id = cudaLaunchAttributeClusterDimension;
+  dattr[1].val.clusterDim.x = unsigned(top_k);
+  dattr[1].val.clusterDim.y = 1;
+  dattr[1].val.clusterDim.z = 1;
+  cfg.attrs = dattr;
+  cfg.numAttrs = 2;
+  cfg.gridDim = dim3(unsigned((hidden + 31) / 32 * top_k));
+  cfg.blockDim = dim3(kDnThreads);
   cfg.dynamicSmemBytes = smem_dn;
-  return cudaLaunchKernelEx(&cfg, kdn, hidden, inter, top_k, static_cast<const int32_t*>(out_idx),
+  return cudaLaunchKernelEx(&cfg, kdn, hidden, inter, E, top_k,
+                            static_cast<const int32_t*>(out_idx),
                             static_cast<const float*>(out_prob), dn, static_cast<const float*>(h),
                             out, di->error_word);
 }
