@@ -204,19 +204,24 @@ __device__ __forceinline__ void stage_f4(float4* __restrict__ dst, const float4*
 // The signed table of a vector v (length len, zero past it; len % 4 == 0):
 // entry [g][nib] = ((s_0 v[4g] + s_1 v[4g+1]) + s_2 v[4g+2]) + s_3 v[4g+3],
 // s_i = -1 where bit i of nib is set, for g over round_up(len, 128) / 4
-// groups.  A thread per entry: the 16 threads of a group read its 4 values
-// as one broadcast float4 and store consecutive words (no bank conflicts).
+// groups.  A thread per (group, top two sign bits): its 4 entries share
+// s_2 and s_3; the 4 threads of a group read its values as one broadcast
+// float4 and store consecutive 16-byte pieces (no bank conflicts).
 __device__ __forceinline__ void build_sign_table(float* __restrict__ tab, int len,
                                                  const float* __restrict__ v, int tid,
                                                  int nthreads) {
-  const int entries = (len + kLbBlock - 1) / kLbBlock * (kLbBlock / 4) * 16;
-  for (int i = tid; i < entries; i += nthreads) {
-    const int g = i >> 4, nib = i & 15;
+  const int quads = (len + kLbBlock - 1) / kLbBlock * (kLbBlock / 4) * 4;
+  for (int i = tid; i < quads; i += nthreads) {
+    const int g = i >> 2, q = i & 3;
     const float4 a = 4 * g < len ? *reinterpret_cast<const float4*>(v + 4 * g)
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float t0 = (nib & 1) ? -a.x : a.x, t1 = (nib & 2) ? -a.y : a.y;
-    const float t2 = (nib & 4) ? -a.z : a.z, t3 = (nib & 8) ? -a.w : a.w;
-    tab[i] = ((t0 + t1) + t2) + t3;
+    const float sz = (q & 1) ? -a.z : a.z, sw = (q & 2) ? -a.w : a.w;
+    float4 e;
+    e.x = ((a.x + a.y) + sz) + sw;
+    e.y = ((-a.x + a.y) + sz) + sw;
+    e.z = ((a.x - a.y) + sz) + sw;
+    e.w = ((-a.x - a.y) + sz) + sw;
+    reinterpret_cast<float4*>(tab)[i] = e;
   }
 }
 
