@@ -19,6 +19,7 @@
 // the dependency wait on the previous kernel.
 #include "common.cuh"
 #include "launch.h"
+#include "mxfp4_core.cuh"
 
 namespace tt {
 namespace {
@@ -31,6 +32,11 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint3
   // d = (a & mask) | bits
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));
   return d;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<const uint16_t*>(&b);
 }
 
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
@@ -202,6 +208,154 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// m = 1, group 128: the multiply-adds of a row pair on mma.sync m16n8k16
+// (f16 x f16 -> fp32), in the diagonal form of the FP8 kernel.  A step
+// covers 8 groups (1024 k): A row g holds 16 k of group 8t+g of the pair's
+// first row and A row 8+g the same k of its second row, B column c holds x
+// of group 8t+c, so over the step's 8 MMAs D[g][g] and D[8+g][g] are the two
+// rows' dot products over exactly one group; the group's fp16 scale (and
+// x's per-group inverse prescale) is applied to them once.  Lane (g, q)
+// owns the 32 weights 32q.. of its group: one 16-byte code load per row,
+// decoded as above into the exact (q - zp) f16x2 pairs that are the A
+// fragments.  x is prescaled per 128-group (R16) and staged once per CTA in
+// shared memory already in B-fragment order.  A warp owns one or two row
+// pairs, all requested before the dependency wait, so the whole matrix is
+// in flight by then, with about one CTA per SM left free for the next
+// kernel's CTAs to do the same.
+// ---------------------------------------------------------------------------
+constexpr int kMmaCtaWarps = 8;
+
+template <int ST, int PPW>  // steps of 1024 k (k <= 1024 * ST); row pairs per warp
+__global__ void __launch_bounds__(kMmaCtaWarps * 32, 2)
+    int4_mma_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                    const uint8_t* __restrict__ zp, int n, int k,
+                    const uint16_t* __restrict__ x, uint16_t* __restrict__ y) {
+  __shared__ uint4 xs[ST][4][32];  // step, 16-byte word, lane: B fragments
+  __shared__ float xis[ST][8];     // inverse prescale of group 8t+g
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  const int ng = (k + 127) >> 7;  // groups per row (the last may be partial)
+  const int zb = (ng + 1) >> 1;
+  const int npairs = (n + 1) >> 1;
+  const int gw = blockIdx.x * kMmaCtaWarps + warp, nw = gridDim.x * kMmaCtaWarps;
+
+  uint4 c[PPW][2][ST];      // codes of the lane's piece, rows 2p and 2p + 1
+  uint32_t zz[PPW][2][ST];  // f16x2 (1024 + zp) of the piece's group
+  float sc[PPW][2][ST];     // the group's scale (0 past the end)
+  auto load_pair = [&](int u, int p) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int row = 2 * p + r;
+#pragma unroll
+      for (int t = 0; t < ST; ++t) {
+        const int grp = 8 * t + g;
+        const bool ok = row < n && p < npairs && grp < ng;
+        const int kk = 128 * grp + 32 * q;
+        c[u][r][t] = ok && kk < k
+                      ? __ldcs(reinterpret_cast<const uint4*>(codes + (size_t)row * (k >> 1) +
+                                                              (kk >> 1)))
+                      : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t z = ok ? (__ldg(zp + (size_t)row * zb + (grp >> 1)) >> (4 * (grp & 1))) & 15u : 0u;
+        zz[u][r][t] = 0x64006400u + z * 0x00010001u;
+        sc[u][r][t] = ok ? __half2float(__ushort_as_half(__ldg(scales + (size_t)row * ng + grp))) : 0.f;
+      }
+    }
+  };
+  // the warp's pairs gw + i * nw, all requested before the wait
+#pragma unroll
+  for (int u = 0; u < PPW; ++u) load_pair(u, gw + u * nw);
+  pdl_allow_next_grid();
+  pdl_wait_prior_grid();  // x comes from the preceding kernel
+
+  // warp t stages step t of x: its lanes' pieces as f16 in the pair order
+  // (x[8w+i], x[8w+i+4]), each 128-group prescaled by its exact power of two
+  if (warp < ST) {
+    const int t = warp;
+    const int kk = 128 * (8 * t + g) + 32 * q;
+    uint4 v[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      v[w] = kk < k ? __ldcg(reinterpret_cast<const uint4*>(x + kk) + w) : make_uint4(0u, 0u, 0u, 0u);
+    float e[32];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t u[4] = {v[w].x, v[w].y, v[w].z, v[w].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        e[8 * w + 2 * h] = bf16_bits_to_f32(u[h] & 0xFFFFu);
+        e[8 * w + 2 * h + 1] = bf16_bits_to_f32(u[h] >> 16);
+      }
+    }
+    float mx = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(e[i]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));  // the group's 4 pieces
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const int sb = min(f16_prescale_exponent(mx), 127);
+    const float two_s = scalbnf(1.0f, sb);
+    if (q == 0) xis[t][g] = scalbnf(1.0f, -sb);  // exact
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      xs[t][w][lane] = make_uint4(pack_f16x2_scaled(e[8 * w + 0], e[8 * w + 4], two_s),
+                                  pack_f16x2_scaled(e[8 * w + 1], e[8 * w + 5], two_s),
+                                  pack_f16x2_scaled(e[8 * w + 2], e[8 * w + 6], two_s),
+                                  pack_f16x2_scaled(e[8 * w + 3], e[8 * w + 7], two_s));
+  }
+  __syncthreads();
+
+  const bool diag = q == (g >> 1);  // this lane holds D[g][g] and D[8+g][g]
+#pragma unroll
+  for (int u = 0; u < PPW; ++u) {
+    const int p = gw + u * nw;
+    if (p >= npairs) break;
+    float acc[2] = {0.f, 0.f};
+#pragma unroll
+    for (int t = 0; t < ST; ++t) {
+      uint32_t xb[16];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint4 xv = xs[t][w][lane];
+        xb[4 * w] = xv.x;
+        xb[4 * w + 1] = xv.y;
+        xb[4 * w + 2] = xv.z;
+        xb[4 * w + 3] = xv.w;
+      }
+      uint32_t pa[16], pb[16];
+      const uint32_t wa[4] = {c[u][0][t].x, c[u][0][t].y, c[u][0][t].z, c[u][0][t].w};
+      const uint32_t wb[4] = {c[u][1][t].x, c[u][1][t].y, c[u][1][t].z, c[u][1][t].w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          pa[4 * w + i] = hsub2(lop3_and_or(wa[w] >> (4 * i), 0x000F000Fu, 0x64006400u), zz[u][0][t]);
+          pb[4 * w + i] = hsub2(lop3_and_or(wb[w] >> (4 * i), 0x000F000Fu, 0x64006400u), zz[u][1][t]);
+        }
+      float d0[4], d1[4];  // two accumulation chains
+      mma_16816_z(d0, pa[0], pb[0], pa[1], pb[1], xb[0], xb[1]);
+      mma_16816_z(d1, pa[2], pb[2], pa[3], pb[3], xb[2], xb[3]);
+#pragma unroll
+      for (int m = 2; m < 8; m += 2) {
+        mma_16816(d0, pa[2 * m], pb[2 * m], pa[2 * m + 1], pb[2 * m + 1], xb[2 * m], xb[2 * m + 1]);
+        mma_16816(d1, pa[2 * m + 2], pb[2 * m + 2], pa[2 * m + 3], pb[2 * m + 3], xb[2 * m + 2],
+                  xb[2 * m + 3]);
+      }
+      if (diag) {
+        const int e0 = g & 1;
+        const float xi = xis[t][g];
+        acc[0] = fmaf(d0[e0] + d1[e0], sc[u][0][t] * xi, acc[0]);
+        acc[1] = fmaf(d0[2 + e0] + d1[2 + e0], sc[u][1][t] * xi, acc[1]);
+      }
+    }
+    const float ya = warp_sum(acc[0]), yb = warp_sum(acc[1]);  // other lanes hold 0
+    if (lane == 0) {
+      y[2 * p] = f32_to_bf16_bits(ya);
+      if (2 * p + 1 < n) y[2 * p + 1] = f32_to_bf16_bits(yb);
+    }
+  }
+}
+
 template <int CPL, int MT, int RPW>
 cudaError_t run(const DeviceInfo& di, const uint8_t* codes, const uint16_t* scales,
                 const uint8_t* zp, int n, int k, int group, const uint16_t* x, int m,
@@ -225,6 +379,38 @@ cudaError_t run(const DeviceInfo& di, const uint8_t* codes, const uint16_t* scal
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, codes, scales, zp, n, k, group, x, m, y);
+}
+
+
+template <int ST, int PPW>
+cudaError_t run_mma(const DeviceInfo& di, const uint8_t* codes, const uint16_t* scales,
+                    const uint8_t* zp, int n, int k, const uint16_t* x, uint16_t* y,
+                    cudaStream_t s, bool pdl) {
+  const int npairs = (n + 1) / 2;
+  const int grid = (npairs + kMmaCtaWarps * PPW - 1) / (kMmaCtaWarps * PPW);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMmaCtaWarps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, int4_mma_kernel<ST, PPW>, codes, scales, zp, n, k, x, y);
+}
+
+// Pairs per warp: one pass over the rows with about one CTA per SM (two
+// when the rows need more), so the next kernel's CTAs can be resident
+// early and request their weights before their own wait.
+template <int ST>
+cudaError_t run_mma_ppw(const DeviceInfo& di, const uint8_t* codes, const uint16_t* scales,
+                        const uint8_t* zp, int n, int k, const uint16_t* x, uint16_t* y,
+                        cudaStream_t s, bool pdl) {
+  const int npairs = (n + 1) / 2;
+  if (npairs <= kMmaCtaWarps * di.sms)
+    return run_mma<ST, 1>(di, codes, scales, zp, n, k, x, y, s, pdl);
+  return run_mma<ST, 2>(di, codes, scales, zp, n, k, x, y, s, pdl);
 }
 
 template <int CPL>
@@ -251,6 +437,14 @@ cudaError_t launch_int4_matvec(const uint8_t* codes, const uint16_t* scales, con
                                cudaStream_t s, bool pdl) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorNoDevice;
+  if (m == 1 && group == 128 && k <= 4096) {
+    switch ((k + 1023) / 1024) {
+      case 1: return run_mma_ppw<1>(*di, codes, scales, zp, n, k, x, y, s, pdl);
+      case 2: return run_mma_ppw<2>(*di, codes, scales, zp, n, k, x, y, s, pdl);
+      case 3: return run_mma_ppw<3>(*di, codes, scales, zp, n, k, x, y, s, pdl);
+      default: return run_mma_ppw<4>(*di, codes, scales, zp, n, k, x, y, s, pdl);
+    }
+  }
   switch ((k / 32 + 31) / 32) {
     case 1: return run_m<1>(*di, codes, scales, zp, n, k, group, x, m, y, s, pdl);
     case 2: return run_m<2>(*di, codes, scales, zp, n, k, group, x, m, y, s, pdl);

@@ -98,6 +98,10 @@ def test_int4_quantize_full_qkv():
     (50, 2880, 96, 4), (300, 4096, 256, 1), (5, 32, 32, 1),
     # more rows than one pass of the grid covers (three rows per warp at m = 1)
     (9001, 256, 64, 1), (9001, 256, 64, 3),
+    # m = 1, group 128: the tensor-core row-pair kernel (k in 1..4 steps of 1024,
+    # partial last group, odd row counts, several pairs per warp)
+    (1, 128, 128, 1), (2, 1024, 128, 1), (33, 1056, 128, 1), (40, 2048, 128, 1),
+    (31, 3008, 128, 1), (64, 4096, 128, 1), (9001, 2880, 128, 1), (12, 4128, 128, 1),
 ])
 def test_int4_matvec_shapes(n, k, group, m):
     d = synth.int4_inputs(97, 0, n, k, m)
@@ -142,3 +146,26 @@ def test_int4_matvec_chunks_of_very_different_magnitude():
     ref = oracle.int4_matvec(gu.host(codes), gu.host(scales, np.uint16), gu.host(zp), group, x)
     assert_float_parity(y, ref, "int4 chunk magnitudes 2^-60..2^60")
     assert gu.device_error() == 0
+
+
+def test_int4_matvec_groups_of_very_different_magnitude():
+    """The m = 1, group-128 tensor-core kernel prescales x per 128-group:
+    groups spread over 2^-60 .. 2^60 (and an all-zero group), weights scaled
+    the other way as far as fp16 group scales allow."""
+    n, k, group = 64, 2880, 128
+    d = synth.int4_inputs(99, 0, n, k, 1)
+    g = synth.rng(99, 1)
+    ng = (k + group - 1) // group
+    e = g.integers(-60, 61, ng)
+    fx = np.repeat(np.ldexp(1.0, e), group)[:k]
+    fw = np.repeat(np.ldexp(1.0, -np.clip(e, -6, 10)), group)[:k]
+    xf = (synth.bf16_bits_to_f32(d["x"]).astype(np.float64) * fx).astype(np.float32)
+    xf[:, 256:384] = 0.0
+    x = synth.f32_to_bf16_bits(xf)
+    w = (d["w"].astype(np.float64) * fw).astype(np.float32)
+    codes, scales, zp = _check_quantize(w, group)
+    y = gpu_int4_matvec(codes, scales, zp, n, k, group, x)
+    ref = oracle.int4_matvec(gu.host(codes), gu.host(scales, np.uint16), gu.host(zp), group, x)
+    assert_float_parity(y, ref, "int4 group magnitudes 2^-60..2^60")
+    assert gu.device_error() == 0
+
