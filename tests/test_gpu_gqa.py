@@ -69,6 +69,8 @@ def _check(q, k, v, length, scale, what, ws=None):
     (40, 10, 128, 300, 300),    # Phi-4 heads
     (28, 4, 128, 500, 333),     # 7-wide groups
     (4, 4, 128, 64, 64),
+    (64, 64, 128, 400, 399),    # the most kv heads (64), one query head each
+    (1024, 64, 64, 130, 130),   # 64 kv heads with 16-wide groups
 ])
 def test_gqa_shapes(heads, kvh, d, cap, length):
     c = synth.gqa_inputs(WID, heads * 1000 + length, heads, kvh, d, cap)

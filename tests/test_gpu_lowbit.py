@@ -124,7 +124,10 @@ def _check_layer(bits, hidden, inter, E, top_k, wid):
 @pytest.mark.parametrize("bits", [1, 2])
 @pytest.mark.parametrize("hidden,inter,E,top_k", [(64, 32, 4, 1), (256, 96, 8, 2),
                                                   (2880, 2880, 32, 4), (1024, 4096, 64, 8),
-                                                  (4096, 512, 40, 3)])
+                                                  (4096, 512, 40, 3),
+                                                  # the largest hidden and inter (8192)
+                                                  (8192, 1024, 4, 2), (1024, 8192, 4, 2),
+                                                  (96, 64, 256, 8)])
 def test_moe_lowbit_layer(bits, hidden, inter, E, top_k):
     _check_layer(bits, hidden, inter, E, top_k, WID + hidden + E)
 
