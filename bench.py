@@ -281,6 +281,28 @@ DRAM_TRAFFIC = {
 }
 # The kernel that serves the batch-1 MXFP4 gate/up layer at K = 2048.
 MXFP4_M1_KERNEL = "swiglu_mxfp4_m1x_kernel"
+
+# The other workloads' kernels: (kernel(s), bound, DRAM read + write of one
+# launch (summed over a call's kernels) from an ncu capture of the current
+# code on the same shape, or None where no such capture exists).
+WORKLOAD_KERNELS = {
+    "fp8_gate_up_k2048_n11008_m1": ("fp8_pair_kernel", "hbm", 45209088),
+    "bf16_down_k11008_n2048_m1": ("bf16_rows_kernel", "hbm", 45124096),
+    "fp8_down_k11008_n2048_m1": ("fp8_pair_kernel", "hbm", None),
+    "mxfp4_down_k11008_n2048_m1": ("mxfp4_rows_kernel", "hbm", None),
+    "gptoss20b_int4_qkv_k2880_n5120_g128": ("int4_mma_kernel", "hbm", None),
+    "gptoss20b_moe_h2880_e32_top4": ("moe_fused_kernel", "hbm", None),
+    "gptoss20b_moe_q1_h2880_e32_top4": ("lowbit_router_kernel + lowbit_swiglu_kernel + "
+                                        "lowbit_down_kernel", "hbm", 14180864),
+    "gptoss20b_moe_q2_h2880_e32_top4": ("lowbit_router_kernel + lowbit_swiglu_kernel + "
+                                        "lowbit_down_kernel", "hbm", None),
+    # time per call (split + merge kernels); traffic of the split kernel (the
+    # merge kernel's reads of the split partials hit L2)
+    "gqa_decode_smollm3_3b_h16_kv4_d128_len32768": ("gqa_decode_kernel + gqa_merge_kernel",
+                                                    "hbm", 67459072),
+    "gqa_decode_gptoss20b_h64_kv8_d64_len32768": ("gqa_decode_kernel + gqa_merge_kernel",
+                                                  "hbm", 67426560),
+}
 NOMINAL_HBM_GBS = 8000.0
 
 
@@ -483,6 +505,15 @@ def main():
          "bytes_per_launch": bf_b, "us_per_launch": round(ms_bf * 1e3, 3),
          "traffic": DRAM_TRAFFIC.get("swiglu_bf16_kernel")},
     ]
+    for name, (kern, bound, traffic) in WORKLOAD_KERNELS.items():
+        o = others.get(name)
+        if not isinstance(o, dict) or "GBps" not in o:
+            continue
+        kernels.append({"kernel": kern, "workload": name, "bound": bound, "achieved": o["GBps"],
+                        "peak": hbm, "unit": "GB/s", "frac": round(o["GBps"] / hbm, 4),
+                        "bytes_per_launch": o.get("bytes", o.get("bytes_per_layer")),
+                        "us_per_launch": o.get("us", o.get("us_per_layer")),
+                        "traffic": traffic})
     roofline = {k: kernels[0][k] for k in ("bound", "achieved", "peak", "unit", "frac",
                                            "traffic")}
     roofline["kernel"] = mx_kernel
