@@ -66,15 +66,23 @@ constexpr int kThreads = kWarps * 32;
 // touches 32 consecutive 16-byte words.
 // Keeping x out of registers lets WARPS warps per CTA stay resident while
 // the next kernel's CTA (programmatic dependent launch) shares the SM.
-// NB = number of 1024-wide K chunks; RPC = records per bulk copy.
+// NB = number of 1024-wide K chunks; RPC = records per bulk copy; KC = K
+// when it is fixed at compile time (0: K is the runtime argument), which
+// turns every record and x offset into an immediate; FULL = K is exactly
+// 1024 * NB, so every lane owns a block in every chunk and the per-block
+// bounds tests drop out (measured: 6.46 against 6.77 us on the SmolLM3
+// gate/up layer, the difference being integer and branch instructions).
 // ---------------------------------------------------------------------------
-template <int NB, int RPC, int WARPS>
+template <int NB, int RPC, int WARPS, int KC, bool FULL>
 __global__ void __launch_bounds__(WARPS * 32, 2)
-    swiglu_mxfp4_m1x_kernel(const uint8_t* __restrict__ packed, int n, int k,
+    swiglu_mxfp4_m1x_kernel(const uint8_t* __restrict__ packed, int n, int k_arg,
                             const uint16_t* __restrict__ x, uint16_t* __restrict__ h, int slots,
                             int32_t* err) {
+  static_assert(KC == 0 || (KC % 32 == 0 && (KC + 1023) / 1024 == NB), "KC and NB disagree");
+  static_assert(!FULL || KC == 0 || KC == 1024 * NB, "FULL needs K == 1024 * NB");
   constexpr int THREADS = WARPS * 32;
   extern __shared__ __align__(128) uint8_t smem[];
+  const int k = KC > 0 ? KC : k_arg;
   const SwigluRecord L(k);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r0 = int((int64_t)n * blockIdx.x / gridDim.x);
@@ -146,7 +154,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   if (TT_M1_LATE_TRIGGER) pdl_allow_next_grid();
   float xi[NB];  // this lane's blocks' 2^-s
 #pragma unroll
-  for (int i = 0; i < NB; ++i) xi[i] = 32 * i + lane < L.nblk ? xinv[32 * i + lane] : 0.f;
+  for (int i = 0; i < NB; ++i) xi[i] = (FULL || 32 * i + lane < L.nblk) ? xinv[32 * i + lane] : 0.f;
   EpilogueBatch ep;
 
   for (int j = 0; j < nitems; ++j) {
@@ -164,7 +172,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
 #pragma unroll
     for (int i = 0; i < NB; ++i) {
       const int b = 32 * i + lane;
-      if (b < L.nblk) {
+      if (FULL || b < L.nblk) {
         uint32_t xv[16];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -176,7 +184,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
         }
 #pragma unroll
         for (int rr = 0; rr < RPC; ++rr) {
-          if (rr < count) {
+          if (RPC == 1 || rr < count) {  // a one-record item always holds its record
             const uint8_t* rec = slot + rr * L.bytes;
             const uint4 cg = *reinterpret_cast<const uint4*>(rec + L.gate_codes() + b * 16);
             const uint4 cu = *reinterpret_cast<const uint4*>(rec + L.up_codes() + b * 16);
@@ -385,7 +393,7 @@ cudaError_t launch_threads(Kern kern, int grid, int threads, int smem, cudaStrea
 #endif
 constexpr int kHalfSmBudget = TT_M1_SMEM_BUDGET;
 
-template <int NB, int RPC, int WARPS>
+template <int NB, int RPC, int WARPS, int KC = 0, bool FULL = false>
 cudaError_t run_m1x(const DeviceInfo& di, const uint8_t* packed, int n, int k, const uint16_t* x,
                     uint16_t* h, cudaStream_t s, bool pdl) {
   const SwigluRecord L(k);
@@ -396,7 +404,7 @@ cudaError_t run_m1x(const DeviceInfo& di, const uint8_t* packed, int n, int k, c
   if (slots < 1) slots = 1;
   const int smem = WARPS * slots * (slot_bytes + 8) + fixed;
   if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
-  auto kern = swiglu_mxfp4_m1x_kernel<NB, RPC, WARPS>;
+  auto kern = swiglu_mxfp4_m1x_kernel<NB, RPC, WARPS, KC, FULL>;
   cudaError_t e = ensure_smem(di, kern, smem);
   if (e != cudaSuccess) return e;
   int grid = di.sms;  // one CTA per SM
@@ -437,6 +445,20 @@ cudaError_t launch_swiglu_mxfp4_cc(const uint8_t* packed, int n, int k, const ui
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorNoDevice;
   if (m == 1) {
+    // K of the gate/up layers of the models the library serves (SmolLM3-3B:
+    // 2048, Phi-4: 5120) get kernels with K fixed; every other K takes the
+    // runtime-K kernel, without per-block bounds tests when K % 1024 == 0.
+    if (k == 2048) return run_m1x<2, TT_M1_RPC, TT_M1_WARPS, 2048, true>(*di, packed, n, k, x, h, s, pdl);
+    if (k == 5120) return run_m1x<5, 1, TT_M1_WARPS, 5120, true>(*di, packed, n, k, x, h, s, pdl);
+    if (k % 1024 == 0) {
+      switch (k / 1024) {
+        case 1: return run_m1x<1, TT_M1_RPC, TT_M1_WARPS, 0, true>(*di, packed, n, k, x, h, s, pdl);
+        case 3: return run_m1x<3, TT_M1_RPC, TT_M1_WARPS, 0, true>(*di, packed, n, k, x, h, s, pdl);
+        case 4: return run_m1x<4, 1, TT_M1_WARPS, 0, true>(*di, packed, n, k, x, h, s, pdl);
+        case 8: return run_m1x<8, 1, TT_M1_WARPS, 0, true>(*di, packed, n, k, x, h, s, pdl);
+        default: break;  // 6 and 7 chunks: the runtime kernel below
+      }
+    }
     switch ((k / 32 + 31) / 32) {
       case 1: return run_m1x<1, TT_M1_RPC, TT_M1_WARPS>(*di, packed, n, k, x, h, s, pdl);
       case 2: return run_m1x<2, TT_M1_RPC, TT_M1_WARPS>(*di, packed, n, k, x, h, s, pdl);

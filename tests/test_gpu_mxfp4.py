@@ -121,6 +121,11 @@ def _swiglu_case(n, k, m, postscale=True, wid=92, layer=0):
 @pytest.mark.parametrize("n,k,m,post", [
     (37, 96, 1, True), (64, 32, 1, False), (129, 1024, 1, True), (300, 2880, 1, True),
     (50, 5120, 1, False), (33, 8192, 1, True), (21, 16384, 1, True),
+    # m = 1 kernels with K fixed at compile time (2048, 5120), with K a
+    # multiple of 1024 (no bounds tests: 3072, 4096) and the runtime-K kernel
+    # at 6 chunks; rows spread over every CTA with ragged per-CTA counts
+    (3001, 2048, 1, True), (517, 5120, 1, True), (200, 3072, 1, True), (150, 4096, 1, False),
+    (61, 6144, 1, True),
     (77, 2048, 2, True), (77, 2048, 3, False),
     # m <= 8, k <= 5120: the mma.sync streaming kernel; 8-row tiles with
     # ragged ends, n below one tile, fewer 32-blocks than consumer warps
