@@ -149,14 +149,14 @@ __device__ __forceinline__ void red_release_add(uint64_t* p, uint64_t v) {
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// Spins (bounded in time) until *p >= target.  One thread per CTA; the
-// acquire load orders the reads that follow it (with the __syncthreads that
-// comes after, for the whole CTA).
+// Spins (bounded in time) until *p >= target.  One thread per CTA (the
+// others wait at a barrier, so the poll takes no issue slots from work and
+// does not sleep between loads); the acquire load orders the reads that
+// follow it (with the __syncthreads that comes after, for the whole CTA).
 __device__ bool wait_counter(const uint64_t* p, uint64_t target) {
   if (ld_acquire_u64(p) >= target) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    __nanosleep(32);
     if (ld_acquire_u64(p) >= target) return true;
     if ((it & 63u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
@@ -179,7 +179,8 @@ __device__ __forceinline__ void st_relaxed_f2(float2* p, float2 v) {
   asm volatile("st.relaxed.gpu.global.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(v.x), "f"(v.y)
                : "memory");
 }
-// Polls `n` partials until every one has been written (bounded in time).
+// Polls `n` partials until every one has been written (bounded in time);
+// one warp polls while the rest of the CTA waits at a barrier.
 __device__ bool poll_partials(const float2* p, int n, float2* v) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
@@ -192,7 +193,6 @@ __device__ bool poll_partials(const float2* p, int n, float2* v) {
       }
     if (all) return true;
     if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    __nanosleep(32);
   }
 }
 
@@ -239,9 +239,11 @@ __device__ __forceinline__ float dot16_f32(const uint2& c, const float* hv) {
   return (a0 + a1) + (a2 + a3);
 }
 
-template <int NBG>
+// KH, KI: hidden and inter when fixed at compile time (0: the runtime
+// arguments), which turns the record, slice and x offsets into immediates.
+template <int NBG, int KH, int KI>
 __global__ void __launch_bounds__(kFThreads, 1)
-    moe_fused_kernel(const uint16_t* __restrict__ x, int hidden, int inter,
+    moe_fused_kernel(const uint16_t* __restrict__ x, int hidden_arg, int inter_arg,
                      const uint16_t* __restrict__ wr, int E, int top_k,
                      const uint8_t* const* __restrict__ gu_tab,
                      const uint8_t* const* __restrict__ dn_tab, uint16_t* __restrict__ out,
@@ -249,6 +251,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
                      float* __restrict__ out_prob, uint8_t* __restrict__ ws, int split,
                      MoePlan P, int32_t* err) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const int hidden = KH > 0 ? KH : hidden_arg;
+  const int inter = KI > 0 ? KI : inter_arg;
   const SwigluRecord Lg(hidden);
   const ColSlices Ld(hidden, inter);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -303,11 +307,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
     fence_mbar_init();
   }
   // The expert tables, like the weights, are not written by the previous
-  // kernel: copy them in while that kernel finishes.
-  for (int e = threadIdx.x; e < E; e += kFThreads) {
-    tab_g[e] = gu_tab[e];
-    tab_d[e] = dn_tab[e];
-  }
+  // kernel: their loads are issued now and stay in flight through the
+  // router phase; the values go to shared memory just before the routing
+  // decision reads them (E <= kMaxExperts <= kFThreads).
+  const uint8_t* my_tab_g = threadIdx.x < E ? gu_tab[threadIdx.x] : nullptr;
+  const uint8_t* my_tab_d = threadIdx.x < E ? dn_tab[threadIdx.x] : nullptr;
   // Router weights do not depend on the previous kernel: warm L2 with this
   // CTA's slices while that kernel finishes.
   if (threadIdx.x == 0)
@@ -405,6 +409,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
       xs[(ch & 3) * Lg.nblk + (ch >> 2)] = o;  // chunk q = ch % 4 of block ch / 4
     }
   }
+
+  if (threadIdx.x < E) {
+    tab_g[threadIdx.x] = my_tab_g;
+    tab_d[threadIdx.x] = my_tab_d;
+  }  // read after the __syncthreads that ends the routing decision
 
   // ---- routing decision (every CTA, same fixed-order fold) ---------------
   // Warp 0 polls this CTA's replica until every partial has arrived (the
@@ -762,9 +771,11 @@ cudaError_t launch_moe_fused(const uint16_t* x, int hidden, int inter, const uin
     }
     return r;
   };
+  // gpt-oss-20b's expert shape gets a kernel with the sizes fixed
+  if (hidden == 2880 && inter == 2880) return go(moe_fused_kernel<3, 2880, 2880>);
   switch ((hidden / 32 + 31) / 32) {
 #define TT_FU(nb) \
-  case nb: return go(moe_fused_kernel<nb>);
+  case nb: return go(moe_fused_kernel<nb, 0, 0>);
     TT_FU(1) TT_FU(2) TT_FU(3) TT_FU(4) TT_FU(5) TT_FU(6) TT_FU(7) TT_FU(8)
 #undef TT_FU
     default: return cudaErrorInvalidValue;
