@@ -194,6 +194,112 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   }
 }
 
+// m = 1 with K fixed at compile time (the down projection of the models the
+// library serves): a warp owns whole rows, and all of a row's code chunks
+// and scale bytes (U = ceil(K / 1024) per lane) are requested in one wave,
+// the first row's before the dependency wait, so that the whole matrix is
+// in flight while the previous kernel finishes.  Only the one partial chunk
+// of a lane is tested against the row's end; every offset is an immediate.
+// Same arithmetic as mxfp4_rows_kernel at m = 1 (measured there: a fixed
+// 8-chunk step that leaves two thirds of the second step empty at
+// K = 11008, and 6.3 instructions per weight).
+template <int KC>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    mxfp4_rows_k_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                        const float* __restrict__ post, int n, int /*k*/,
+                        const uint16_t* __restrict__ x, int /*m*/, uint16_t* __restrict__ y,
+                        int /*ks*/) {
+  static_assert(KC % 32 == 0 && KC / 32 <= 32 * 12, "one wave of at most 12 chunks per lane");
+  constexpr int kNblk = KC / 32;
+  constexpr int kU1 = (kNblk + 31) / 32;  // chunks per lane
+  constexpr int kFull = kNblk / 32;       // chunks every lane has
+  constexpr int kCh = KC / 8;             // 16-byte chunks of x
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint4* xs = reinterpret_cast<uint4*>(smem);              // [4 chunks][nblk] f16
+  float* xinv = reinterpret_cast<float*>(xs + 4 * kNblk);  // [nblk]
+  const uint64_t pol = l2_evict_first_policy();
+  const int rstep = gridDim.x * kWarps;
+
+  uint4 cv[kU1];
+  uint32_t sv[kU1];
+  auto load = [&](int r) {
+    const uint8_t* cr = codes + (size_t)r * (KC / 2);
+    const uint8_t* sr = scales + (size_t)r * kNblk;
+#pragma unroll
+    for (int u = 0; u < kU1; ++u) {
+      const int b = 32 * u + lane;
+      cv[u] = make_uint4(0u, 0u, 0u, 0u);
+      sv[u] = 0u;
+      if (u < kFull || b < kNblk) {
+        cv[u] = ld_global_v4_hint(cr + 16 * b, pol);
+        sv[u] = __ldcs(sr + b);
+      }
+    }
+  };
+  int r = blockIdx.x * kWarps + warp;  // warp-uniform
+  pdl_allow_next_grid();
+  if (r < n) load(r);  // weights do not depend on the previous kernel
+  pdl_wait_prior_grid();
+
+  // x: per 32-block exact prescale, four threads per block (as above)
+  for (int c0 = 0; c0 < kCh; c0 += 4 * kWarps * 32) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * kWarps * 32 + threadIdx.x;
+      v[u] = c < kCh ? reinterpret_cast<const uint4*>(x)[c] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * kWarps * 32 + threadIdx.x;
+      const uint4 w4 = v[u];
+      float mx = fmaxf(fmaxf(fmaxf(fabsf(bf16_bits_to_f32(w4.x & 0xFFFFu)), fabsf(bf16_bits_to_f32(w4.x >> 16))),
+                             fmaxf(fabsf(bf16_bits_to_f32(w4.y & 0xFFFFu)), fabsf(bf16_bits_to_f32(w4.y >> 16)))),
+                       fmaxf(fmaxf(fabsf(bf16_bits_to_f32(w4.z & 0xFFFFu)), fabsf(bf16_bits_to_f32(w4.z >> 16))),
+                             fmaxf(fabsf(bf16_bits_to_f32(w4.w & 0xFFFFu)), fabsf(bf16_bits_to_f32(w4.w >> 16)))));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      if (c < kCh) {
+        const int sb = min(f16_prescale_exponent(mx), 127);
+        const float two_s = scalbnf(1.0f, sb);
+        uint4 o;
+        o.x = pack_f16x2_scaled(bf16_bits_to_f32(w4.x & 0xFFFFu), bf16_bits_to_f32(w4.x >> 16), two_s);
+        o.y = pack_f16x2_scaled(bf16_bits_to_f32(w4.y & 0xFFFFu), bf16_bits_to_f32(w4.y >> 16), two_s);
+        o.z = pack_f16x2_scaled(bf16_bits_to_f32(w4.z & 0xFFFFu), bf16_bits_to_f32(w4.z >> 16), two_s);
+        o.w = pack_f16x2_scaled(bf16_bits_to_f32(w4.w & 0xFFFFu), bf16_bits_to_f32(w4.w >> 16), two_s);
+        xs[(c & 3) * kNblk + (c >> 2)] = o;  // chunk q of block b
+        if ((c & 3) == 0) xinv[c >> 2] = scalbnf(1.0f, -sb);  // exact
+      }
+    }
+  }
+  __syncthreads();
+
+  for (; r < n; r += rstep) {
+    float acc = 0.f;
+#pragma unroll
+    for (int u = 0; u < kU1; ++u) {
+      const int b = 32 * u + lane;
+      if (u < kFull || b < kNblk) {
+        uint32_t hc[16], xv[16];
+        decode32(cv[u], hc);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 t = xs[q * kNblk + b];
+          xv[4 * q + 0] = t.x;
+          xv[4 * q + 1] = t.y;
+          xv[4 * q + 2] = t.z;
+          xv[4 * q + 3] = t.w;
+        }
+        acc = fmaf(dot32_decoded(hc, xv), e8m0_to_f32(sv[u]) * xinv[b], acc);
+      }
+    }
+    if (r + rstep < n) load(r + rstep);  // the warp's next row, in flight during the reduction
+    const float v = warp_sum(acc);
+    if (lane == 0) y[r] = f32_to_bf16_rne(v * (post ? post[r] : 1.f));
+  }
+}
+
 template <int MT>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     bf16_rows_kernel(const uint16_t* __restrict__ w, int n, int k,
@@ -331,6 +437,10 @@ cudaError_t launch_mxfp4_rows(const uint8_t* codes, const uint8_t* scales, const
                               bool pdl) {
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorNoDevice;
+  // SmolLM3-3B's down projection (K = 11008) gets the one-wave kernel
+  if (m == 1 && k == 11008)
+    return launch_rows(*di, mxfp4_rows_k_kernel<11008>, n, 1, 2 * k + 4 * (k / 32), s, pdl, codes,
+                       scales, post, n, k, x, m, y);
   if (m == 1) return run_mxfp4_rows<1>(*di, codes, scales, post, n, k, x, m, y, s, pdl);
   if (m == 2) return run_mxfp4_rows<2>(*di, codes, scales, post, n, k, x, m, y, s, pdl);
   if (m <= 4) return run_mxfp4_rows<4>(*di, codes, scales, post, n, k, x, m, y, s, pdl);

@@ -37,7 +37,11 @@ def _mxfp4_rows(n, k, m, post=True, wid=130, x=None):
 @pytest.mark.parametrize("n,k,m,post", [(1, 32, 1, True), (7, 96, 2, False), (129, 1024, 1, True),
                                         (300, 2880, 3, True), (33, 5120, 8, False),
                                         (21, 16384, 1, True), (64, 8192, 4, True),
-                                        (2048, 11008, 1, False)])
+                                        (2048, 11008, 1, False),
+                                        # K = 11008 at m = 1: the one-wave kernel, with one row
+                                        # per warp, two rows for some warps, and few rows
+                                        (2048, 11008, 1, True), (3001, 11008, 1, True),
+                                        (5, 11008, 1, False), (2048, 11008, 2, True)])
 def test_mxfp4_matvec_shapes(n, k, m, post):
     y, ref = _mxfp4_rows(n, k, m, post)
     for i in range(m):
