@@ -60,7 +60,10 @@ def test_mxfp4_matvec_blocks_of_very_different_magnitude():
 
 
 @pytest.mark.parametrize("n,k,m", [(1, 8, 1), (37, 96, 2), (300, 2880, 5), (2048, 11008, 1),
-                                   (65, 4104, 8)])
+                                   (65, 4104, 8),
+                                   # K = 11008 at m = 1: one row per CTA step; rows beyond
+                                   # two per CTA, and fewer rows than CTAs
+                                   (3001, 11008, 1), (5, 11008, 1), (700, 11008, 2)])
 def test_bf16_matvec_shapes(n, k, m):
     import torch
     d = synth.bf16_gate_up_inputs(132, 0, n, k, m=m)
