@@ -37,6 +37,7 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kU = 8;  // 16-byte chunks per lane in flight per row
+constexpr int kRowsKMaxWarps = 16;  // one-wave MXFP4 kernel: warps per CTA at most
 
 // The K split: a CTA's 8 warps take R = 8 / ks rows at a time, ks warps per
 // row, warp (lr, sl) the sl-th slice of row rb + lr's K; the slices' sums
@@ -195,7 +196,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 }
 
 // m = 1 with K fixed at compile time (the down projection of the models the
-// library serves): a warp owns whole rows, and all of a row's code chunks
+// library serves): one CTA per SM of ceil(n / SMs) warps (at most
+// kRowsKMaxWarps), so the rows spread evenly over the SMs and each SM stages
+// x once; a warp owns whole rows, and all of a row's code chunks
 // and scale bytes (U = ceil(K / 1024) per lane) are requested in one wave,
 // the first row's before the dependency wait, so that the whole matrix is
 // in flight while the previous kernel finishes.  Only the one partial chunk
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 // 8-chunk step that leaves two thirds of the second step empty at
 // K = 11008, and 6.3 instructions per weight).
 template <int KC>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kRowsKMaxWarps * 32, 1)
     mxfp4_rows_k_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
                         const float* __restrict__ post, int n, int /*k*/,
                         const uint16_t* __restrict__ x, int /*m*/, uint16_t* __restrict__ y,
@@ -216,10 +219,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   constexpr int kCh = KC / 8;             // 16-byte chunks of x
   extern __shared__ __align__(16) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int W = blockDim.x >> 5;  // warps of the CTA
   uint4* xs = reinterpret_cast<uint4*>(smem);              // [4 chunks][nblk] f16
   float* xinv = reinterpret_cast<float*>(xs + 4 * kNblk);  // [nblk]
   const uint64_t pol = l2_evict_first_policy();
-  const int rstep = gridDim.x * kWarps;
+  const int rstep = gridDim.x * W;
 
   uint4 cv[kU1];
   uint32_t sv[kU1];
@@ -237,22 +241,22 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
       }
     }
   };
-  int r = blockIdx.x * kWarps + warp;  // warp-uniform
+  int r = blockIdx.x * W + warp;  // warp-uniform
   pdl_allow_next_grid();
   if (r < n) load(r);  // weights do not depend on the previous kernel
   pdl_wait_prior_grid();
 
   // x: per 32-block exact prescale, four threads per block (as above)
-  for (int c0 = 0; c0 < kCh; c0 += 4 * kWarps * 32) {
+  for (int c0 = 0; c0 < kCh; c0 += 4 * (int)blockDim.x) {
     uint4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int c = c0 + u * kWarps * 32 + threadIdx.x;
+      const int c = c0 + u * (int)blockDim.x + threadIdx.x;
       v[u] = c < kCh ? reinterpret_cast<const uint4*>(x)[c] : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int c = c0 + u * kWarps * 32 + threadIdx.x;
+      const int c = c0 + u * (int)blockDim.x + threadIdx.x;
       const uint4 w4 = v[u];
       float mx = fmaxf(fmaxf(fmaxf(fabsf(bf16_bits_to_f32(w4.x & 0xFFFFu)), fabsf(bf16_bits_to_f32(w4.x >> 16))),
                              fmaxf(fabsf(bf16_bits_to_f32(w4.y & 0xFFFFu)), fabsf(bf16_bits_to_f32(w4.y >> 16)))),
@@ -421,6 +425,31 @@ cudaError_t launch_rows(const DeviceInfo& di, Kern kern, int n, int ks, int smem
   return cudaLaunchKernelEx(&cfg, kern, args..., ks);
 }
 
+// One CTA per SM with ceil(n / SMs) warps (rows spread evenly over the SMs).
+template <class Kern, class... Args>
+cudaError_t launch_rows_k(const DeviceInfo& di, Kern kern, int n, int smem, cudaStream_t s,
+                          bool pdl, Args... args) {
+  if (smem > di.smem_optin) return cudaErrorInvalidConfiguration;
+  const cudaError_t e = ensure_smem(di, kern, smem);
+  if (e != cudaSuccess) return e;
+  int warps = (n + di.sms - 1) / di.sms;
+  if (warps > kRowsKMaxWarps) warps = kRowsKMaxWarps;
+  if (warps < 1) warps = 1;
+  int grid = (n + warps - 1) / warps;
+  if (grid > di.sms) grid = di.sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(warps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args..., 1);
+}
+
 template <int MT>
 cudaError_t run_mxfp4_rows(const DeviceInfo& di, const uint8_t* codes, const uint8_t* scales,
                            const float* post, int n, int k, const uint16_t* x, int m, uint16_t* y,
@@ -519,8 +548,8 @@ cudaError_t launch_mxfp4_rows(const uint8_t* codes, const uint8_t* scales, const
   if (!di) return cudaErrorNoDevice;
   // SmolLM3-3B's down projection (K = 11008) gets the one-wave kernel
   if (m == 1 && k == 11008)
-    return launch_rows(*di, mxfp4_rows_k_kernel<11008>, n, 1, 2 * k + 4 * (k / 32), s, pdl, codes,
-                       scales, post, n, k, x, m, y);
+    return launch_rows_k(*di, mxfp4_rows_k_kernel<11008>, n, 2 * k + 4 * (k / 32), s, pdl, codes,
+                         scales, post, n, k, x, m, y);
   if (m == 1) return run_mxfp4_rows<1>(*di, codes, scales, post, n, k, x, m, y, s, pdl);
   if (m == 2) return run_mxfp4_rows<2>(*di, codes, scales, post, n, k, x, m, y, s, pdl);
   if (m <= 4) return run_mxfp4_rows<4>(*di, codes, scales, post, n, k, x, m, y, s, pdl);
