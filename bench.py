@@ -287,9 +287,9 @@ MXFP4_M1_KERNEL = "swiglu_mxfp4_m1x_kernel"
 # code on the same shape, or None where no such capture exists).
 WORKLOAD_KERNELS = {
     "fp8_gate_up_k2048_n11008_m1": ("fp8_pair_kernel", "hbm", 45209088),
-    "bf16_down_k11008_n2048_m1": ("bf16_rows_k_kernel", "hbm", None),
+    "bf16_down_k11008_n2048_m1": ("bf16_rows_k_kernel", "hbm", 45119488),
     "fp8_down_k11008_n2048_m1": ("fp8_pair_kernel", "hbm", None),
-    "mxfp4_down_k11008_n2048_m1": ("mxfp4_rows_k_kernel", "hbm", None),
+    "mxfp4_down_k11008_n2048_m1": ("mxfp4_rows_k_kernel", "hbm", 12020224),
     "gptoss20b_int4_qkv_k2880_n5120_g128": ("int4_mma_kernel", "hbm", 7704832),
     "gptoss20b_moe_h2880_e32_top4": ("moe_fused_kernel", "hbm", 53537536),
     "gptoss20b_moe_q1_h2880_e32_top4": ("lowbit_router_kernel + lowbit_swiglu_kernel + "
