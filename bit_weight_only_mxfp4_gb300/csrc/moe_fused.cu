@@ -253,6 +253,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
   extern __shared__ __align__(128) uint8_t smem[];
   const int hidden = KH > 0 ? KH : hidden_arg;
   const int inter = KI > 0 ? KI : inter_arg;
+  // With hidden fixed, the host launches this instance only with whole-
+  // column down items (P.rc == hidden, one row chunk): the rows each thread
+  // owns, and which of them exist, are then known at compile time.
+  constexpr bool kOneChunk = KH > 0 && KH <= kMaxChunkRows;
+  const int rc = kOneChunk ? KH : P.rc;
   const SwigluRecord Lg(hidden);
   const ColSlices Ld(hidden, inter);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -497,14 +502,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
   auto issue_dn = [&](int k) {  // one thread: down item k -> slot k % dslots
     const int ch = k / nhb, i = k - ch * nhb;
     const int g = hb0 + i, j = g / spe, sl = g - j * spe;
-    const int r0 = ch * P.rc, nr = min(P.rc, hidden - r0);
+    const int r0 = ch * rc, nr = min(rc, hidden - r0);
     const int s = k % P.dslots;
     const uint32_t bar = smem_u32(&dbars[s]);
     uint8_t* dst = dring + (size_t)s * P.item;
     const uint8_t* src = tab_d[sidx[j]];
     mbar_arrive_expect_tx(bar, uint32_t(nr * 9));
     bulk_g2s(smem_u32(dst), src + Ld.code_at(sl, r0), uint32_t(nr * 8), bar, policy);
-    bulk_g2s(smem_u32(dst + (size_t)P.rc * 8), src + Ld.scale_at(sl >> 1, r0), uint32_t(nr), bar,
+    bulk_g2s(smem_u32(dst + (size_t)rc * 8), src + Ld.scale_at(sl >> 1, r0), uint32_t(nr), bar,
              policy);
   };
   if (lane == 0)
@@ -527,7 +532,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   // the last of the 16 warps to finish a slot refills it.
   auto do_down = [&]() {
     const int ch = kd_ch, i = kd_i;
-    const int r0 = ch * P.rc, nr = min(P.rc, hidden - r0);
+    const int r0 = kOneChunk ? 0 : ch * rc, nr = kOneChunk ? KH : min(rc, hidden - r0);
     const int s = kd_s;
     const uint8_t* slot = dring + (size_t)s * P.item;
     float hv[16];
@@ -545,7 +550,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       const int r = threadIdx.x + m * kFThreads;  // row within the chunk
       if (r < nr) {
         const uint2 cw = *reinterpret_cast<const uint2*>(slot + (size_t)r * 8);
-        const float ps = pj * e8m0_to_f32(slot[(size_t)P.rc * 8 + r]);  // exact
+        const float ps = pj * e8m0_to_f32(slot[(size_t)rc * 8 + r]);  // exact
         acc[m] = fmaf(ps, dot16_f32(cw, hv), acc[m]);
       }
     }
@@ -772,7 +777,8 @@ cudaError_t launch_moe_fused(const uint16_t* x, int hidden, int inter, const uin
     return r;
   };
   // gpt-oss-20b's expert shape gets a kernel with the sizes fixed
-  if (hidden == 2880 && inter == 2880) return go(moe_fused_kernel<3, 2880, 2880>);
+  if (hidden == 2880 && inter == 2880 && plan.rc == hidden)
+    return go(moe_fused_kernel<3, 2880, 2880>);
   switch ((hidden / 32 + 31) / 32) {
 #define TT_FU(nb) \
   case nb: return go(moe_fused_kernel<nb, 0, 0>);
