@@ -291,7 +291,7 @@ WORKLOAD_KERNELS = {
     "fp8_down_k11008_n2048_m1": ("fp8_pair_kernel", "hbm", None),
     "mxfp4_down_k11008_n2048_m1": ("mxfp4_rows_k_kernel", "hbm", 12020224),
     "gptoss20b_int4_qkv_k2880_n5120_g128": ("int4_mma_kernel", "hbm", 7704832),
-    "gptoss20b_moe_h2880_e32_top4": ("moe_fused_kernel", "hbm", None),
+    "gptoss20b_moe_h2880_e32_top4": ("moe_fused_kernel", "hbm", 53512192),
     "gptoss20b_moe_q1_h2880_e32_top4": ("lowbit_router_kernel + lowbit_swiglu_kernel + "
                                         "lowbit_down_kernel", "hbm", 14180864),
     "gptoss20b_moe_q2_h2880_e32_top4": ("lowbit_router_kernel + lowbit_swiglu_kernel + "
