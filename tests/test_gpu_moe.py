@@ -39,6 +39,9 @@ def _case(E, H, I, K, wid, tie_rows=None):
 
 @pytest.mark.parametrize("E,H,I,K", [(6, 64, 96, 3), (8, 320, 640, 4), (32, 1024, 512, 4),
                                      (5, 2880, 2880, 1), (16, 256, 2048, 8),
+                                     # the gpt-oss expert shape (its own kernel instance) at
+                                     # top-8: about ten 16-wide h slices per CTA
+                                     (8, 2880, 2880, 8),
                                      (8, 4096, 1024, 8),
                                      # the down columns come in two row chunks of 3584 and
                                      # 1024 rows (shared memory too small for whole columns)
