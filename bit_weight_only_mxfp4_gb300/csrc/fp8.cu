@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int c = c0 + u * kWarps * 32 + threadIdx.x;
-        v[u] = c < k / 8 ? *reinterpret_cast<const uint4*>(x + (size_t)i * k + 8 * c)
+        v[u] = c < k / 8 ? __ldca(reinterpret_cast<const uint4*>(x + (size_t)i * k + 8 * c))
                          : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
@@ -195,8 +195,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int off = (rem >> 5) * 512 + 16 * (rem & 31);
     uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
     if (i < m && off < k) {
-      v0 = *reinterpret_cast<const uint4*>(x + (size_t)i * k + off);
-      v1 = *reinterpret_cast<const uint4*>(x + (size_t)i * k + off + 8);
+      v0 = __ldca(reinterpret_cast<const uint4*>(x + (size_t)i * k + off));
+      v1 = __ldca(reinterpret_cast<const uint4*>(x + (size_t)i * k + off + 8));
     }
     const float two_s = scalbnf(1.0f, sx[i]);
     uint4 o0, o1;

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int c = c0 + threadIdx.x;
     const int i = c / (k >> 3), t8 = c - i * (k >> 3);  // x[8*t8 .. 8*t8+7] of row i
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (c < n8 && i < m) v = reinterpret_cast<const uint4*>(x + (size_t)i * k)[t8];
+    if (c < n8 && i < m) v = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)i * k) + t8);
     const float e0 = bf16_bits_to_f32(v.x & 0xFFFFu), e1 = bf16_bits_to_f32(v.x >> 16);
     const float e2 = bf16_bits_to_f32(v.y & 0xFFFFu), e3 = bf16_bits_to_f32(v.y >> 16);
     const float e4 = bf16_bits_to_f32(v.z & 0xFFFFu), e5 = bf16_bits_to_f32(v.z >> 16);

@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float mx = 0.f;
     if (i < m)
       for (int t = threadIdx.x; t < k; t += kThreads)
-        mx = fmaxf(mx, fabsf(bf16_bits_to_f32(x[(size_t)i * k + t])));
+        mx = fmaxf(mx, fabsf(bf16_bits_to_f32(__ldca(x + (size_t)i * k + t))));
     mx = warp_max(mx);
     if (lane == 0) red[i * kWarps + warp] = mx;
   }
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint4 o = make_uint4(0, 0, 0, 0);
     if (i < m) {
       const float two_s = scalbnf(1.0f, sxs[i]);
-      const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)i * k + b * 32 + q * 8);
+      const uint4 v = __ldca(reinterpret_cast<const uint4*>(x + (size_t)i * k + b * 32 + q * 8));
       o.x = pack_f16x2_scaled(bf16_bits_to_f32(v.x & 0xFFFFu), bf16_bits_to_f32(v.x >> 16), two_s);
       o.y = pack_f16x2_scaled(bf16_bits_to_f32(v.y & 0xFFFFu), bf16_bits_to_f32(v.y >> 16), two_s);
       o.z = pack_f16x2_scaled(bf16_bits_to_f32(v.z & 0xFFFFu), bf16_bits_to_f32(v.z >> 16), two_s);

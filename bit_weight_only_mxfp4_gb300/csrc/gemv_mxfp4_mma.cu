@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int b = warp + kMmaWarps * j;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (j < cnt && g < m)
-      v = *reinterpret_cast<const uint4*>(x + (size_t)g * k + 32 * b + 8 * t);
+      v = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)g * k + 32 * b + 8 * t));
     float mx = bf16_abs_max8(v);
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));

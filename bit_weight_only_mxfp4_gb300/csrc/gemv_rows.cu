@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
       const int c = c0 + u * kWarps * 32 + threadIdx.x;
       const int i = c / (k >> 3), cc = c - i * (k >> 3);
       v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (c < nch && i < m) v[u] = *reinterpret_cast<const uint4*>(x + (size_t)i * k + 8 * cc);
+      if (c < nch && i < m) v[u] = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)i * k + 8 * cc));
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kRowsKMaxWarps * 32, 1)
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int c = c0 + u * (int)blockDim.x + threadIdx.x;
-      v[u] = c < kCh ? reinterpret_cast<const uint4*>(x)[c] : make_uint4(0u, 0u, 0u, 0u);
+      v[u] = c < kCh ? __ldcg(reinterpret_cast<const uint4*>(x) + c) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
           if (i < m) {
-            const uint4 xv = __ldg(x4 + (size_t)i * cpr + c);
+            const uint4 xv = __ldca(x4 + (size_t)i * cpr + c);
             fma_bf16x2_f32(a0[i], a1[i], wc[u].x, xv.x);
             fma_bf16x2_f32(a0[i], a1[i], wc[u].y, xv.y);
             fma_bf16x2_f32(a0[i], a1[i], wc[u].z, xv.z);
@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     for (int u = 0; u < kU1; ++u) {
       const int c = 32 * u + lane;
       if (u < kFull || c < kCps) {
-        const uint4 xv = __ldg(x4 + c0 + c);
+        const uint4 xv = __ldca(x4 + c0 + c);
         fma_bf16x2_f32(a0, a1, wv[u].x, xv.x);
         fma_bf16x2_f32(a0, a1, wv[u].y, xv.y);
         fma_bf16x2_f32(a0, a1, wv[u].z, xv.z);

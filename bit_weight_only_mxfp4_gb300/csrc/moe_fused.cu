@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const int c0 = p * cs, c1 = min(nch, c0 + cs);
     float s = 0.f, cc = 0.f;
     for (int ch = c0 + threadIdx.x; ch < c1; ch += kFThreads) {
-      const uint4 a = x4[ch];
+      const uint4 a = __ldcg(x4 + ch);
       const uint4 b = __ldcs(w4 + (size_t)e * nch + ch);
       const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
       const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll
   for (int i = 0; i < kMaxXChunksPerThread; ++i) {
     const int ch = threadIdx.x + i * kFThreads;
-    xr[i] = ch < nch ? x4[ch] : make_uint4(0u, 0u, 0u, 0u);
+    xr[i] = ch < nch ? __ldcg(x4 + ch) : make_uint4(0u, 0u, 0u, 0u);
     const uint32_t vw[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e)

@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * k);
 #pragma unroll 4
           for (int c = lane; c < nch; c += 32) {
-            const uint4 v = xr[c];
+            const uint4 v = __ldcg(xr + c);
             const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e)

@@ -129,6 +129,15 @@ def test_fp8_down_projection_full_smollm3_shape():
     assert_float_parity(h, ref, "fp8 down 2048x11008")
 
 
+@pytest.mark.parametrize("n", [1, 5, 303, 3001])
+def test_fp8_down_projection_k11008_row_counts(n):
+    """K = 11008 at m = 1 (one row per CTA step): fewer rows than CTAs, about
+    one per CTA, and rows beyond the rows in flight of every CTA."""
+    h, ref = _fp8_case(n, 11008, 1, wid=125, swiglu=False)
+    assert_float_parity(h, ref, f"fp8 down {n}x11008")
+    assert gu.device_error() == 0
+
+
 def test_fp8_large_and_outlier_activations():
     n, k, m = 64, 2048, 3
     d = synth.gate_up_inputs(124, 0, n, k, m=m)
