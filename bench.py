@@ -277,7 +277,7 @@ def cpu_baseline(target_s: float = 8.0):
 # set an entry back to None whenever its kernel changes.
 DRAM_TRAFFIC = {
     "swiglu_mxfp4_m1x_kernel": 24154624,
-    "swiglu_bf16_kernel": None,
+    "swiglu_bf16_kernel": 92470784,
 }
 # The kernel that serves the batch-1 MXFP4 gate/up layer at K = 2048.
 MXFP4_M1_KERNEL = "swiglu_mxfp4_m1x_kernel"
@@ -286,12 +286,12 @@ MXFP4_M1_KERNEL = "swiglu_mxfp4_m1x_kernel"
 # launch (summed over a call's kernels) from an ncu capture of the current
 # code on the same shape, or None where no such capture exists).
 WORKLOAD_KERNELS = {
-    "fp8_gate_up_k2048_n11008_m1": ("fp8_pair_kernel", "hbm", None),
-    "bf16_down_k11008_n2048_m1": ("bf16_rows_k_kernel", "hbm", None),
+    "fp8_gate_up_k2048_n11008_m1": ("fp8_pair_kernel", "hbm", 45207808),
+    "bf16_down_k11008_n2048_m1": ("bf16_rows_k_kernel", "hbm", 45119744),
     "fp8_down_k11008_n2048_m1": ("fp8_pair_kernel", "hbm", None),
-    "mxfp4_down_k11008_n2048_m1": ("mxfp4_rows_k_kernel", "hbm", None),
+    "mxfp4_down_k11008_n2048_m1": ("mxfp4_rows_k_kernel", "hbm", 12020736),
     "gptoss20b_int4_qkv_k2880_n5120_g128": ("int4_mma_kernel", "hbm", 7704832),
-    "gptoss20b_moe_h2880_e32_top4": ("moe_fused_kernel", "hbm", None),
+    "gptoss20b_moe_h2880_e32_top4": ("moe_fused_kernel", "hbm", 53517824),
     "gptoss20b_moe_q1_h2880_e32_top4": ("lowbit_router_kernel + lowbit_swiglu_kernel + "
                                         "lowbit_down_kernel", "hbm", 14180864),
     "gptoss20b_moe_q2_h2880_e32_top4": ("lowbit_router_kernel + lowbit_swiglu_kernel + "
