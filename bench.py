@@ -286,7 +286,7 @@ MXFP4_M1_KERNEL = "swiglu_mxfp4_m1x_kernel"
 # launch (summed over a call's kernels) from an ncu capture of the current
 # code on the same shape, or None where no such capture exists).
 WORKLOAD_KERNELS = {
-    "fp8_gate_up_k2048_n11008_m1": ("fp8_pair_kernel", "hbm", 45207808),
+    "fp8_gate_up_k2048_n11008_m1": ("fp8_swiglu_k_kernel", "hbm", None),
     "bf16_down_k11008_n2048_m1": ("bf16_rows_k_kernel", "hbm", 45119744),
     "fp8_down_k11008_n2048_m1": ("fp8_pair_kernel", "hbm", None),
     "mxfp4_down_k11008_n2048_m1": ("mxfp4_rows_k_kernel", "hbm", 12020736),

@@ -339,6 +339,128 @@ cudaError_t run_pair(const DeviceInfo& di, const uint8_t* wa, const float* sa, c
   return cudaLaunchKernelEx(&cfg, kern, wa, sa, wb, sb, n, k, x, m, y, ks);
 }
 
+// Gate/up SwiGLU at m = 1 with K fixed at compile time (the gate/up layers
+// of the models the library serves): a warp per row pair (gate row r, up
+// row r), both rows' codes requested at once (KC / 512 chunks of 16 codes
+// per lane and row), the warp's next pair in flight while the current one
+// is computed, the first pair before the dependency wait.  x is staged once
+// per CTA in shared memory with coherent loads after the wait: chunk c of
+// the row (x[16 c .. 16 c + 15]) as f16 after an exact power-of-two prescale
+// per chunk (its max |x| -> [2^14, 2^15)), kept as two arrays of 16-byte
+// halves so a warp's reads are conflict-free, the inverse applied to the
+// chunk's partial sums.  Codes are widened with cvt.rn.f16x2.e4m3x2 and
+// multiplied by fma.rn.f32.f16 (exact products, fp32 sums); the row scales
+// and SwiGLU follow the warp's reduction.
+template <int KC>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    fp8_swiglu_k_kernel(const uint8_t* __restrict__ gc, const float* __restrict__ gs,
+                        const uint8_t* __restrict__ uc, const float* __restrict__ us, int n,
+                        const uint16_t* __restrict__ x, uint16_t* __restrict__ h) {
+  static_assert(KC % 512 == 0, "whole 16-code chunks for every lane");
+  constexpr int kU = KC / 512;    // chunks per lane and row
+  constexpr int kCh = KC / 16;    // chunks per row
+  __shared__ uint4 xlo[kCh], xhi[kCh];  // f16 x[16 c .. 16 c + 7], x[16 c + 8 .. 16 c + 15]
+  __shared__ float xinv[kCh];           // 2^-s of chunk c
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int nw = gridDim.x * kWarps;
+  auto load = [&](int r, uint4 (&a)[kU], uint4 (&b)[kU]) {
+    const uint4* g4 = reinterpret_cast<const uint4*>(gc + (size_t)r * KC);
+    const uint4* u4 = reinterpret_cast<const uint4*>(uc + (size_t)r * KC);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      a[u] = __ldcs(g4 + 32 * u + lane);
+      b[u] = __ldcs(u4 + 32 * u + lane);
+    }
+  };
+  uint4 ga[kU], ua[kU], gb[kU], ub[kU];  // two pairs in flight
+  pdl_allow_next_grid();
+  if (gw < n) load(gw, ga, ua);  // weights do not depend on the producer of x
+  if (gw + nw < n) load(gw + nw, gb, ub);
+  pdl_wait_prior_grid();
+
+  {  // coherent loads: the previous kernel wrote x
+    const uint4* x4 = reinterpret_cast<const uint4*>(x);
+    for (int c = threadIdx.x; c < kCh; c += kWarps * 32) {
+      const uint4 va = __ldcg(x4 + 2 * c), vb = __ldcg(x4 + 2 * c + 1);
+      const uint32_t w[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+      float mx = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(w[e] & 0xFFFFu)),
+                             fabsf(bf16_bits_to_f32(w[e] >> 16))));
+      const int sb = mx > 0.f ? min(f16_prescale_exponent(mx), 127) : 0;
+      const float two_s = scalbnf(1.0f, sb);
+      uint32_t o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        o[e] = pack_f16x2_scaled(bf16_bits_to_f32(w[e] & 0xFFFFu), bf16_bits_to_f32(w[e] >> 16), two_s);
+      xlo[c] = make_uint4(o[0], o[1], o[2], o[3]);
+      xhi[c] = make_uint4(o[4], o[5], o[6], o[7]);
+      xinv[c] = scalbnf(1.0f, -sb);  // exact
+    }
+  }
+  __syncthreads();
+  // sum over the lane's chunks of codes . x (each chunk scaled by its 2^-s)
+  auto dot = [&](const uint4 (&cw)[kU]) {
+    float acc = 0.f;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int c = 32 * u + lane;
+      const uint4 xa = xlo[c], xb = xhi[c];
+      float a0 = 0.f, a1 = 0.f;
+      uint32_t h0, h1;
+      e4m3x4_to_f16x2(cw[u].x, h0, h1);
+      fma_f16x2_f32(a0, a1, h0, xa.x);
+      fma_f16x2_f32(a0, a1, h1, xa.y);
+      e4m3x4_to_f16x2(cw[u].y, h0, h1);
+      fma_f16x2_f32(a0, a1, h0, xa.z);
+      fma_f16x2_f32(a0, a1, h1, xa.w);
+      e4m3x4_to_f16x2(cw[u].z, h0, h1);
+      fma_f16x2_f32(a0, a1, h0, xb.x);
+      fma_f16x2_f32(a0, a1, h1, xb.y);
+      e4m3x4_to_f16x2(cw[u].w, h0, h1);
+      fma_f16x2_f32(a0, a1, h0, xb.z);
+      fma_f16x2_f32(a0, a1, h1, xb.w);
+      acc = fmaf(a0 + a1, xinv[c], acc);
+    }
+    return acc;
+  };
+  auto pair = [&](int r, const uint4 (&cg)[kU], const uint4 (&cu)[kU]) {
+    const float v = warp_sum2(dot(cg), dot(cu), lane);  // lanes 0-15: gate, 16-31: up
+    const float vu = __shfl_sync(0xffffffffu, v, 16);
+    if (lane == 0) h[r] = f32_to_bf16_rne(silu_mul(v * gs[r], vu * us[r]));
+  };
+  for (int r = gw; r < n; r += 2 * nw) {  // warp-uniform
+    pair(r, ga, ua);
+    if (r + 2 * nw < n) load(r + 2 * nw, ga, ua);
+    if (r + nw < n) {
+      pair(r + nw, gb, ub);
+      if (r + 3 * nw < n) load(r + 3 * nw, gb, ub);
+    }
+  }
+}
+
+template <int KC>
+cudaError_t run_swiglu_k(const DeviceInfo& di, const uint8_t* gc, const float* gs,
+                         const uint8_t* uc, const float* us, int n, const uint16_t* x,
+                         uint16_t* h, cudaStream_t s, bool pdl) {
+  int grid = 2 * di.sms;
+  const int need = (n + kWarps - 1) / kWarps;
+  if (grid > need) grid = need;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fp8_swiglu_k_kernel<KC>, gc, gs, uc, us, n, x, h);
+}
+
 template <bool SWIGLU>
 cudaError_t run_fp8(const uint8_t* wa, const float* sa, const uint8_t* wb, const float* sb, int n,
                     int k, const uint16_t* x, int m, uint16_t* y, cudaStream_t s, bool pdl) {
@@ -367,6 +489,11 @@ cudaError_t launch_fp8_matvec(const uint8_t* codes, const float* scales, int n, 
 cudaError_t launch_fp8_swiglu(const uint8_t* gc, const float* gs, const uint8_t* uc,
                               const float* us, int n, int k, const uint16_t* x, int m,
                               uint16_t* h, cudaStream_t s, bool pdl) {
+  if (m == 1 && k == 2048) {  // SmolLM3-3B's gate/up: a warp per row pair
+    const DeviceInfo* di = device_info();
+    if (!di) return cudaErrorNoDevice;
+    return run_swiglu_k<2048>(*di, gc, gs, uc, us, n, x, h, s, pdl);
+  }
   return run_fp8<true>(gc, gs, uc, us, n, k, x, m, h, s, pdl);
 }
 

@@ -150,4 +150,17 @@ def test_fp8_large_and_outlier_activations():
         h, ref = _fp8_case(n, k, m, wid=124, swiglu=swiglu, x=x)
         for i in range(m):
             assert_float_parity(h[i], ref[i], f"fp8 row {i} swiglu={swiglu}")
+        # the same rows one at a time (m = 1 has its own kernels at k = 2048)
+        for i in range(m):
+            h1, ref1 = _fp8_case(n, k, 1, wid=124, swiglu=swiglu, x=x[i:i + 1])
+            assert_float_parity(h1[0], ref1[0], f"fp8 m=1 row {i} swiglu={swiglu}")
+    assert gu.device_error() == 0
+
+
+@pytest.mark.parametrize("n", [1, 7, 2433, 5000])
+def test_fp8_gate_up_k2048_row_counts(n):
+    """K = 2048 at m = 1 (a warp per row pair, two pairs in flight): a single
+    row, a few, one more than one pass of the grid's warps, several passes."""
+    h, ref = _fp8_case(n, 2048, 1, wid=126, swiglu=True)
+    assert_float_parity(h, ref, f"fp8 gate/up {n}x2048")
     assert gu.device_error() == 0
