@@ -276,11 +276,11 @@ def cpu_baseline(target_s: float = 8.0):
 # capture of the current kernel on the same shape (K = 2048, N = 11008, m = 1);
 # set an entry back to None whenever its kernel changes.
 DRAM_TRAFFIC = {
-    "swiglu_mxfp4_m1x_kernel": 24154624,
+    "swiglu_mxfp4_m1r_kernel": 24148480,
     "swiglu_bf16_kernel": 92470784,
 }
 # The kernel that serves the batch-1 MXFP4 gate/up layer at K = 2048.
-MXFP4_M1_KERNEL = "swiglu_mxfp4_m1x_kernel"
+MXFP4_M1_KERNEL = "swiglu_mxfp4_m1r_kernel"
 
 # The other workloads' kernels: (kernel(s), bound, DRAM read + write of one
 # launch (summed over a call's kernels) from an ncu capture of the current
