@@ -225,8 +225,9 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
 }
 
 // ---------------------------------------------------------------------------
-// m = 1 at K = 2048 (SmolLM3-3B's gate/up), records in registers: three
-// CTAs of 8 warps per SM (80 registers a thread), warp w of the grid takes
+// m = 1 with K fixed at compile time, records in registers (SmolLM3-3B's
+// gate/up, K = 2048: three CTAs of 8 warps per SM, 80 registers a thread;
+// Phi-4's, K = 5120: two, 96 registers), warp w of the grid takes
 // records w, w + (warps of the grid), ...; each lane keeps the one record it
 // is about to compute in registers (its two 16-byte code chunks of each
 // matrix, their scale bytes and the postscales, all requested with plain
@@ -239,10 +240,10 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
 // the SmolLM3 layer (rotating copies): 5.67 us, against 6.46 for the ring
 // kernel; 4 CTAs per SM (64 registers) 6.15, 3 CTAs with 2 records in
 // flight 6.30, 2 CTAs 6.30 to 6.46, 1 CTA 8.35 to 8.82, and 3 CTAs with a
-// fourth slot left free for the next kernel's CTA 6.93.
+// fourth slot left free for the next kernel's CTA 6.93.  Phi-4's layer
+// (K = 5120, N = 17920): 19.8 us against 21.2 for the ring kernel.
 // ---------------------------------------------------------------------------
 constexpr int kRegWarps = 8;
-constexpr int kRegCtasPerSm = 3;
 
 template <int NB>
 struct RegRecord {
@@ -251,12 +252,12 @@ struct RegRecord {
   float2 post;              // (post_g, post_u), the same for every lane
 };
 
-template <int KC>
-__global__ void __launch_bounds__(kRegWarps * 32, kRegCtasPerSm)
+template <int KC, int CTAS>  // CTAS: CTAs per SM (the register budget of a record)
+__global__ void __launch_bounds__(kRegWarps * 32, CTAS)
     swiglu_mxfp4_m1r_kernel(const uint8_t* __restrict__ packed, int n,
                             const uint16_t* __restrict__ x, uint16_t* __restrict__ h) {
   constexpr int THREADS = kRegWarps * 32;
-  static_assert(KC % 1024 == 0 && KC / 8 == THREADS, "x staged in one pass of the CTA");
+  static_assert(KC % 1024 == 0, "whole warps in the x staging loop");
   constexpr int NB = KC / 1024;
   __shared__ __align__(16) uint4 xs[KC / 8];  // f16 x, chunk-major (as the ring kernel)
   __shared__ float xinv[KC / 32];             // 2^-s of each x block
@@ -282,8 +283,8 @@ __global__ void __launch_bounds__(kRegWarps * 32, kRegCtasPerSm)
   if (nitems > 0) load(R, gw);  // weights do not depend on the previous kernel
   pdl_wait_prior_grid();
 
-  {  // x: one coherent read per CTA, each 32-block prescaled by its own 2^s
-    const int c = threadIdx.x;  // 16-byte chunk c = 4 b + q of x
+  // x: one coherent read per CTA, each 32-block prescaled by its own 2^s
+  for (int c = threadIdx.x; c < KC / 8; c += THREADS) {  // 16-byte chunk c = 4 b + q of x
     const uint4 v = ld_global_v4_hint(reinterpret_cast<const uint4*>(x) + c, l2_evict_last_policy());
     float mx = fmaxf(fmaxf(fmaxf(fabsf(bf16_bits_to_f32(v.x & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.x >> 16))),
                            fmaxf(fabsf(bf16_bits_to_f32(v.y & 0xFFFFu)), fabsf(bf16_bits_to_f32(v.y >> 16)))),
@@ -333,10 +334,10 @@ __global__ void __launch_bounds__(kRegWarps * 32, kRegCtasPerSm)
   }
 }
 
-template <int KC>
+template <int KC, int CTAS>
 cudaError_t run_m1r(const DeviceInfo& di, const uint8_t* packed, int n, const uint16_t* x,
                     uint16_t* h, cudaStream_t s, bool pdl) {
-  int grid = kRegCtasPerSm * di.sms;
+  int grid = CTAS * di.sms;
   const int need = (n + kRegWarps - 1) / kRegWarps;
   if (grid > need) grid = need;
   cudaLaunchConfig_t cfg = {};
@@ -348,7 +349,7 @@ cudaError_t run_m1r(const DeviceInfo& di, const uint8_t* packed, int n, const ui
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, swiglu_mxfp4_m1r_kernel<KC>, packed, n, x, h);
+  return cudaLaunchKernelEx(&cfg, swiglu_mxfp4_m1r_kernel<KC, CTAS>, packed, n, x, h);
 }
 
 // ---------------------------------------------------------------------------
@@ -572,12 +573,13 @@ cudaError_t launch_swiglu_mxfp4_cc(const uint8_t* packed, int n, int k, const ui
   const DeviceInfo* di = device_info();
   if (!di) return cudaErrorNoDevice;
   if (m == 1) {
-    // K of the gate/up layers of the models the library serves get kernels
-    // with K fixed (SmolLM3-3B's 2048: records in registers; Phi-4's 5120:
-    // the ring kernel); every other K takes the runtime-K ring kernel, without
-    // per-block bounds tests when K % 1024 == 0.
-    if (k == 2048) return run_m1r<2048>(*di, packed, n, x, h, s, pdl);
-    if (k == 5120) return run_m1x<5, 1, TT_M1_WARPS, 5120, true>(*di, packed, n, k, x, h, s, pdl);
+    // K of the gate/up layers of the models the library serves get the
+    // register kernel with K fixed (SmolLM3-3B's 2048 at three CTAs per SM,
+    // Phi-4's 5120, whose records take more registers, at two); every other K
+    // takes the runtime-K ring kernel, without per-block bounds tests when
+    // K % 1024 == 0.
+    if (k == 2048) return run_m1r<2048, 3>(*di, packed, n, x, h, s, pdl);
+    if (k == 5120) return run_m1r<5120, 2>(*di, packed, n, x, h, s, pdl);
     if (k % 1024 == 0) {
       switch (k / 1024) {
         case 1: return run_m1x<1, TT_M1_RPC, TT_M1_WARPS, 0, true>(*di, packed, n, k, x, h, s, pdl);
