@@ -286,9 +286,9 @@ MXFP4_M1_KERNEL = "swiglu_mxfp4_m1r_kernel"
 # launch (summed over a call's kernels) from an ncu capture of the current
 # code on the same shape, or None where no such capture exists).
 WORKLOAD_KERNELS = {
-    "fp8_gate_up_k2048_n11008_m1": ("fp8_swiglu_k_kernel", "hbm", None),
+    "fp8_gate_up_k2048_n11008_m1": ("fp8_swiglu_k_kernel", "hbm", 45198848),
     "bf16_down_k11008_n2048_m1": ("bf16_rows_k_kernel", "hbm", 45119744),
-    "fp8_down_k11008_n2048_m1": ("fp8_pair_kernel", "hbm", None),
+    "fp8_down_k11008_n2048_m1": ("fp8_pair_kernel", "hbm", 22598656),
     "mxfp4_down_k11008_n2048_m1": ("mxfp4_rows_k_kernel", "hbm", 12020736),
     "gptoss20b_int4_qkv_k2880_n5120_g128": ("int4_mma_kernel", "hbm", 7704832),
     "gptoss20b_moe_h2880_e32_top4": ("moe_fused_kernel", "hbm", 53517824),
