@@ -28,9 +28,10 @@
 // tile, whose padding rows TMA fills with zeros) into a ring of raw slots.
 // Warp 16 allocates tensor memory, waits for each stage and issues the
 // tcgen05.mma (M=128, N, K=16) x 4 per matrix per stage, then tcgen05.commit
-// releases the stage.  Warps 0-3 finally read D with tcgen05.ld (warp w owns
-// TMEM lanes 32w..32w+31 = rows), scale by 2^X_row and the postscale, apply
-// silu(g)*u and store bf16.
+// releases the stage.  The 16 producer warps finally read D with tcgen05.ld
+// (warp w owns TMEM lanes 32(w%4)..+31 = rows and a quarter of the batch
+// columns), scale by 2^X_row and the postscale, apply silu(g)*u and store
+// bf16.
 
 #include "common.cuh"
 #include "launch.h"
@@ -49,6 +50,7 @@ constexpr int kGroupWarps = TT_TC_GROUP_WARPS;  // one producer group: 8 warps =
 #endif
 constexpr int kGroups = TT_TC_GROUPS;            // groups decode k-tiles in turn
 constexpr int kProdWarps = kGroupWarps * kGroups;
+static_assert(kProdWarps == 16, "the epilogue splits the batch columns over 4 warp quads");
 constexpr int kMmaWarp = kProdWarps;             // tensor memory + MMA issue
 constexpr int kTmaWarp = kProdWarps + 1;         // TMA loads
 constexpr int kThreads = (kProdWarps + 2) * 32;  // 576 with two groups
@@ -64,6 +66,7 @@ constexpr int kTileK = 64;                      // f16: 128 bytes = one swizzle 
 #endif
 constexpr int kStages = TT_TC_STAGES;  // decoded A/B stages
 constexpr int kScaleBatch = 20;        // scale words per thread per load batch
+constexpr int kScanDepth = 16;         // x-scan loads per lane in flight
 
 // ---- tcgen05 / descriptor helpers ------------------------------------------
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
@@ -132,6 +135,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 4 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float* v) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
@@ -374,19 +388,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dependency wait; the epilogue divides the factor back out.
     pdl_wait_prior_grid();  // x is produced by the previous kernel
     {
+      // kScanDepth loads per lane in flight: a 5120-wide row is two round
+      // trips (four at a time it was five, and 9-10 us at m = 64)
       const int nch = k >> 3;  // 16-byte chunks per row
       for (int row = warp; row < P.np; row += kProdWarps) {
         float mx = 0.f;
         if (row < m) {
           const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * k);
-#pragma unroll 4
-          for (int c = lane; c < nch; c += 32) {
-            const uint4 v = __ldcg(xr + c);
-            const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+          for (int c0 = lane; c0 < nch; c0 += 32 * kScanDepth) {
+            uint4 v[kScanDepth];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(vw[e] & 0xFFFFu)),
-                                   fabsf(bf16_bits_to_f32(vw[e] >> 16))));
+            for (int u = 0; u < kScanDepth; ++u) {
+              const int c = c0 + 32 * u;
+              v[u] = c < nch ? __ldcg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < kScanDepth; ++u) {
+              const uint32_t vw[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(vw[e] & 0xFFFFu)),
+                                     fabsf(bf16_bits_to_f32(vw[e] >> 16))));
+            }
           }
           mx = warp_max(mx);
         }
@@ -482,9 +505,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) flag_error(err, kErrTimeout);
   }
 
-  // ---------------- epilogue: warps 0-3, thread = row ----------------
-  if (warp < 4) {
-    const int r = threadIdx.x;
+  // ---------------- epilogue: the 16 producer warps ----------------
+  // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (its rows, thread = row) and
+  // the w / 4-th quarter of the batch columns, 4 columns per load (one warp
+  // quad per column quarter: at m = 64 the 4-warp epilogue took ~9 us).
+  if (warp < kProdWarps) {
+    const int q = warp & 3, cq = warp >> 2;
+    const int r = q * 32 + lane;
     const bool ok = mbar_wait_bounded(smem_u32(done), 0u);
     fence_after_sync();
     if (ok) {
@@ -494,14 +521,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float pg = *reinterpret_cast<const float*>(rec + L.post);
       const float pu = *reinterpret_cast<const float*>(rec + L.post + 4);
       const int eg = sxr[r], eu = sxr[kTileRows + r];
-      const uint32_t lane_base = uint32_t(warp * 32) << 16;
-      for (int c0 = 0; c0 < P.np; c0 += 16) {
-        float g[16], u[16];
-        tmem_ld16(tmem + lane_base + uint32_t(c0), g);
-        tmem_ld16(tmem + lane_base + uint32_t(P.np + c0), u);
+      const uint32_t lane_base = uint32_t(q * 32) << 16;
+      const int cpq = P.np / (kProdWarps / 4);  // columns per quarter (np % 16 == 0)
+      for (int c0 = cq * cpq; c0 < (cq + 1) * cpq; c0 += 4) {
+        float g[4], u[4];
+        tmem_ld4(tmem + lane_base + uint32_t(c0), g);
+        tmem_ld4(tmem + lane_base + uint32_t(P.np + c0), u);
         if (nr < n) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
+          for (int i = 0; i < 4; ++i) {
             const int mm = c0 + i;
             if (mm < m) {
               // exact power-of-two factors: the row's block exponent and the
