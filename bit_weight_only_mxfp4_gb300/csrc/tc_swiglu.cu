@@ -65,6 +65,8 @@ constexpr int kTileK = 64;                      // f16: 128 bytes = one swizzle 
 #define TT_TC_MAX_RAW 4
 #endif
 constexpr int kStages = TT_TC_STAGES;  // decoded A/B stages
+constexpr int kACol = 128;             // first TMEM column of the A tiles (after D_g, D_u)
+static_assert(kACol + 64 * kStages <= 512, "A stages fit the SM's 512 TMEM columns");
 constexpr int kScaleBatch = 20;        // scale words per thread per load batch
 constexpr int kScanDepth = 16;         // x-scan loads per lane in flight
 
@@ -99,13 +101,15 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t accumulate) {
+// D (+)= A B with A read from tensor memory (row i of A in TMEM lane i, two
+// f16 of consecutive k per 32-bit column) and B from shared memory.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -122,19 +126,19 @@ __device__ __forceinline__ void fence_before_sync() {
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
+// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes (thread i of
+// the warp writes lane 32 (warp % 4) + i).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // 4 consecutive fp32 columns of this warp's 32 TMEM lanes.
@@ -192,16 +196,14 @@ struct TcPlan {
   int np;          // MMA N (batch rows padded to 16)
   int nblk;        // k / 32
   int sstride;     // bytes per row of block scales in shared memory (odd word count)
-  int a_bytes;     // one A tile: 128 x 128 B
-  int stage_bytes; // A_g + A_u + B, 1024-aligned
+  int stage_bytes; // one B (x) tile, 1024-aligned; the A tiles live in tensor memory
   int raw_bytes;   // one raw slot: gate 4 KB + up 4 KB + x np x 128 B
   int off_raw, off_scale, off_xr, off_sx, off_bar, off_tmem, total;
   __host__ __device__ TcPlan(int m, int k, int nraw_) : nraw(nraw_) {
     np = (m + 15) & ~15;
     nblk = k >> 5;
     sstride = 4 * ((nblk >> 1) | 1);
-    a_bytes = kTileRows * 128;
-    stage_bytes = (2 * a_bytes + np * 128 + 1023) & ~1023;
+    stage_bytes = (np * 128 + 1023) & ~1023;
     raw_bytes = (2 * kTileRows * 32 + np * 128 + 127) & ~127;
     off_raw = kStages * stage_bytes;
     off_scale = off_raw + nraw * raw_bytes;
@@ -236,7 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + P.off_tmem);
   const int n0 = blockIdx.x * kTileRows;
   const int nkt = k / kTileK;
-  const uint32_t tcols = (2 * P.np <= 32) ? 32u : (2 * P.np <= 64 ? 64u : 128u);
+  // tensor memory: D_g, D_u in columns [0, 2 np), np <= 64; the decoded A
+  // tiles of stage s at kACol + 64 s (gate 32 columns, then up 32)
+  const uint32_t tcols = 512u;
   const uint32_t raw_tx = uint32_t(2 * kTileRows * 32 + P.np * 128);
 
   auto raw_slot = [&](int d) { return sbase + uint32_t(P.off_raw + d * P.raw_bytes); };
@@ -352,16 +356,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait_bounded(smem_u32(&a_full[s]), uint32_t((kt / kStages) & 1));
         if (!ok) break;
         fence_after_sync();
-        const uint32_t ag = sbase + uint32_t(s * P.stage_bytes);
-        const uint32_t au = ag + uint32_t(P.a_bytes);
-        const uint32_t bx = au + uint32_t(P.a_bytes);
+        const uint32_t ag = tmem + uint32_t(kACol + 64 * s);  // lane 0, column of A_g
+        const uint32_t au = ag + 32u;
+        const uint32_t bx = sbase + uint32_t(s * P.stage_bytes);
 #pragma unroll
         for (int kk = 0; kk < kTileK / 16; ++kk) {
           const uint32_t koff = uint32_t(kk * 32);  // 16 f16 = 32 bytes along K
           const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
-          mma_f16(tmem, smem_desc_sw128(ag + koff), smem_desc_sw128(bx + koff), idesc, acc);
-          mma_f16(tmem + uint32_t(P.np), smem_desc_sw128(au + koff), smem_desc_sw128(bx + koff),
-                  idesc, acc);
+          mma_f16_ta(tmem, ag + uint32_t(kk * 8), smem_desc_sw128(bx + koff), idesc, acc);
+          mma_f16_ta(tmem + uint32_t(P.np), au + uint32_t(kk * 8), smem_desc_sw128(bx + koff),
+                     idesc, acc);
         }
         mma_commit(smem_u32(&a_empty[s]));  // stage s free once these MMAs are done
       }
@@ -378,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kParts = kGroupWarps * 32 / kTileRows;  // 2 (8 warps) or 4 (16 warps)
     constexpr int kPartK = kTileK / kParts;              // weights per part: 32 or 16
     constexpr int kPartWords = kPartK / 8;                // 32-bit code words per part
+    static_assert(kPartWords == 4, "a part is 16 TMEM columns (one 32x32b.x16 store)");
     const int g = warp / kGroupWarps;
     const int t = threadIdx.x - g * kGroupWarps * 32, r = t & 127, part = t >> 7;
     const int xg = sxr[r], xu = sxr[kTileRows + r];
@@ -425,7 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int kt = g; kt < nkt; kt += kGroups) {
       const int s = kt % kStages, d = kt % P.nraw;
-      ok = mbar_wait_bounded(smem_u32(&raw_full[d]), uint32_t((kt / P.nraw) & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&raw_full[d]),
+                                                     uint32_t((kt / P.nraw) & 1)));
       if (!ok) break;
       const uint8_t* rw = base + P.off_raw + d * P.raw_bytes;
       // Every load of the k-tile first, into registers: the stores below go
@@ -464,23 +470,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (kt >= kStages)
-        ok = mbar_wait_bounded(smem_u32(&a_empty[s]), uint32_t(((kt / kStages) - 1) & 1));
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&a_empty[s]),
+                                                       uint32_t(((kt / kStages) - 1) & 1)));
       if (!ok) break;
-      uint8_t* stage = base + s * P.stage_bytes;
-      // W: kPartK weights per matrix -> kPartWords swizzled 16-byte chunks each
+      fence_after_sync();  // the stage's MMAs (committed) are done with its A columns
+      uint8_t* stage = base + s * P.stage_bytes;  // the B (x) tile
+      // W: kPartK = 32 weights per matrix -> 16 f16x2 columns of this row's
+      // TMEM lane (k = 32 part .. 32 part + 31 of the k-tile, two per column)
+      const uint32_t arow =
+          tmem + (uint32_t(r & ~31) << 16) + uint32_t(kACol + 64 * s + 16 * part);
 #pragma unroll
       for (int mat = 0; mat < 2; ++mat) {
         const uint32_t f =
             sb[mat] == 255u ? 0x7E007E00u : pow2_f16x2(int(sb[mat]) - 127 - (mat ? xu : xg));
-        uint8_t* a = stage + mat * P.a_bytes;
+        uint32_t av[4 * kPartWords];
 #pragma unroll
         for (int q = 0; q < kPartWords; ++q) {
           uint32_t h0, h1, h2, h3;
           e2m1x8_to_f16x2(w[mat][q], h0, h1, h2, h3);
-          *reinterpret_cast<uint4*>(a + sw128(r, part * kPartWords + q)) =
-              make_uint4(hmul2(h0, f), hmul2(h1, f), hmul2(h2, f), hmul2(h3, f));
+          av[4 * q + 0] = hmul2(h0, f);
+          av[4 * q + 1] = hmul2(h1, f);
+          av[4 * q + 2] = hmul2(h2, f);
+          av[4 * q + 3] = hmul2(h3, f);
         }
+        tmem_st16(arow + uint32_t(32 * mat), av);
       }
+      tmem_wait_st();
       // x: bf16 * 2^sxs[row] -> f16, within range by the choice of sxs
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -494,11 +509,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 4; ++e)
             o[e] = pack_f16x2_scaled(bf16_bits_to_f32(vw[e] & 0xFFFFu),
                                      bf16_bits_to_f32(vw[e] >> 16), two_s);  // exact
-          *reinterpret_cast<uint4*>(stage + 2 * P.a_bytes + sw128(row, piece)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(stage + sw128(row, piece)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
-      fence_proxy_async();
+      fence_proxy_async();  // x stores -> the MMA's shared-memory reads
+      fence_before_sync();  // A stores -> the MMA
       mbar_arrive(smem_u32(&a_full[s]));
       mbar_arrive(smem_u32(&raw_empty[d]));
     }
