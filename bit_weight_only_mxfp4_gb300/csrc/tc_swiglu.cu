@@ -65,7 +65,7 @@ constexpr int kTileK = 64;                      // f16: 128 bytes = one swizzle 
 #define TT_TC_MAX_RAW 4
 #endif
 constexpr int kStages = TT_TC_STAGES;  // decoded A/B stages
-constexpr int kACol = 128;             // first TMEM column of the A tiles (after D_g, D_u)
+constexpr int kACol = 256;             // first TMEM column of the A tiles (after the D sets)
 static_assert(kACol + 64 * kStages <= 512, "A stages fit the SM's 512 TMEM columns");
 constexpr int kScaleBatch = 20;        // scale words per thread per load batch
 constexpr int kScanDepth = 16;         // x-scan loads per lane in flight
@@ -238,9 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + P.off_tmem);
   const int n0 = blockIdx.x * kTileRows;
   const int nkt = k / kTileK;
-  // tensor memory: D_g, D_u in columns [0, 2 np), np <= 64; the decoded A
-  // tiles of stage s at kACol + 64 s (gate 32 columns, then up 32)
+  // tensor memory: nacc independent accumulator sets, set j's D_g at column
+  // 2 j np and D_u at (2 j + 1) np (2 nacc np <= 256); the decoded A tiles of
+  // stage s at kACol + 64 s (gate 32 columns, then up 32).  The k-steps of a
+  // k-tile go to the sets in turn, so consecutive MMAs never wait on each
+  // other's accumulator; the epilogue adds the sets in a fixed order.
   const uint32_t tcols = 512u;
+  const int nacc = P.np <= 32 ? 4 : 2;
   const uint32_t raw_tx = uint32_t(2 * kTileRows * 32 + P.np * 128);
 
   auto raw_slot = [&](int d) { return sbase + uint32_t(P.off_raw + d * P.raw_bytes); };
@@ -362,10 +366,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kTileK / 16; ++kk) {
           const uint32_t koff = uint32_t(kk * 32);  // 16 f16 = 32 bytes along K
-          const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
-          mma_f16_ta(tmem, ag + uint32_t(kk * 8), smem_desc_sw128(bx + koff), idesc, acc);
-          mma_f16_ta(tmem + uint32_t(P.np), au + uint32_t(kk * 8), smem_desc_sw128(bx + koff),
-                     idesc, acc);
+          const int j = kk % nacc;  // accumulator set
+          const uint32_t acc = (kt > 0 || kk >= nacc) ? 1u : 0u;
+          const uint32_t dg = tmem + uint32_t(2 * j * P.np);
+          mma_f16_ta(dg, ag + uint32_t(kk * 8), smem_desc_sw128(bx + koff), idesc, acc);
+          mma_f16_ta(dg + uint32_t(P.np), au + uint32_t(kk * 8), smem_desc_sw128(bx + koff), idesc,
+                     acc);
         }
         mma_commit(smem_u32(&a_empty[s]));  // stage s free once these MMAs are done
       }
@@ -542,6 +548,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         float g[4], u[4];
         tmem_ld4(tmem + lane_base + uint32_t(c0), g);
         tmem_ld4(tmem + lane_base + uint32_t(P.np + c0), u);
+        for (int j = 1; j < nacc; ++j) {  // the other accumulator sets, in order
+          float gj[4], uj[4];
+          tmem_ld4(tmem + lane_base + uint32_t(2 * j * P.np + c0), gj);
+          tmem_ld4(tmem + lane_base + uint32_t((2 * j + 1) * P.np + c0), uj);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            g[i] += gj[i];
+            u[i] += uj[i];
+          }
+        }
         if (nr < n) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
