@@ -51,9 +51,10 @@ constexpr int kGroupWarps = TT_TC_GROUP_WARPS;  // one producer group: 8 warps =
 constexpr int kGroups = TT_TC_GROUPS;            // groups decode k-tiles in turn
 constexpr int kProdWarps = kGroupWarps * kGroups;
 static_assert(kProdWarps == 16, "the epilogue splits the batch columns over 4 warp quads");
-constexpr int kMmaWarp = kProdWarps;             // tensor memory + MMA issue
+constexpr int kMmaWarp = kProdWarps;             // tensor memory + the gate MMAs
 constexpr int kTmaWarp = kProdWarps + 1;         // TMA loads
-constexpr int kThreads = (kProdWarps + 2) * 32;  // 576 with two groups
+constexpr int kMmaWarpU = kProdWarps + 2;        // the up MMAs
+constexpr int kThreads = (kProdWarps + 3) * 32;  // 608 with two groups
 constexpr int kTileRows = 128;
 constexpr int kTileK = 64;                      // f16: 128 bytes = one swizzle row
 // Decoded A/B stages and the most raw k-tiles in flight: 3 and 4 measured
@@ -252,13 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == kTmaWarp * 32) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&a_full[s]), kGroupWarps * 32);
-      mbar_init(smem_u32(&a_empty[s]), 1);
+      mbar_init(smem_u32(&a_empty[s]), 2);  // one commit per MMA issuer
     }
     for (int d = 0; d < P.nraw; ++d) {
       mbar_init(smem_u32(&raw_full[d]), 1);
       mbar_init(smem_u32(&raw_empty[d]), kGroupWarps * 32);
     }
-    mbar_init(smem_u32(done), 1);
+    mbar_init(smem_u32(done), 2);
     fence_mbar_init();
     // weights do not depend on the previous kernel: request the first
     // k-tiles while the CTA loads its block scales (x follows the wait)
@@ -350,9 +351,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) flag_error(err, kErrTimeout);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == kMmaWarp || warp == kMmaWarpU) {
+    // ---------------- MMA issuers: gate (kMmaWarp) and up (kMmaWarpU) ----
+    // Two issuing threads, one per matrix: a thread issuing tcgen05.mma back
+    // to back was the k-tile loop's pace (~40 ns an instruction).
     if (lane == 0) {
+      const int mat = warp == kMmaWarpU ? 1 : 0;
       const uint32_t idesc = idesc_f16(P.np);
       bool ok = true;
       for (int kt = 0; kt < nkt && ok; ++kt) {
@@ -360,24 +364,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait_bounded(smem_u32(&a_full[s]), uint32_t((kt / kStages) & 1));
         if (!ok) break;
         fence_after_sync();
-        const uint32_t ag = tmem + uint32_t(kACol + 64 * s);  // lane 0, column of A_g
-        const uint32_t au = ag + 32u;
+        // lane 0, the column of this matrix's A tile of stage s
+        const uint32_t a = tmem + uint32_t(kACol + 64 * s + 32 * mat);
         const uint32_t bx = sbase + uint32_t(s * P.stage_bytes);
 #pragma unroll
         for (int kk = 0; kk < kTileK / 16; ++kk) {
           const uint32_t koff = uint32_t(kk * 32);  // 16 f16 = 32 bytes along K
           const int j = kk % nacc;  // accumulator set
           const uint32_t acc = (kt > 0 || kk >= nacc) ? 1u : 0u;
-          const uint32_t dg = tmem + uint32_t(2 * j * P.np);
-          mma_f16_ta(dg, ag + uint32_t(kk * 8), smem_desc_sw128(bx + koff), idesc, acc);
-          mma_f16_ta(dg + uint32_t(P.np), au + uint32_t(kk * 8), smem_desc_sw128(bx + koff), idesc,
-                     acc);
+          mma_f16_ta(tmem + uint32_t((2 * j + mat) * P.np), a + uint32_t(kk * 8),
+                     smem_desc_sw128(bx + koff), idesc, acc);
         }
-        mma_commit(smem_u32(&a_empty[s]));  // stage s free once these MMAs are done
+        mma_commit(smem_u32(&a_empty[s]));  // stage s free once both issuers' MMAs are done
       }
       if (!ok) flag_error(err, kErrTimeout);
       mma_commit(smem_u32(done));
-      // Wait for our own MMAs before tensor memory can be released.
+      // Wait for both issuers' MMAs before tensor memory can be released.
       (void)mbar_wait_bounded(smem_u32(done), 0u);
     }
     __syncwarp();
