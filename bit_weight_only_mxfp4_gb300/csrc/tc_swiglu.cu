@@ -57,13 +57,14 @@ constexpr int kMmaWarpU = kProdWarps + 2;        // the up MMAs
 constexpr int kThreads = (kProdWarps + 3) * 32;  // 608 with two groups
 constexpr int kTileRows = 128;
 constexpr int kTileK = 64;                      // f16: 128 bytes = one swizzle row
-// Decoded A/B stages and the most raw k-tiles in flight: 3 and 4 measured
-// best at m = 16..64 (2 stages, 8 raw slots or 3 producer groups were slower).
+// Decoded stages and the most raw k-tiles in flight (4 stages fill the 512
+// TMEM columns with the accumulator sets; 4 / 6 measured 45.1 / 57.3 us at
+// m = 16 / 64 against 46.4 / 58.0 with 3 / 4, 8 raw slots no further gain).
 #ifndef TT_TC_STAGES
-#define TT_TC_STAGES 3
+#define TT_TC_STAGES 4
 #endif
 #ifndef TT_TC_MAX_RAW
-#define TT_TC_MAX_RAW 4
+#define TT_TC_MAX_RAW 6
 #endif
 constexpr int kStages = TT_TC_STAGES;  // decoded A/B stages
 constexpr int kACol = 256;             // first TMEM column of the A tiles (after the D sets)
@@ -188,6 +189,43 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 // Barrier among the producer warps only (warps 0 .. kProdWarps-1).
 __device__ __forceinline__ void producer_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kProdWarps * 32) : "memory");
+}
+
+// Largest |x| of rows warp + kProdWarps i (i < NA) over all of K, into
+// mx[i] (every lane): the rows' loads interleaved, kScanDepth per lane in
+// flight.
+template <int NA>
+__device__ __forceinline__ void scan_x_rows(const uint16_t* __restrict__ x, int k, int warp,
+                                            int lane, float* mx) {
+  constexpr int kPer = kScanDepth / NA;  // chunks per row and lane per round trip
+  const int nch = k >> 3;                // 16-byte chunks per row
+  float a[NA];
+#pragma unroll
+  for (int i = 0; i < NA; ++i) a[i] = 0.f;
+  for (int c0 = lane; c0 < nch; c0 += 32 * kPer) {
+    uint4 v[NA][kPer];
+#pragma unroll
+    for (int i = 0; i < NA; ++i) {
+      const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)(warp + kProdWarps * i) * k);
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int c = c0 + 32 * u;
+        v[i][u] = c < nch ? __ldcg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NA; ++i)
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const uint32_t vw[4] = {v[i][u].x, v[i][u].y, v[i][u].z, v[i][u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          a[i] = fmaxf(a[i], fmaxf(fabsf(bf16_bits_to_f32(vw[e] & 0xFFFFu)),
+                                   fabsf(bf16_bits_to_f32(vw[e] >> 16))));
+      }
+  }
+#pragma unroll
+  for (int i = 0; i < NA; ++i) mx[i] = warp_max(a[i]);
 }
 
 // Shared-memory plan of one CTA (offsets from a 1024-aligned base).
@@ -401,32 +439,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dependency wait; the epilogue divides the factor back out.
     pdl_wait_prior_grid();  // x is produced by the previous kernel
     {
-      // kScanDepth loads per lane in flight: a 5120-wide row is two round
-      // trips (four at a time it was five, and 9-10 us at m = 64)
-      const int nch = k >> 3;  // 16-byte chunks per row
-      for (int row = warp; row < P.np; row += kProdWarps) {
-        float mx = 0.f;
-        if (row < m) {
-          const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * k);
-          for (int c0 = lane; c0 < nch; c0 += 32 * kScanDepth) {
-            uint4 v[kScanDepth];
+      // Warp w scans its x rows (w, w + 16, w + 32, w + 48 below m) together,
+      // kScanDepth loads per lane in flight across them: two round trips per
+      // 5120-wide row at m <= 16, five for four rows at m = 64 (row by row,
+      // four loads at a time, it was twenty, ~10 us).
+      const int na = warp < m ? min(4, (m - warp + kProdWarps - 1) / kProdWarps) : 0;
+      float mxr[4] = {0.f, 0.f, 0.f, 0.f};
+      switch (na) {
+        case 1: scan_x_rows<1>(x, k, warp, lane, mxr); break;
+        case 2: scan_x_rows<2>(x, k, warp, lane, mxr); break;
+        case 3: scan_x_rows<3>(x, k, warp, lane, mxr); break;
+        case 4: scan_x_rows<4>(x, k, warp, lane, mxr); break;
+        default: break;
+      }
 #pragma unroll
-            for (int u = 0; u < kScanDepth; ++u) {
-              const int c = c0 + 32 * u;
-              v[u] = c < nch ? __ldcg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int u = 0; u < kScanDepth; ++u) {
-              const uint32_t vw[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(vw[e] & 0xFFFFu)),
-                                     fabsf(bf16_bits_to_f32(vw[e] >> 16))));
-            }
-          }
-          mx = warp_max(mx);
-        }
-        if (lane == 0) xmax[row] = __float_as_uint(mx);
+      for (int i = 0; i < 4; ++i) {
+        const int row = warp + kProdWarps * i;
+        if (lane == 0 && row < P.np) xmax[row] = __float_as_uint(mxr[i]);
       }
     }
     producer_bar_sync();
