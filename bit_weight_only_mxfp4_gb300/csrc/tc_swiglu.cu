@@ -4,34 +4,39 @@
 // From a few batch rows on, the gate/up product is a dense contraction
 // (config: Phi-4 sizes, K = 5120, N = 17920) whose cost on CUDA cores grows
 // with m (one fp32 FMA per weight and batch row), so it runs on the
-// 5th-generation tensor cores, where m = 4..16 cost the same.  The pages' prior art is Triton's tl.dot_scaled over the selected
-// experts, with fast_math off because lossy accumulation broke the MoE
+// 5th-generation tensor cores, where m = 4..16 cost the same.  The pages'
+// prior art is Triton's tl.dot_scaled over the selected experts, with fast_math off because lossy accumulation broke the MoE
 // trajectory (stardance.hackclub.com/projects/29750, MoE drift devlog); here
 // the products are exact and accumulate in fp32 in tensor memory.
 //
 // Layout of the computation (swap-AB): one CTA owns 128 output rows (gate
 // rows n0..n0+127 and the matching up rows) and all m batch rows.
-//   A = W tile   [128 rows x 64 k]  f16, K-major, 128-byte swizzle
-//   B = x tile   [N     x 64 k]     f16, K-major, 128-byte swizzle, N = m
-//                                    rounded up to 16 (pad rows are zero)
-//   D_g, D_u     [128 x N] fp32 in tensor memory (2N columns)
+//   A = W tile   [128 rows x 64 k]  f16 in tensor memory: row i in TMEM lane
+//                                    i, two f16 of consecutive k per column
+//   B = x tile   [N     x 64 k]     f16 in shared memory, K-major, 128-byte
+//                                    swizzle, N = m rounded up to 16 (pad rows
+//                                    are zero)
+//   D_g, D_u     [128 x N] fp32 in tensor memory, in 2 or 4 accumulator sets
+//                (the 4 k-steps of a k-tile go to the sets in turn, so
+//                back-to-back MMAs do not wait on one accumulator)
 // Warps 0-15 produce, in two groups of 8 that take the k-tiles in turn:
 // thread t of a group decodes half a k-tile (one 32-weight block) of row
 // t % 128 for gate and up: cvt.rn.f16x2.e2m1x2, then an exact HMUL2 by
 // 2^(X_block - X_row) where X_row is the row's largest block exponent (so the
-// f16 values stay in range and exact), stored in the swizzled layout; and
-// converts its share of the x tile to f16 after an exact power-of-two
-// prescale per x row that puts the row's largest |x| (over all of K, read
-// once per CTA) in [2^14, 2^15), so no finite input leaves f16's range.
-// Warp 17 brings each k-tile in with three TMA loads (gate codes 128 x 32 B,
-// up codes 128 x 32 B, both strided by the packed record size, and the x
-// tile, whose padding rows TMA fills with zeros) into a ring of raw slots.
-// Warp 16 allocates tensor memory, waits for each stage and issues the
-// tcgen05.mma (M=128, N, K=16) x 4 per matrix per stage, then tcgen05.commit
-// releases the stage.  The 16 producer warps finally read D with tcgen05.ld
-// (warp w owns TMEM lanes 32(w%4)..+31 = rows and a quarter of the batch
-// columns), scale by 2^X_row and the postscale, apply silu(g)*u and store
-// bf16.
+// f16 values stay in range and exact), stored with tcgen05.st into its row's
+// TMEM lane; and converts its share of the x tile to f16 after an exact
+// power-of-two prescale per x row that puts the row's largest |x| (over all
+// of K, read once per CTA) in [2^14, 2^15), so no finite input leaves f16's
+// range.  Warp 17 brings each k-tile in with three TMA loads (gate codes
+// 128 x 32 B, up codes 128 x 32 B, both strided by the packed record size,
+// and the x tile, whose padding rows TMA fills with zeros) into a ring of raw
+// slots.  Warp 16 allocates tensor memory; warps 16 (gate) and 18 (up) wait
+// for each stage and issue the tcgen05.mma (M=128, N, K=16, A from TMEM) x 4
+// per matrix per stage, then tcgen05.commit releases the stage.  The 16
+// producer warps finally read D with tcgen05.ld (warp w owns TMEM lanes
+// 32(w%4)..+31 = rows and a quarter of the batch columns), add the
+// accumulator sets in order, scale by 2^X_row and the postscale, apply
+// silu(g)*u and store bf16.
 
 #include "common.cuh"
 #include "launch.h"
