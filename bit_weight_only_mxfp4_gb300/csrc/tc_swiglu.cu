@@ -5,9 +5,10 @@
 // (config: Phi-4 sizes, K = 5120, N = 17920) whose cost on CUDA cores grows
 // with m (one fp32 FMA per weight and batch row), so it runs on the
 // 5th-generation tensor cores, where m = 4..16 cost the same.  The pages'
-// prior art is Triton's tl.dot_scaled over the selected experts, with fast_math off because lossy accumulation broke the MoE
-// trajectory (stardance.hackclub.com/projects/29750, MoE drift devlog); here
-// the products are exact and accumulate in fp32 in tensor memory.
+// prior art is Triton's tl.dot_scaled over the selected experts, with
+// fast_math off because lossy accumulation broke the MoE trajectory
+// (stardance.hackclub.com/projects/29750, MoE drift devlog); here the
+// products are exact and accumulate in fp32 in tensor memory.
 //
 // Layout of the computation (swap-AB): one CTA owns 128 output rows (gate
 // rows n0..n0+127 and the matching up rows) and all m batch rows.
