@@ -57,6 +57,7 @@ constexpr int kGroupWarps = TT_TC_GROUP_WARPS;  // one producer group: 8 warps =
 constexpr int kGroups = TT_TC_GROUPS;            // groups decode k-tiles in turn
 constexpr int kProdWarps = kGroupWarps * kGroups;
 static_assert(kProdWarps == 16, "the epilogue splits the batch columns over 4 warp quads");
+static_assert(kGroupWarps * 32 >= 128, "a producer group covers the tile's 128 rows");
 constexpr int kMmaWarp = kProdWarps;             // tensor memory + the gate MMAs
 constexpr int kTmaWarp = kProdWarps + 1;         // TMA loads
 constexpr int kMmaWarpU = kProdWarps + 2;        // the up MMAs
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kParts = kGroupWarps * 32 / kTileRows;  // 2 (8 warps) or 4 (16 warps)
     constexpr int kPartK = kTileK / kParts;              // weights per part: 32 or 16
     constexpr int kPartWords = kPartK / 8;                // 32-bit code words per part
-    static_assert(kPartWords == 4, "a part is 16 TMEM columns (one 32x32b.x16 store)");
+    static_assert(kPartWords == 4 || kPartWords == 8, "a part is 16 or 32 TMEM columns");
     const int g = warp / kGroupWarps;
     const int t = threadIdx.x - g * kGroupWarps * 32, r = t & 127, part = t >> 7;
     const int xg = sxr[r], xu = sxr[kTileRows + r];
@@ -482,11 +483,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       // load back.  Only the stores wait for the stage to be free.  The raw
       // slot is released after the stores, which consume every loaded value,
       // so no copy into the slot can overtake a load from it.
-      uint32_t w[2][kPartWords], sb[2];
+      constexpr int kPB = (kPartK + 31) / 32;  // 32-blocks per part
+      uint32_t w[2][kPartWords], sb[2][kPB];
 #pragma unroll
       for (int mat = 0; mat < 2; ++mat) {
         const uint8_t* src = rw + mat * 4096 + r * 32 + part * (kPartK / 2);
-        if constexpr (kPartWords == 4) {
+        if constexpr (kPartWords == 8) {
+          const uint4 c0 = *reinterpret_cast<const uint4*>(src);
+          const uint4 c1 = *reinterpret_cast<const uint4*>(src + 16);
+          w[mat][0] = c0.x;
+          w[mat][1] = c0.y;
+          w[mat][2] = c0.z;
+          w[mat][3] = c0.w;
+          w[mat][4] = c1.x;
+          w[mat][5] = c1.y;
+          w[mat][6] = c1.z;
+          w[mat][7] = c1.w;
+        } else if constexpr (kPartWords == 4) {
           const uint4 c = *reinterpret_cast<const uint4*>(src);
           w[mat][0] = c.x;
           w[mat][1] = c.y;
@@ -497,12 +510,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           w[mat][0] = c.x;
           w[mat][1] = c.y;
         }
-        sb[mat] = sscale[r * P.sstride + mat * P.nblk + kt * 2 + (part * kPartK) / 32];
-      }
-      uint4 xv[2];
-      int xe[2];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
+        for (int pb = 0; pb < kPB; ++pb)
+          sb[mat][pb] = sscale[r * P.sstride + mat * P.nblk + kt * 2 + (part * kPartK) / 32 + pb];
+      }
+      constexpr int kXJ = 64 * 8 / (kGroupWarps * 32);  // x pieces per thread (np <= 64)
+      uint4 xv[kXJ];
+      int xe[kXJ];
+#pragma unroll
+      for (int j = 0; j < kXJ; ++j) {
         const int c = t + j * kGroupWarps * 32;  // row c / 8, 16-byte piece c % 8
         const int row = c >> 3, piece = c & 7;
         xv[j] = make_uint4(0u, 0u, 0u, 0u);
@@ -521,14 +537,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // W: kPartK = 32 weights per matrix -> 16 f16x2 columns of this row's
       // TMEM lane (k = 32 part .. 32 part + 31 of the k-tile, two per column)
       const uint32_t arow =
-          tmem + (uint32_t(r & ~31) << 16) + uint32_t(kACol + 64 * s + 16 * part);
+          tmem + (uint32_t(r & ~31) << 16) + uint32_t(kACol + 64 * s + (kPartK / 2) * part);
 #pragma unroll
       for (int mat = 0; mat < 2; ++mat) {
-        const uint32_t f =
-            sb[mat] == 255u ? 0x7E007E00u : pow2_f16x2(int(sb[mat]) - 127 - (mat ? xu : xg));
         uint32_t av[4 * kPartWords];
 #pragma unroll
         for (int q = 0; q < kPartWords; ++q) {
+          const uint32_t sbq = sb[mat][q / 4];  // 4 code words per 32-block
+          const uint32_t f =
+              sbq == 255u ? 0x7E007E00u : pow2_f16x2(int(sbq) - 127 - (mat ? xu : xg));
           uint32_t h0, h1, h2, h3;
           e2m1x8_to_f16x2(w[mat][q], h0, h1, h2, h3);
           av[4 * q + 0] = hmul2(h0, f);
@@ -536,12 +553,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           av[4 * q + 2] = hmul2(h2, f);
           av[4 * q + 3] = hmul2(h3, f);
         }
-        tmem_st16(arow + uint32_t(32 * mat), av);
+#pragma unroll
+        for (int h = 0; h < kPartWords / 4; ++h)
+          tmem_st16(arow + uint32_t(32 * mat + 16 * h), av + 16 * h);
       }
       tmem_wait_st();
       // x: bf16 * 2^sxs[row] -> f16, within range by the choice of sxs
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
+      for (int j = 0; j < kXJ; ++j) {
         const int c = t + j * kGroupWarps * 32;
         const int row = c >> 3, piece = c & 7;
         if (row < P.np) {
