@@ -534,8 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       fence_after_sync();  // the stage's MMAs (committed) are done with its A columns
       uint8_t* stage = base + s * P.stage_bytes;  // the B (x) tile
-      // W: kPartK = 32 weights per matrix -> 16 f16x2 columns of this row's
-      // TMEM lane (k = 32 part .. 32 part + 31 of the k-tile, two per column)
+      // W: kPartK weights per matrix -> kPartK / 2 f16x2 columns of this row's
+      // TMEM lane (k = kPartK part .. kPartK (part + 1) - 1 of the k-tile, two
+      // per column), each code word scaled by its own 32-block's factor
       const uint32_t arow =
           tmem + (uint32_t(r & ~31) << 16) + uint32_t(kACol + 64 * s + (kPartK / 2) * part);
 #pragma unroll
