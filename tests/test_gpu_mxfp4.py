@@ -137,6 +137,9 @@ def _swiglu_case(n, k, m, postscale=True, wid=92, layer=0):
     # tcgen05 tensor-core path (m >= 9, k % 64 == 0); ragged row tiles
     (128, 128, 16, True), (130, 2048, 16, True), (300, 2880, 32, False), (256, 5120, 64, True),
     (77, 1024, 9, True), (129, 4096, 40, True), (1000, 768, 63, True),
+    # wide K on tcgen05: the block-scale area takes most of shared memory,
+    # so fewer raw k-tiles are in flight (three at m = 64, k = 16384)
+    (70, 16384, 16, True), (130, 12288, 40, False), (33, 16384, 64, True),
 ])
 def test_swiglu_matvec_shapes(n, k, m, post):
     h, ref, _, _ = _swiglu_case(n, k, m, post)
