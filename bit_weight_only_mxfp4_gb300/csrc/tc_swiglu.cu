@@ -432,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- producers: decode W, convert x ----------------
     // group g decodes k-tiles g, g + kGroups, ...; thread t of the group owns
     // part t / 128 of the k-tile (kPartK weights) of row t % 128
-    constexpr int kParts = kGroupWarps * 32 / kTileRows;  // 2 (8 warps) or 4 (16 warps)
-    constexpr int kPartK = kTileK / kParts;              // weights per part: 32 or 16
+    constexpr int kParts = kGroupWarps * 32 / kTileRows;  // 2 (8 warps) or 1 (4 warps)
+    constexpr int kPartK = kTileK / kParts;              // weights per part: 32 or 64
     constexpr int kPartWords = kPartK / 8;                // 32-bit code words per part
     static_assert(kPartWords == 4 || kPartWords == 8, "a part is 16 or 32 TMEM columns");
     const int g = warp / kGroupWarps;
@@ -442,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Each x row gets the exact power-of-two prescale 2^sxs[i] that puts its
     // largest |x| over the whole row in [2^14, 2^15): every finite value then
     // fits f16 and keeps its bits down to 2^-28 of the row's max.  The
-    // producer warps scan x once (a warp per row, all of K) after the
-    // dependency wait; the epilogue divides the factor back out.
+    // producer warps scan x once (all of K) after the dependency wait; the
+    // epilogue divides the factor back out.
     pdl_wait_prior_grid();  // x is produced by the previous kernel
     {
       // Warp w scans its x rows (w, w + 16, w + 32, w + 48 below m) together,
